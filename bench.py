@@ -1,0 +1,346 @@
+"""Benchmark of DSpark sequential Markov draft sampling on one GB300.
+
+A step is one whole Markov call of the DeepSeek-V4.1-shaped workload
+(V=129280, r=256, 8 request rows of which 2 are padding, N=8 draft
+positions, Gumbel mode): the noise kernel plus the persistent chain kernel,
+over inputs already resident in HBM.  L2 is flushed (a 256 MB write) before
+every timed step and the flush is not timed.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gpus N > 1 (one process per GPU under torch.distributed.run) every
+rank runs an independent replica of the workload: the path has no exchange
+step, so there is no collective; value is the tokens of all ranks over the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the plain C definition of the method)
+on this machine's host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft tokens/s and µs per N-step Markov call; % of GB300 HBM roofline"
+UNIT = "draft tokens/s"
+WORKLOAD_CFG = 2
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_deepseek_traffic.json")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "draft_token_markov_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic():
+    """DRAM bytes per chain launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+        if t.get("source_hash") == _kernel_source_hash():
+            return int(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(seconds_hint: float = 20.0):
+    """Time the oracle on a bounded sample of the workload: one call over the
+    workload's first live row (all N positions), repeated while the total
+    stays near seconds_hint.  Returns (tokens/s, sample description, cores)."""
+    import numpy as np
+    import oracle
+    from draft_token_markov_gb300 import workloads as W
+    w = W.CONFIGS[WORKLOAD_CFG]
+    head, embed = W.make_weights(w)
+    inp = W.make_call(w)
+    hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
+    live = [b for b in range(w.rows) if int(inp["row_state_idx"][b]) >= 0]
+    b0 = live[0]
+    idx = np.full(w.rows, -1, dtype=np.int64)
+    idx[b0] = b0
+    cores = os.cpu_count() or 1
+    base = oracle.bf16_bits(inp["base"])
+    args = (base, hb, eb, inp["anchor"].numpy(), inp["temperature"].numpy(),
+            inp["seeds"].numpy(), idx, w.mode)
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.chain(*args, nthreads=cores)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el * (calls + 1) / calls > seconds_hint or calls >= 50:
+            break
+    tokens = calls * w.steps
+    return tokens / el, (f"{calls} oracle call(s) of the {w.name} workload restricted to one "
+                         f"live row ({w.steps} draft tokens each), OpenMP over vocab ids"), cores
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    vals = []
+    desc = cores = None
+    for _ in range(args.warmup):
+        cpu_oracle_sample(2.0)
+    for _ in range(args.steps):
+        v, desc, cores = cpu_oracle_sample(8.0)
+        vals.append(v)
+    value = statistics.mean(vals)
+    from draft_token_markov_gb300 import workloads as W
+    w = W.CONFIGS[WORKLOAD_CFG]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.steps / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, shaped like the pages' DeepSeek-V4.1 Markov head)",
+        "config": {"workload": w.name, "sample": "one live row per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from draft_token_markov_gb300 import api
+    from draft_token_markov_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.CONFIGS[WORKLOAD_CFG]
+    head, embed = W.make_weights(w)
+    inp = W.make_call(w)
+    head, embed = head.to(dev), embed.to(dev)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    plan = api.Plan(w.vocab, w.rank, w.steps, w.rows, device=local)
+    R, N, V = w.rows, w.steps, w.vocab
+    toks = torch.full((R, N), -1, dtype=torch.int64, device=dev)
+    cache = torch.empty((R, N, V), dtype=torch.bfloat16, device=dev)
+    live = int((inp["row_state_idx"] >= 0).sum())
+    tokens_per_step = live * N
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    L = api.lib()
+
+    def step(evs=None):
+        # the noise kernel, then the chain; events between them time the chain
+        if evs:
+            evs[0].record(stream)
+        api.markov_noise_fork(plan, d["seeds"], d["temperature"], d["row_state_idx"], stream)
+        api.markov_noise_join(plan, stream)
+        if evs:
+            evs[1].record(stream)
+        api.markov_chain_sample(plan, d["base"], head, embed, d["anchor"], d["temperature"],
+                                d["seeds"], d["row_state_idx"], w.mode, w.mult, w.cap, toks,
+                                cache, stream)
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = api.markov_plan_status(plan)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    launches_per_step = plan.query(api.Q_LAST_LAUNCHES) + 1   # + the forked noise kernel
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            flush.fill_(k & 0xFF)
+            step(ev[k])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = api.markov_plan_status(plan)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    chain_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+
+    # end to end: host (pinned) inputs copied in, tokens copied out, per step
+    h_in = {k: v.pin_memory() for k, v in inp.items()}
+    h_tok = torch.empty((R, N), dtype=torch.int64).pin_memory()
+    e2e_ms = []
+    for k in range(max(3, min(args.steps, 50)) + 3):
+        flush.fill_(k & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for key in d:
+            d[key].copy_(h_in[key], non_blocking=True)
+        step()
+        h_tok.copy_(toks, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if k >= 3:
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_tok.numel() * h_tok.element_size()
+
+    peak, peak_kind = _peaks()
+    alg_bytes = W.algorithmic_bytes(w)
+    chain_avg_s = statistics.mean(chain_ms) / 1000.0
+    achieved = alg_bytes / chain_avg_s / 1e9
+    traffic = _traffic()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, cores = cpu_oracle_sample(args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+    ms_per_step = total_ms / args.steps
+    value = tokens_per_step * world * args.steps / (total_ms / 1000.0)
+    e2e_step = statistics.mean(e2e_ms)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded, shaped like the pages' DeepSeek-V4.1 Markov head; "
+                "random weights)",
+        "config": {"workload": w.name, "rows": R, "live_rows": live, "vocab": V, "rank": w.rank,
+                   "steps_per_call": N, "mode": "gumbel", "l2": "flushed before every step",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
+                        "p99": sorted(step_ms)[min(len(step_ms) - 1,
+                                                   int(0.99 * len(step_ms)))] * 1000.0,
+                        "chain_kernel_median": statistics.median(chain_ms) * 1000.0},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "chain_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": tokens_per_step / (e2e_step / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_step},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

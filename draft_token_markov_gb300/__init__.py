@@ -5,13 +5,14 @@ The compute path is the CUDA library built from ``csrc/`` (C ABI declared in
 package does not load the library: ``api`` loads it on first use and raises
 if it is missing, so a missing build fails loudly instead of falling back.
 """
+import importlib
+
 from . import workloads  # noqa: F401  (pure input generation, no arithmetic)
 
 __all__ = ["workloads", "api"]
 
 
 def __getattr__(name):
-    if name == "api":
-        from . import api
-        return api
+    if name in ("api", "build"):
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

@@ -1,0 +1,66 @@
+// internal.h -- structures shared by the C-ABI host code and the kernels.
+#pragma once
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace dtm {
+
+constexpr int kMaxSteps = 16;          // draft positions a plan may take
+constexpr int kMaxVocab = 262144;      // vocabulary bound
+constexpr int kMaxRows = 256;          // rows a plan may take
+constexpr int kChainRows = 8;          // rows of one chain launch (MMA N = 8)
+constexpr int kChainThreads = 512;     // threads of a chain CTA (one CTA per SM)
+constexpr int kBatchThreads = 256;
+constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
+constexpr int kKeyPad = 16;            // u64 slots per CTA-key block are padded to 128 B
+
+// The output-logit transform (muse_spark markov page, FusedMarkovParams):
+// multiplier and cap rounded to fp32, inv_cap = fp32(1) / fp32(cap).
+struct Transform {
+    int has_transform;
+    int has_cap;
+    float mult;
+    float cap;
+    float inv_cap;
+};
+
+// Everything one sample call passes to its kernels.
+struct SampleArgs {
+    const uint16_t *base;
+    int64_t base_s0, base_s1;
+    const uint16_t *head;
+    const uint16_t *embed;
+    const int32_t *anchor;
+    const float *temperature;
+    const int64_t *seeds;
+    const int64_t *row_state_idx;
+    int rows, V, r, N, mode;
+    Transform tf;
+    int64_t *tokens;
+    int64_t tok_s0;
+    uint16_t *cache;
+    int64_t cache_s0, cache_s1;
+    const float *noise;        // [rows * N, V] fp32 Gumbel noise (Gumbel mode)
+    int64_t noise_s0;          // row stride of the noise, in floats
+    // plan scratch
+    uint64_t *keys;            // cross-CTA key / partial slots
+    uint64_t *sums;            // cross-CTA inverse-CDF sums
+    uint32_t *bar_count;       // grid barrier counter
+    uint32_t *bar_base;        // the counter's value at the start of a launch
+    uint32_t *status;          // [2]: sticky device status, where it happened
+    uint64_t timeout_ns;
+    int grid;                  // persistent grid size (chain) or vocab blocks (batch)
+};
+
+// Kernel launchers (return the CUDA error of the launch).
+cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
+                         const int64_t *row_state_idx, int rows, int N, int V, float *out,
+                         int64_t out_s0, int mode_gumbel_only, cudaStream_t stream);
+cudaError_t launch_device_math(int fn, const float *x, float *y, int64_t n, cudaStream_t s);
+cudaError_t chain_occupancy(int *blocks_per_sm);
+cudaError_t launch_chain(const SampleArgs &a, cudaStream_t stream);
+cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches);
+int batch_blocks(int V);
+
+}  // namespace dtm

@@ -1,0 +1,347 @@
+// markov_abi.cu -- host side of the C ABI declared in include/markov.h:
+// plan creation (all scratch allocated once), argument validation (the
+// conditions the sharded_markov page's unsupported_reason and sample()
+// assert), path dispatch (the persistent chain up to 8 rows, the
+// per-position kernels above), the optional side-stream noise fork, and the
+// sticky device status.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/markov.h"
+#include "internal.h"
+
+using namespace dtm;
+
+struct markov_plan {
+    markov_desc d;
+    int sm_count = 0;
+    int chain_occ = 0;            // chain CTAs per SM
+    int chain_grid = 0;
+    int batch_grid = 0;
+    float *noise = nullptr;       // [max_rows * N, V]
+    int64_t noise_s0 = 0;
+    uint64_t *keys = nullptr;
+    uint64_t *sums = nullptr;
+    uint32_t *ctrl = nullptr;     // [0] barrier count, [1] barrier base, [2..3] status
+    size_t keys_n = 0;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_noise = nullptr;
+    int noise_state = 0;          // 0 none, 1 forked, 2 forked and joined
+    int forked_rows = 0;
+    markov_path path = MARKOV_PATH_AUTO;
+    int last_launches = 0;
+    int last_path = 0;
+};
+
+namespace {
+
+// Makes the plan's device current for the duration of a call and restores
+// the caller's device afterwards.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+
+bool valid_rank(int r) { return r == 64 || r == 128 || r == 256; }
+
+void free_plan(markov_plan *p) {
+    if (!p) return;
+    if (p->noise) cudaFree(p->noise);
+    if (p->keys) cudaFree(p->keys);
+    if (p->sums) cudaFree(p->sums);
+    if (p->ctrl) cudaFree(p->ctrl);
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_noise) cudaEventDestroy(p->ev_noise);
+    if (p->side) cudaStreamDestroy(p->side);
+    delete p;
+}
+
+Transform make_transform(float mult, float cap) {
+    Transform tf{};
+    tf.mult = mult;
+    tf.has_cap = cap > 0.0f;
+    tf.cap = tf.has_cap ? cap : 1.0f;
+    tf.inv_cap = tf.has_cap ? 1.0f / tf.cap : 1.0f;   // fp32(1) / fp32(cap)
+    tf.has_transform = (mult != 1.0f) || tf.has_cap;
+    return tf;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *markov_status_string(markov_status s) {
+    switch (s) {
+        case MARKOV_OK: return "ok";
+        case MARKOV_EINVAL: return "invalid argument";
+        case MARKOV_EUNSUPPORTED: return "unsupported configuration";
+        case MARKOV_ECUDA: return "CUDA runtime error";
+        case MARKOV_ETIMEOUT: return "an in-kernel bounded wait timed out";
+        case MARKOV_ENOTRESIDENT: return "persistent grid cannot be co-resident";
+        case MARKOV_EDEVICE: return "device error or unusable device";
+    }
+    return "unknown status";
+}
+
+markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
+    if (!out) return MARKOV_EINVAL;
+    *out = nullptr;
+    if (!desc) return MARKOV_EINVAL;
+    const markov_desc d = *desc;
+    if (d.vocab <= 0 || d.vocab % kTile != 0 || d.vocab > kMaxVocab) return MARKOV_EINVAL;
+    if (!valid_rank(d.rank)) return MARKOV_EINVAL;
+    if (d.num_steps < 1 || d.num_steps > kMaxSteps) return MARKOV_EINVAL;
+    if (d.max_rows < 1 || d.max_rows > kMaxRows) return MARKOV_EINVAL;
+    if (d.timeout_ms < 0) return MARKOV_EINVAL;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || d.device < 0 || d.device >= ndev)
+        return MARKOV_EDEVICE;
+    DeviceGuard guard(d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, d.device) != cudaSuccess) return MARKOV_EDEVICE;
+    if (prop.major < 10) return MARKOV_EUNSUPPORTED;    // the kernels are built for sm_103a
+    if (!prop.cooperativeLaunch) return MARKOV_EUNSUPPORTED;
+
+    markov_plan *p = new (std::nothrow) markov_plan();
+    if (!p) return MARKOV_ECUDA;
+    p->d = d;
+    if (p->d.timeout_ms == 0) p->d.timeout_ms = 100;
+    p->sm_count = prop.multiProcessorCount;
+    if (chain_occupancy(&p->chain_occ) != cudaSuccess) { free_plan(p); return MARKOV_ECUDA; }
+    const int ntiles = d.vocab / kTile;
+    int g = ntiles / (kChainThreads / 32);
+    if (g < 1) g = 1;
+    if (g > p->sm_count * p->chain_occ) g = p->sm_count * p->chain_occ;
+    p->chain_grid = g;
+    p->batch_grid = batch_blocks(d.vocab);
+
+    const int Gp = (p->chain_grid + kKeyPad - 1) / kKeyPad * kKeyPad;
+    size_t chain_keys = (size_t)kMaxSteps * 2 * kChainRows * Gp;
+    size_t batch_keys = (size_t)d.max_rows * p->batch_grid;
+    p->keys_n = chain_keys > batch_keys ? chain_keys : batch_keys;
+    p->noise_s0 = d.vocab;
+    const size_t noise_bytes = (size_t)d.max_rows * d.num_steps * d.vocab * sizeof(float);
+    if (cudaMalloc(&p->noise, noise_bytes) != cudaSuccess ||
+        cudaMalloc(&p->keys, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->sums, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->ctrl, 8 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->keys, 0, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_noise, cudaEventDisableTiming) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        free_plan(p);
+        return MARKOV_ECUDA;
+    }
+    *out = p;
+    return MARKOV_OK;
+}
+
+void markov_plan_destroy(markov_plan *p) {
+    if (!p) return;
+    DeviceGuard guard(p->d.device);
+    cudaDeviceSynchronize();
+    free_plan(p);
+}
+
+int32_t markov_chain_max_rows(const markov_plan *p) {
+    if (!p) return -1;
+    return p->d.max_rows < kChainRows ? p->d.max_rows : kChainRows;
+}
+
+markov_status markov_plan_set_path(markov_plan *p, markov_path path) {
+    if (!p) return MARKOV_EINVAL;
+    if (path != MARKOV_PATH_AUTO && path != MARKOV_PATH_CHAIN && path != MARKOV_PATH_BATCH)
+        return MARKOV_EINVAL;
+    p->path = path;
+    return MARKOV_OK;
+}
+
+markov_status markov_noise_fork(markov_plan *p, const int64_t *seeds, const float *temperature,
+                                const int64_t *row_state_idx, int32_t rows, void *stream) {
+    if (!p || !seeds || !temperature || !row_state_idx) return MARKOV_EINVAL;
+    if (rows < 1 || rows > p->d.max_rows) return MARKOV_EINVAL;
+    DeviceGuard guard(p->d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    cudaStream_t main = (cudaStream_t)stream;
+    if (cudaEventRecord(p->ev_fork, main) != cudaSuccess ||
+        cudaStreamWaitEvent(p->side, p->ev_fork, 0) != cudaSuccess)
+        return MARKOV_ECUDA;
+    if (launch_noise(seeds, temperature, row_state_idx, rows, p->d.num_steps, p->d.vocab,
+                     p->noise, p->noise_s0, 1, p->side) != cudaSuccess)
+        return MARKOV_ECUDA;
+    if (cudaEventRecord(p->ev_noise, p->side) != cudaSuccess) return MARKOV_ECUDA;
+    p->noise_state = 1;
+    p->forked_rows = rows;
+    return MARKOV_OK;
+}
+
+markov_status markov_noise_join(markov_plan *p, void *stream) {
+    if (!p) return MARKOV_EINVAL;
+    if (p->noise_state != 1) return MARKOV_OK;
+    DeviceGuard guard(p->d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    if (cudaStreamWaitEvent((cudaStream_t)stream, p->ev_noise, 0) != cudaSuccess)
+        return MARKOV_ECUDA;
+    p->noise_state = 2;
+    return MARKOV_OK;
+}
+
+markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, int64_t base_s0,
+                                  int64_t base_s1, const uint16_t *head, const uint16_t *embed,
+                                  const int32_t *anchor_tokens, const float *temperature,
+                                  const int64_t *seeds, const int64_t *row_state_idx,
+                                  int32_t rows, markov_mode mode, float output_multiplier,
+                                  float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
+                                  uint16_t *logit_cache, int64_t cache_s0, int64_t cache_s1,
+                                  void *stream) {
+    if (!p) return MARKOV_EINVAL;
+    const int V = p->d.vocab, r = p->d.rank, N = p->d.num_steps;
+    if (!base_logits || !head || !embed || !anchor_tokens || !temperature || !seeds ||
+        !row_state_idx || !draft_tokens || !logit_cache)
+        return MARKOV_EINVAL;
+    if (rows < 1 || rows > p->d.max_rows) return MARKOV_EINVAL;
+    if (mode != MARKOV_GUMBEL && mode != MARKOV_INVCDF) return MARKOV_EINVAL;
+    if (base_s1 < V || base_s0 < (int64_t)(N - 1) * base_s1 + V) return MARKOV_EINVAL;
+    if (cache_s1 < V || cache_s0 < (int64_t)(N - 1) * cache_s1 + V) return MARKOV_EINVAL;
+    if (tok_s0 < N) return MARKOV_EINVAL;
+    // the cache asserts of the sharded_markov page's sample(): 16-byte
+    // aligned pointer and row strides
+    if (!aligned16(logit_cache) || (cache_s0 * 2) % 16 != 0 || (cache_s1 * 2) % 16 != 0)
+        return MARKOV_EINVAL;
+    if (!aligned16(head) || !aligned16(embed)) return MARKOV_EINVAL;
+    if (!std::isfinite(output_multiplier) || std::isnan(soft_cap)) return MARKOV_EINVAL;
+    if (p->noise_state != 0 && p->forked_rows != rows) return MARKOV_EINVAL;
+
+    bool chain = rows <= kChainRows;
+    if (p->path == MARKOV_PATH_CHAIN && !chain) return MARKOV_EUNSUPPORTED;
+    if (p->path == MARKOV_PATH_BATCH) chain = false;
+
+    DeviceGuard guard(p->d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    SampleArgs a{};
+    a.base = base_logits;
+    a.base_s0 = base_s0;
+    a.base_s1 = base_s1;
+    a.head = head;
+    a.embed = embed;
+    a.anchor = anchor_tokens;
+    a.temperature = temperature;
+    a.seeds = seeds;
+    a.row_state_idx = row_state_idx;
+    a.rows = rows;
+    a.V = V;
+    a.r = r;
+    a.N = N;
+    a.mode = (int)mode;
+    a.tf = make_transform(output_multiplier, soft_cap);
+    a.tokens = draft_tokens;
+    a.tok_s0 = tok_s0;
+    a.cache = logit_cache;
+    a.cache_s0 = cache_s0;
+    a.cache_s1 = cache_s1;
+    a.noise = p->noise;
+    a.noise_s0 = p->noise_s0;
+    a.keys = p->keys;
+    a.sums = p->sums;
+    a.bar_count = p->ctrl;
+    a.bar_base = p->ctrl + 1;
+    a.status = p->ctrl + 2;
+    a.timeout_ns = (uint64_t)p->d.timeout_ms * 1000000ull;
+
+    int launches = 0;
+    if (p->noise_state == 1) {
+        // join the forked noise (in inverse-CDF mode it is unused, but the
+        // plan's buffer must not be rewritten while it is being drawn)
+        if (cudaStreamWaitEvent(s, p->ev_noise, 0) != cudaSuccess) return MARKOV_ECUDA;
+    } else if (p->noise_state == 0 && mode == MARKOV_GUMBEL) {
+        if (launch_noise(seeds, temperature, row_state_idx, rows, N, V, p->noise, p->noise_s0, 1,
+                         s) != cudaSuccess)
+            return MARKOV_ECUDA;
+        ++launches;
+    }
+    p->noise_state = 0;
+
+    if (chain) {
+        if (p->chain_occ < 1) return MARKOV_ENOTRESIDENT;
+        a.grid = p->chain_grid;
+        cudaError_t e = launch_chain(a, s);
+        if (e == cudaErrorCooperativeLaunchTooLarge) { cudaGetLastError(); return MARKOV_ENOTRESIDENT; }
+        if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+        ++launches;
+        p->last_path = MARKOV_PATH_CHAIN;
+    } else {
+        a.grid = p->batch_grid;
+        int n = 0;
+        cudaError_t e = launch_batch(a, s, &n);
+        if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+        launches += n;
+        p->last_path = MARKOV_PATH_BATCH;
+    }
+    p->last_launches = launches;
+    return MARKOV_OK;
+}
+
+markov_status markov_plan_status(markov_plan *p) {
+    if (!p) return MARKOV_EINVAL;
+    DeviceGuard guard(p->d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    if (cudaDeviceSynchronize() != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+    uint32_t ctrl[4];
+    if (cudaMemcpy(ctrl, p->ctrl, sizeof(ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MARKOV_ECUDA;
+    if (ctrl[2] == 0u) return MARKOV_OK;
+    // a launch gave up: clear the status and restart the barrier counter
+    if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess) return MARKOV_ECUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MARKOV_ECUDA;
+    return (markov_status)ctrl[2];
+}
+
+markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature,
+                                  const int64_t *row_state_idx, int32_t rows, int32_t num_steps,
+                                  int32_t vocab, float *out, int64_t out_s0, void *stream) {
+    if (!seeds || !temperature || !row_state_idx || !out) return MARKOV_EINVAL;
+    if (rows < 1 || rows > kMaxRows || num_steps < 1 || num_steps > kMaxSteps) return MARKOV_EINVAL;
+    if (vocab < 1 || vocab > kMaxVocab || out_s0 < vocab) return MARKOV_EINVAL;
+    if (launch_noise(seeds, temperature, row_state_idx, rows, num_steps, vocab, out, out_s0, 1,
+                     (cudaStream_t)stream) != cudaSuccess)
+        return MARKOV_ECUDA;
+    return MARKOV_OK;
+}
+
+markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n, void *stream) {
+    if (fn < 0 || fn > 4 || n < 0 || (n > 0 && (!x || !y))) return MARKOV_EINVAL;
+    if (launch_device_math(fn, x, y, n, (cudaStream_t)stream) != cudaSuccess) return MARKOV_ECUDA;
+    return MARKOV_OK;
+}
+
+int64_t markov_plan_query(const markov_plan *p, int32_t key) {
+    if (!p) return -1;
+    switch (key) {
+        case MARKOV_Q_CHAIN_CTAS: return p->chain_grid;
+        case MARKOV_Q_RESIDENT_HEAD_BYTES: return 0;
+        case MARKOV_Q_LAST_LAUNCHES: return p->last_launches;
+        case MARKOV_Q_LAST_PATH: return p->last_path;
+        case MARKOV_Q_SM_COUNT: return p->sm_count;
+    }
+    return -1;
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// noise.cu -- counter-based Gumbel noise, and the device-math probe kernel.
+//
+// The noise of (row b, position i, vocab id v) is -log(-log u) with u the top
+// 23 bits of splitmix64(h_bi ^ v), h_bi = sm(sm(sm(seed_b) ^ b) ^ i).  It
+// depends on the seeds and positions only, never on the chain, so it can be
+// drawn on a side stream before the chain runs (sharded_markov page,
+// fork_noise and _shard_noise_kernel).  The kernel is ALU bound: one 64-bit
+// hash and two logarithms per element; each thread makes 4 consecutive ids
+// and stores them as one 16-byte vector.
+#include "common.cuh"
+
+namespace dtm {
+
+constexpr int kNoiseThreads = 256;
+constexpr int kNoisePerThread = 4;
+
+__global__ void __launch_bounds__(kNoiseThreads)
+noise_kernel(const int64_t *__restrict__ seeds, const float *__restrict__ temperature,
+             const int64_t *__restrict__ row_state_idx, int N, int V, float *__restrict__ out,
+             int64_t out_s0) {
+    const int sample = blockIdx.y;          // b * N + i
+    const int b = sample / N;
+    const int i = sample - b * N;
+    if (row_state_idx[b] < 0 || !samples(temperature[b])) return;
+    const uint64_t hri = dm_row_step_hash((uint64_t)seeds[b], (uint32_t)b, (uint32_t)i);
+    float *dst = out + (int64_t)sample * out_s0;
+    const int stride = gridDim.x * kNoiseThreads * kNoisePerThread;
+    for (int v0 = (blockIdx.x * kNoiseThreads + threadIdx.x) * kNoisePerThread; v0 < V;
+         v0 += stride) {
+        float g[kNoisePerThread];
+#pragma unroll
+        for (int j = 0; j < kNoisePerThread; ++j) g[j] = dm_gumbel(hri, (uint32_t)(v0 + j));
+        if (v0 + kNoisePerThread <= V && ((reinterpret_cast<uintptr_t>(dst + v0) & 15u) == 0u)) {
+            *reinterpret_cast<float4 *>(dst + v0) = make_float4(g[0], g[1], g[2], g[3]);
+        } else {
+            for (int j = 0; j < kNoisePerThread && v0 + j < V; ++j) dst[v0 + j] = g[j];
+        }
+    }
+}
+
+cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
+                         const int64_t *row_state_idx, int rows, int N, int V, float *out,
+                         int64_t out_s0, int /*mode_gumbel_only*/, cudaStream_t stream) {
+    int per_block = kNoiseThreads * kNoisePerThread;
+    int bx = (V + per_block - 1) / per_block;
+    if (bx > 65535) bx = 65535;
+    dim3 grid(bx, rows * N);
+    noise_kernel<<<grid, kNoiseThreads, 0, stream>>>(seeds, temperature, row_state_idx, N, V,
+                                                      out, out_s0);
+    return cudaGetLastError();
+}
+
+__global__ void device_math_kernel(int fn, const float *__restrict__ x, float *__restrict__ y,
+                                   int64_t n) {
+    for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        float v = x[j];
+        float r;
+        switch (fn) {
+            case 0: r = dm_log(v); break;
+            case 1: r = dm_exp(v); break;
+            case 2: r = dm_tanh(v); break;
+            case 3: r = -dm_log(-dm_log(v)); break;
+            default: r = __uint_as_float(dm_bf16_bits(v)); break;
+        }
+        y[j] = r;
+    }
+}
+
+cudaError_t launch_device_math(int fn, const float *x, float *y, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 65536) blocks = 65536;
+    device_math_kernel<<<(unsigned)blocks, 256, 0, s>>>(fn, x, y, n);
+    return cudaGetLastError();
+}
+
+}  // namespace dtm

@@ -1,0 +1,201 @@
+/*
+ * markov.h -- C ABI of the GB300 (sm_103a) library for DSpark sequential
+ * Markov sampling of speculative draft tokens.
+ *
+ * The method (sources: the documentation pages
+ *   "vllm.models.deepseek_v41.nvidia.specialized_decode.sampling.sharded_markov",
+ *   "vllm.models.deepseek_v41.nvidia.ops.fused_markov",
+ *   "vllm.models.muse_spark.nvidia.specialized_decode.runtime.markov"):
+ * for every request row b and draft position i = 0 .. N-1, with p the
+ * anchor token at i = 0 and token i-1 afterwards,
+ *   bias  = bf16(markov_head[V, r] . markov_embed[p])            (fp32 sums)
+ *   l     = bf16(f32(base[b, i]) + f32(bias)), then optionally
+ *           bf16(cap * tanh((l * mult) * (1 / cap)))               (transform)
+ *   cache[b, i] = l;  token[b, i] = Gumbel-max of l / T + gumbel, or inverse
+ *   CDF of softmax(l / T), argmax at T = 0; lowest NaN id first, lowest id
+ *   among equal maxima.
+ * (sharded_markov page, module docstring and "Per call" diagram; fused_markov
+ * page, module docstring; muse_spark markov page, module docstring,
+ * FusedMarkovParams and fused_markov_params.)
+ *
+ * Conventions for every entry point:
+ *   - BF16 tensors are passed as uint16_t bit patterns.
+ *   - "device" pointers must be CUDA device memory of the plan's device;
+ *     "host" pointers are ordinary (preferably pinned) host memory.
+ *   - The caller owns every tensor it passes; the library never frees or
+ *     retains them beyond the call's stream work.  A plan owns only its own
+ *     scratch, allocated once at creation (so CUDA graphs keep addresses).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *     default stream.  Calls enqueue work and return without synchronizing,
+ *     except markov_plan_status.
+ *   - Argument errors are reported synchronously by the return value and
+ *     nothing is launched.  Device-side failures (a bounded wait that timed
+ *     out) are recorded in a sticky device status word that
+ *     markov_plan_status reads; kernels never trap.
+ */
+#ifndef DTM_MARKOV_H
+#define DTM_MARKOV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum markov_status {
+    MARKOV_OK = 0,
+    MARKOV_EINVAL = 1,          /* bad argument: shape, stride, alignment, range */
+    MARKOV_EUNSUPPORTED = 2,    /* valid but outside what this build runs */
+    MARKOV_ECUDA = 3,           /* a CUDA runtime call failed */
+    MARKOV_ETIMEOUT = 4,        /* an in-kernel bounded wait gave up */
+    MARKOV_ENOTRESIDENT = 5,    /* the persistent grid cannot be co-resident */
+    MARKOV_EDEVICE = 6          /* wrong or unusable device */
+} markov_status;
+
+typedef enum markov_mode {
+    MARKOV_GUMBEL = 0,          /* Gumbel-max (sharded_markov page) */
+    MARKOV_INVCDF = 1           /* inverse CDF (fused_markov page) */
+} markov_mode;
+
+typedef enum markov_path {
+    MARKOV_PATH_AUTO = 0,       /* chain up to markov_chain_max_rows rows, else batch */
+    MARKOV_PATH_CHAIN = 1,      /* the persistent single-launch chain kernel */
+    MARKOV_PATH_BATCH = 2       /* per-position kernels (the larger-batch loop) */
+} markov_path;
+
+/* Static configuration of a plan.  vocab % 16 == 0 and vocab <= 262144
+ * (sharded_markov page, unsupported_reason: V divisible by 16 per rank and
+ * bounded); rank a power of two in {64, 128, 256} (muse_spark page,
+ * unsupported: a power-of-two-rank w1); 1 <= num_steps <= 16 (a bound on
+ * draft positions, unsupported_reason); 1 <= max_rows <= 256.
+ * timeout_ms bounds every in-kernel wait (0 selects 100 ms). */
+typedef struct markov_desc {
+    int32_t vocab;
+    int32_t rank;
+    int32_t num_steps;
+    int32_t max_rows;
+    int32_t device;
+    int32_t timeout_ms;
+} markov_desc;
+
+typedef struct markov_plan markov_plan;
+
+/* Validate `desc`, select the device, and allocate every scratch buffer the
+ * plan's calls use (noise [max_rows * N, V] fp32, key and partial-sum slots,
+ * barrier and status words, the side stream and its events).  On success
+ * *out receives the plan; on failure *out is NULL and nothing is leaked.
+ * (sharded_markov page, DSparkShardedMarkovSampler.__init__: persistent
+ * buffers allocated once; fused_markov page, FusedMarkovSampler: scratch
+ * allocated at init so CUDA graphs keep the addresses.) */
+markov_status markov_plan_create(const markov_desc *desc, markov_plan **out);
+
+/* Synchronize the plan's device work and free its scratch.  NULL is a no-op. */
+void markov_plan_destroy(markov_plan *plan);
+
+/* Rows a single chain launch takes: 8 (sharded_markov page, module
+ * docstring: "up to 8 request rows", the MMA columns). */
+int32_t markov_chain_max_rows(const markov_plan *plan);
+
+/* Force the path of later markov_chain_sample calls (testing and
+ * benchmarking); MARKOV_PATH_AUTO restores the default.  EINVAL for an
+ * unknown path; EUNSUPPORTED is returned later by a call whose rows the
+ * forced chain path cannot take. */
+markov_status markov_plan_set_path(markov_plan *plan, markov_path path);
+
+/* Draw this call's Gumbel noise on the plan's side stream, ordered after the
+ * work already enqueued on `stream`; the next markov_chain_sample on the
+ * plan joins it.  seeds [rows] int64, temperature [rows] fp32,
+ * row_state_idx [rows] int64 are device pointers and must be the arrays the
+ * sample call passes.  The noise depends only on (seed, row, position, vocab
+ * id), never on the chain (sharded_markov page, fork_noise and
+ * _shard_noise_kernel).  Optional: without it the sample call draws the
+ * noise itself on its own stream.  EINVAL if rows > max_rows. */
+markov_status markov_noise_fork(markov_plan *plan, const int64_t *seeds,
+                                const float *temperature, const int64_t *row_state_idx,
+                                int32_t rows, void *stream);
+
+/* Make `stream` wait for the noise of the last markov_noise_fork (the
+ * sharded_markov page's join_noise); the next markov_chain_sample must then
+ * run on this same stream.  A no-op when no fork is pending. */
+markov_status markov_noise_join(markov_plan *plan, void *stream);
+
+/* Draw every live row's N draft tokens and write its logits cache.
+ *   base_logits   device, BF16 [rows, N, V]: element (b, i, v) at
+ *                 b * base_s0 + i * base_s1 + v; last stride 1.
+ *   head, embed   device, BF16 [V, r] contiguous (markov_head / w2 and
+ *                 markov_embed / w1).
+ *   anchor_tokens device, int32 [rows]: each row's previous token at i = 0.
+ *   temperature   device, fp32 [rows]; T > 0 samples, anything else is greedy.
+ *   seeds         device, int64 [rows].
+ *   row_state_idx device, int64 [rows]; < 0 marks a padding row, which is
+ *                 inert: neither its tokens nor its cache are written.
+ *   mode          MARKOV_GUMBEL or MARKOV_INVCDF.
+ *   output_multiplier, soft_cap: the transform; soft_cap <= 0 means none.
+ *                 Both are used as fp32 and inv_cap = fp32(1) / fp32(cap).
+ *   draft_tokens  device, int64 [rows, N], element (b, i) at b * tok_s0 + i.
+ *   logit_cache   device, BF16 [rows, N, V], element (b, i, v) at
+ *                 b * cache_s0 + i * cache_s1 + v; pointer and strides
+ *                 16-byte aligned (sharded_markov page, sample: cache asserts).
+ * Rows up to markov_chain_max_rows take one persistent launch; larger calls
+ * take the per-position kernels (sharded_markov page, module docstring:
+ * larger batches take the fused loop).  EINVAL on a bad shape, stride,
+ * alignment or mode; ENOTRESIDENT if the persistent grid cannot be
+ * co-resident; ECUDA if a launch fails. */
+markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits,
+                                  int64_t base_s0, int64_t base_s1, const uint16_t *head,
+                                  const uint16_t *embed, const int32_t *anchor_tokens,
+                                  const float *temperature, const int64_t *seeds,
+                                  const int64_t *row_state_idx, int32_t rows,
+                                  markov_mode mode, float output_multiplier,
+                                  float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
+                                  uint16_t *logit_cache, int64_t cache_s0,
+                                  int64_t cache_s1, void *stream);
+
+/* Synchronize the plan's device and return (then clear) the sticky device
+ * status: MARKOV_OK, or MARKOV_ETIMEOUT when a bounded wait gave up, in
+ * which case the plan's barrier words are re-zeroed so the next call starts
+ * clean.  ECUDA if the device reports an error. */
+markov_status markov_plan_status(markov_plan *plan);
+
+/* A static English description of a status code. */
+const char *markov_status_string(markov_status status);
+
+/* Gumbel noise, standalone: out[(b * N + i) * out_s0 + v] = -log(-log u) of
+ * (seeds[b], b, i, v) for every live row with temperature > 0, v < V.  Rows
+ * that are padding or greedy are not written.  Device pointers; the same
+ * kernel markov_noise_fork runs (sharded_markov page, _shard_noise_kernel).
+ * out_s0 >= V. */
+markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature,
+                                  const int64_t *row_state_idx, int32_t rows,
+                                  int32_t num_steps, int32_t vocab, float *out,
+                                  int64_t out_s0, void *stream);
+
+/* Evaluate the device's own scalar functions element-wise over n floats
+ * (device pointers): fn 0 natural log, 1 exp, 2 tanh, 3 Gumbel transform
+ * -log(-log x), 4 fp32 -> BF16 round-to-nearest-even (result bits in the
+ * low 16 bits of the output word, read as uint32).  These are the
+ * functions the kernels use; exposed so they can be compared bit for bit with
+ * an independent implementation.  EINVAL for an unknown fn. */
+markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n,
+                                 void *stream);
+
+/* Plan facts for reporting: MARKOV_Q_CHAIN_CTAS (persistent grid size),
+ * MARKOV_Q_RESIDENT_HEAD_BYTES (head bytes the chain kernel keeps on chip
+ * across positions), MARKOV_Q_LAST_LAUNCHES (kernel launches the last
+ * sample call enqueued), MARKOV_Q_LAST_PATH (markov_path it took),
+ * MARKOV_Q_SM_COUNT.  Returns -1 for an unknown key or a NULL plan. */
+enum {
+    MARKOV_Q_CHAIN_CTAS = 0,
+    MARKOV_Q_RESIDENT_HEAD_BYTES = 1,
+    MARKOV_Q_LAST_LAUNCHES = 2,
+    MARKOV_Q_LAST_PATH = 3,
+    MARKOV_Q_SM_COUNT = 4
+};
+int64_t markov_plan_query(const markov_plan *plan, int32_t key);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTM_MARKOV_H */

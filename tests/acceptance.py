@@ -1,0 +1,148 @@
+"""The acceptance rule, checked against the oracle.
+
+  * cache: every element of every live row within 1 BF16 ulp of the oracle
+    (ordered-integer distance, +0 == -0), NaN only where the oracle has NaN;
+  * always: the oracle's selection applied to the GPU's own cache row gives
+    the GPU's token, bit for bit;
+  * tokens: equal to the oracle's, except where the GPU's cache row differs
+    from the oracle's and (Gumbel / greedy) the GPU's token is a contender:
+    nudging each of the two ids' bias by one BF16 ulp either way can bring
+    its key up to the oracle winner's key; (inverse CDF) the GPU token is
+    what the oracle's selection gives on the GPU's cache.  An excused
+    position is reported, and that row's later positions are compared with
+    the oracle rerun from the next position with the GPU's token as the
+    previous token;
+  * padding rows: both outputs still hold the caller's sentinel.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+import oracle
+from oracle import GUMBEL, INVCDF
+
+
+def ordered_bf16(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def is_nan_bf16(bits: np.ndarray) -> np.ndarray:
+    return (bits & 0x7FFF) > 0x7F80
+
+
+def bf16_nudges(bits: int) -> list[int]:
+    """The BF16 value one ulp below, itself, one ulp above (finite inputs)."""
+    o = int(ordered_bf16(np.array([bits], dtype=np.uint16))[0])
+    out = []
+    for d in (-1, 0, 1):
+        q = o + d
+        out.append((q if q >= 0 else (0x8000 | (-q))) & 0xFFFF)
+    return out
+
+
+@dataclass
+class Report:
+    positions: int = 0
+    cache_elems: int = 0
+    cache_ulp_diffs: int = 0
+    excused: list = field(default_factory=list)
+    failures: list = field(default_factory=list)
+
+    def ok(self) -> bool:
+        return not self.failures
+
+    def summary(self) -> str:
+        return (f"positions={self.positions} cache_elems={self.cache_elems} "
+                f"cache_1ulp={self.cache_ulp_diffs} excused={len(self.excused)} "
+                f"failures={self.failures[:5]}")
+
+
+def _key_range(head, embed, base_bits, v, p, T, mode, seed, b, i, tf):
+    bias = oracle.bias_one(head, embed, v, p)
+    keys = []
+    for nb in bf16_nudges(bias):
+        l = oracle.lib().orc_logit(int(base_bits[v]), int(nb), *tf)
+        if not (T > 0):
+            keys.append(float(oracle.bits_to_f32(np.array([l], np.uint16))[0]))
+        else:
+            keys.append(oracle.gumbel_key(l, T, seed, b, i, v))
+    return min(keys), max(keys)
+
+
+def check(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mode: int, mult: float,
+          cap, gpu_tokens: np.ndarray, gpu_cache: np.ndarray, tok_sentinel: int,
+          cache_sentinel: int, nthreads: int = 0) -> Report:
+    base = oracle.bf16_bits(inputs["base"])
+    anchor = inputs["anchor"].numpy()
+    temp = inputs["temperature"].numpy()
+    seeds = inputs["seeds"].numpy()
+    idx = inputs["row_state_idx"].numpy()
+    R, N, V = base.shape
+    o_tok, o_cache = oracle.chain(base, head_bits, embed_bits, anchor, temp, seeds, idx, mode,
+                                  mult, cap, nthreads=nthreads)
+    has_t, m, has_cap, c, inv = oracle.transform_params(mult, cap)
+    tf = (has_t, m, has_cap, c, inv)
+    rep = Report()
+    for b in range(R):
+        if idx[b] < 0:
+            if not (np.all(gpu_tokens[b] == tok_sentinel) and np.all(gpu_cache[b] == cache_sentinel)):
+                rep.failures.append(("padding row written", b))
+            continue
+        ref_tok = o_tok[b].copy()
+        ref_cache = o_cache[b].copy()
+        T = float(temp[b])
+        seed = int(seeds[b])
+        for i in range(N):
+            rep.positions += 1
+            g = gpu_cache[b, i]
+            r_ = ref_cache[i]
+            gn, rn = is_nan_bf16(g), is_nan_bf16(r_)
+            if np.any(gn != rn):
+                rep.failures.append(("cache NaN mismatch", b, i))
+            both = ~gn & ~rn
+            d = np.abs(ordered_bf16(g[both]) - ordered_bf16(r_[both]))
+            rep.cache_elems += int(both.sum())
+            if d.size and d.max() > 1:
+                rep.failures.append(("cache > 1 ulp", b, i, int(d.max())))
+            ndiff = int((d == 1).sum())
+            rep.cache_ulp_diffs += ndiff
+            gt = int(gpu_tokens[b, i])
+            sel, _, _ = oracle.select(g, T, mode, seed, b, i)
+            if sel != gt:
+                rep.failures.append(("selection on GPU cache differs", b, i, sel, gt))
+                continue
+            if gt == int(ref_tok[i]):
+                continue
+            if ndiff == 0:
+                rep.failures.append(("token differs with identical cache", b, i, gt,
+                                     int(ref_tok[i])))
+                continue
+            ot = int(ref_tok[i])
+            p = int(anchor[b]) if i == 0 else int(gpu_tokens[b, i - 1])
+            excuse = None
+            if mode == GUMBEL or not (T > 0):
+                lo_w, _ = _key_range(head_bits, embed_bits, base[b, i], ot, p, T, mode, seed, b, i, tf)
+                _, hi_g = _key_range(head_bits, embed_bits, base[b, i], gt, p, T, mode, seed, b, i, tf)
+                if hi_g >= lo_w:
+                    excuse = ("contender", b, i, gt, ot, float(hi_g - lo_w))
+            else:
+                excuse = ("inverse-cdf on a cache 1 ulp apart", b, i, gt, ot)
+            if excuse is None:
+                rep.failures.append(("token not excusable", b, i, gt, ot))
+                continue
+            rep.excused.append(excuse)
+            if i + 1 < N:
+                idx2 = np.full(R, -1, dtype=np.int64)
+                idx2[b] = idx[b]
+                ss = np.full(R, i + 1, dtype=np.int32)
+                sp = np.zeros(R, dtype=np.int64)
+                sp[b] = gt
+                t2, c2 = oracle.chain(base, head_bits, embed_bits, anchor, temp, seeds, idx2, mode,
+                                      mult, cap, start_step=ss, start_prev=sp, nthreads=nthreads)
+                ref_tok[i + 1:] = t2[b, i + 1:]
+                ref_cache[i + 1:] = c2[b, i + 1:]
+    return rep

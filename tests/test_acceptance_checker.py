@@ -1,0 +1,61 @@
+"""The acceptance checker must accept the oracle's own outputs and reject
+planted mistakes (CPU only: the "GPU" outputs here are the oracle's, edited)."""
+import numpy as np
+
+import oracle
+from draft_token_markov_gb300 import workloads as W
+from tests.acceptance import check
+
+SENT_T, SENT_C = -7, 0xABCD
+
+
+def _run(w):
+    head, embed = W.make_weights(w)
+    inp = W.make_call(w)
+    hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
+    toks = np.full((w.rows, w.steps), SENT_T, dtype=np.int64)
+    cache = np.full((w.rows, w.steps, w.vocab), SENT_C, dtype=np.uint16)
+    toks, cache = oracle.chain(oracle.bf16_bits(inp["base"]), hb, eb, inp["anchor"].numpy(),
+                               inp["temperature"].numpy(), inp["seeds"].numpy(),
+                               inp["row_state_idx"].numpy(), w.mode, w.mult, w.cap,
+                               tokens=toks, cache=cache)
+    return inp, hb, eb, toks, cache
+
+
+def _chk(w, inp, hb, eb, toks, cache):
+    return check(inp, hb, eb, w.mode, w.mult, w.cap, toks, cache, SENT_T, SENT_C)
+
+
+def test_checker_accepts_oracle_and_rejects_mistakes():
+    w = W.small(512, 32, 4, 3, W.GUMBEL, seed=21, padding_rows=(2,), temperatures=(0.0, 1.0))
+    inp, hb, eb, toks, cache = _run(w)
+    assert _chk(w, inp, hb, eb, toks, cache).ok()
+    # a wrong token with an identical cache
+    t2 = toks.copy()
+    t2[0, 1] = (t2[0, 1] + 1) % 512
+    assert not _chk(w, inp, hb, eb, t2, cache).ok()
+    # a cache element 2 ulps away
+    c2 = cache.copy()
+    c2[1, 0, 5] = int(c2[1, 0, 5]) + 2
+    assert not _chk(w, inp, hb, eb, toks, c2).ok()
+    # a padding row written
+    c3 = cache.copy()
+    c3[2, 0, 0] = 0
+    assert not _chk(w, inp, hb, eb, toks, c3).ok()
+    # a 1-ulp cache difference far below the winner is accepted
+    c4 = cache.copy()
+    row = oracle.bits_to_f32(c4[3, 2])
+    j = int(np.argmin(row))
+    c4[3, 2, j] = int(c4[3, 2, j]) + (1 if c4[3, 2, j] < 0x8000 else -1)
+    rep = _chk(w, inp, hb, eb, toks, c4)
+    assert rep.ok() and rep.cache_ulp_diffs == 1
+
+
+def test_checker_inverse_cdf_softcap():
+    w = W.small(400, 64, 3, 4, W.INVCDF, seed=22, mult=0.5, cap=30.0, tie_row=1, nan_row=2,
+                temperatures=(0.7, 1.0))
+    inp, hb, eb, toks, cache = _run(w)
+    assert _chk(w, inp, hb, eb, toks, cache).ok()
+    t2 = toks.copy()
+    t2[0, 3] = (t2[0, 3] + 3) % 400
+    assert not _chk(w, inp, hb, eb, t2, cache).ok()

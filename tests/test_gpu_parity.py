@@ -1,0 +1,197 @@
+"""Parity of the CUDA path (chain and batch) with the oracle under the
+acceptance rule: small shapes spanning several tiles with ragged per-warp and
+per-CTA tails, edge cases, and the five full workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from draft_token_markov_gb300 import workloads as W
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+AUTO, CHAIN, BATCH = 0, 1, 2
+
+SMALL = [
+    W.small(16, 64, 1, 1, W.GUMBEL, seed=1, temperatures=(1.0,)),
+    W.small(272, 64, 3, 4, W.GUMBEL, seed=2),
+    W.small(4144, 128, 8, 5, W.GUMBEL, seed=3, padding_rows=(1, 6), spikes=4),
+    W.small(12000, 256, 5, 3, W.INVCDF, seed=4, mult=0.5, cap=30.0, tie_row=1, nan_row=2,
+            temperatures=(0.7, 1.0)),
+    W.small(2048, 64, 8, 16, W.INVCDF, seed=5, temperatures=(0.0,)),
+    W.small(3008, 256, 8, 3, W.GUMBEL, seed=6, mult=1.5, temperatures=(0.0, 0.6, 1.0)),
+    W.small(5000 - 8, 128, 7, 6, W.INVCDF, seed=7, temperatures=(0.0, 0.5, 1.2),
+            padding_rows=(0,)),
+]
+
+
+def _ids(ws):
+    return [w.name.replace(" ", "_") for w in ws]
+
+
+@pytest.mark.parametrize("path", [CHAIN, BATCH])
+@pytest.mark.parametrize("w", SMALL, ids=_ids(SMALL))
+def test_small_parity(gpu_lib, w, path):
+    inp = W.make_call(w)
+    toks, cache = U.run(gpu_lib, w, inp, path)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+
+
+BATCHES = [
+    W.small(3008, 256, 20, 3, W.GUMBEL, seed=8, padding_rows=(3, 19)),
+    W.small(1024, 128, 70, 2, W.INVCDF, seed=9, temperatures=(0.0, 0.8, 1.0)),
+    W.small(512, 64, 256, 2, W.GUMBEL, seed=10),
+]
+
+
+@pytest.mark.parametrize("w", BATCHES, ids=_ids(BATCHES))
+def test_batch_rows_parity(gpu_lib, w):
+    inp = W.make_call(w)
+    toks, cache = U.run(gpu_lib, w, inp, AUTO)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+
+
+def test_forced_chain_refuses_large_batch(gpu_lib):
+    w = BATCHES[0]
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    plan.set_path(CHAIN)
+    with pytest.raises(gpu_lib.MarkovError) as e:
+        U.run(gpu_lib, w, W.make_call(w), CHAIN, plan=plan)
+    assert e.value.code == 2
+
+
+@pytest.mark.parametrize("path", [CHAIN, BATCH])
+def test_max_vocab_and_steps(gpu_lib, path):
+    w = W.small(262144, 64, 2, 16, W.GUMBEL, seed=11, temperatures=(0.0, 1.0))
+    inp = W.make_call(w)
+    toks, cache = U.run(gpu_lib, w, inp, path)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+
+
+@pytest.mark.parametrize("path", [CHAIN, BATCH])
+def test_infinities_and_empty_rows(gpu_lib, path):
+    # row 0: every logit -inf (inverse CDF takes id 0); row 1: +inf at two
+    # ids (the lowest wins); row 2: a NaN after a +inf (NaN first); row 3:
+    # padding.  No soft cap, so infinities pass through.
+    w = W.small(1024, 64, 4, 2, W.INVCDF, seed=12, temperatures=(1.0,), padding_rows=(3,))
+    inp = W.make_call(w)
+    base = inp["base"].float()
+    base[0] = float("-inf")
+    base[1, :, 700] = float("inf")
+    base[1, :, 300] = float("inf")
+    base[2, :, 50] = float("inf")
+    base[2, :, 900] = float("nan")
+    inp["base"] = base.to(torch.bfloat16)
+    toks, cache = U.run(gpu_lib, w, inp, path)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+    assert toks[0].tolist() == [0, 0]
+    assert toks[1].tolist() == [300, 300]
+    assert toks[2].tolist() == [900, 900]
+    for mode_w in (w.with_(mode=W.GUMBEL),):
+        toks, cache = U.run(gpu_lib, mode_w, inp, path)
+        assert U.check(mode_w, inp, toks, cache).ok()
+        assert toks[1].tolist() == [300, 300] and toks[2].tolist() == [900, 900]
+
+
+def test_closed_form_chain_on_gpu(gpu_lib):
+    # head[v] = c e_{v mod r}, embed[p] = c e_{(p+1) mod r}, zero base, T = 0:
+    # the tokens walk (anchor + 1 + i) mod r.
+    V, r, N = 512, 64, 8
+    head = torch.zeros(V, r)
+    embed = torch.zeros(V, r)
+    for v in range(V):
+        head[v, v % r] = 0.5
+        embed[v, (v + 1) % r] = 0.5
+    w = W.small(V, r, 3, N, W.GUMBEL, seed=13, temperatures=(0.0,))
+    inp = W.make_call(w)
+    inp["base"] = torch.zeros_like(inp["base"])
+    for path in (CHAIN, BATCH):
+        toks, _ = U.run(gpu_lib, w, inp, path, head=head.to(torch.bfloat16).cuda(),
+                        embed=embed.to(torch.bfloat16).cuda())
+        for b in range(3):
+            a = int(inp["anchor"][b])
+            assert toks[b].tolist() == [(a + 1 + i) % r for i in range(N)]
+
+
+def test_forked_noise_and_repeat_are_identical(gpu_lib):
+    w = SMALL[2]
+    inp = W.make_call(w)
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    a = U.run(gpu_lib, w, inp, CHAIN, plan=plan)
+    b = U.run(gpu_lib, w, inp, CHAIN, plan=plan, fork=True)
+    c = U.run(gpu_lib, w, inp, CHAIN, plan=plan)
+    for x, y in ((a, b), (a, c)):
+        assert np.array_equal(x[0], y[0]) and np.array_equal(x[1], y[1])
+    plan.close()
+
+
+def test_repeated_calls_are_deterministic(gpu_lib):
+    w = W.DEEPSEEK.with_(vocab=16384)
+    inp = W.make_call(w)
+    h, e = W.make_weights(w)
+    head, embed = h.cuda(), e.cuda()
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    ref = U.run(gpu_lib, w, inp, CHAIN, plan=plan, head=head, embed=embed)
+    for _ in range(20):
+        out = U.run(gpu_lib, w, inp, CHAIN, plan=plan, head=head, embed=embed)
+        assert np.array_equal(out[0], ref[0]) and np.array_equal(out[1], ref[1])
+    plan.close()
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 4, 5])
+def test_full_workload_parity(gpu_lib, cfg):
+    w = W.CONFIGS[cfg]
+    inp = W.make_call(w)
+    toks, cache = U.run(gpu_lib, w, inp, AUTO)
+    rep = U.check(w, inp, toks, cache)
+    print(cfg, rep.summary())
+    assert rep.ok(), rep.summary()
+
+
+def test_latency_workload_calls(gpu_lib):
+    # the latency workload's calls differ in seed and anchor; a sample of them
+    w = W.LATENCY
+    h, e = W.make_weights(w)
+    head, embed = h.cuda(), e.cuda()
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    for call in (0, 1, 499, 999):
+        inp = W.make_call(w, call)
+        toks, cache = U.run(gpu_lib, w, inp, AUTO, plan=plan, head=head, embed=embed)
+        rep = U.check(w, inp, toks, cache)
+        assert rep.ok(), (call, rep.summary())
+    plan.close()
+
+
+def test_bad_arguments_launch_nothing(gpu_lib):
+    w = W.TINY
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, 4)
+    inp = U.to_dev(W.make_call(w))
+    h, e, _, _ = U.weights(w)
+    toks, cache = U.sentinel_outputs(1, w.steps, w.vocab)
+    L = gpu_lib.lib()
+    def call(**kw):
+        args = dict(base=inp["base"].data_ptr(), s0=w.steps * w.vocab, s1=w.vocab,
+                    head=h.cuda().data_ptr(), embed=e.cuda().data_ptr(),
+                    anchor=inp["anchor"].data_ptr(), T=inp["temperature"].data_ptr(),
+                    seeds=inp["seeds"].data_ptr(), idx=inp["row_state_idx"].data_ptr(), rows=1,
+                    mode=0, mult=1.0, cap=-1.0, toks=toks.data_ptr(), ts0=w.steps,
+                    cache=cache.data_ptr(), cs0=w.steps * w.vocab, cs1=w.vocab)
+        args.update(kw)
+        return L.markov_chain_sample(plan.handle, *args.values(), None)
+    assert call(rows=0) == 1
+    assert call(rows=5) == 1
+    assert call(mode=3) == 1
+    assert call(s1=w.vocab - 1) == 1
+    assert call(cs1=w.vocab + 1) == 1          # 16-byte row stride of the cache
+    assert call(cache=cache.data_ptr() + 2) == 1
+    assert call(mult=float("inf")) == 1
+    torch.cuda.synchronize()
+    assert np.all(toks.cpu().numpy() == U.SENT_T)
+    assert call() == 0
+    assert gpu_lib.markov_plan_status(plan) == 0
+    plan.close()
