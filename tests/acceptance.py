@@ -2,6 +2,10 @@
 
   * cache: every element of every live row within 1 BF16 ulp of the oracle
     (ordered-integer distance, +0 == -0), NaN only where the oracle has NaN;
+    an element further away must be exactly what the oracle's epilogue gives
+    with its BF16 bias moved by one ulp (the licensed difference: the bias
+    reduction order may change the bias's last bit).  That case arises under
+    cancellation, base ~ -bias, where one bias ulp is many ulps of the sum;
   * always: the oracle's selection applied to the GPU's own cache row gives
     the GPU's token, bit for bit;
   * tokens: equal to the oracle's, except where the GPU's cache row differs
@@ -49,6 +53,7 @@ class Report:
     positions: int = 0
     cache_elems: int = 0
     cache_ulp_diffs: int = 0
+    cache_bias_ulp: int = 0
     excused: list = field(default_factory=list)
     failures: list = field(default_factory=list)
 
@@ -57,7 +62,8 @@ class Report:
 
     def summary(self) -> str:
         return (f"positions={self.positions} cache_elems={self.cache_elems} "
-                f"cache_1ulp={self.cache_ulp_diffs} excused={len(self.excused)} "
+                f"cache_1ulp={self.cache_ulp_diffs} cache_bias_ulp={self.cache_bias_ulp} "
+                f"excused={len(self.excused)} "
                 f"failures={self.failures[:5]}")
 
 
@@ -104,12 +110,21 @@ def check(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mode: int
             if np.any(gn != rn):
                 rep.failures.append(("cache NaN mismatch", b, i))
             both = ~gn & ~rn
-            d = np.abs(ordered_bf16(g[both]) - ordered_bf16(r_[both]))
+            d = np.zeros(V, dtype=np.int64)
+            d[both] = np.abs(ordered_bf16(g[both]) - ordered_bf16(r_[both]))
             rep.cache_elems += int(both.sum())
-            if d.size and d.max() > 1:
-                rep.failures.append(("cache > 1 ulp", b, i, int(d.max())))
-            ndiff = int((d == 1).sum())
-            rep.cache_ulp_diffs += ndiff
+            p_i = int(anchor[b]) if i == 0 else int(gpu_tokens[b, i - 1])
+            for v in np.flatnonzero(d > 1):
+                bias = oracle.bias_one(head_bits, embed_bits, int(v), p_i)
+                allowed = {oracle.lib().orc_logit(int(base[b, i, v]), int(nb), *tf)
+                           for nb in bf16_nudges(bias)}
+                if int(g[v]) in allowed:
+                    rep.cache_bias_ulp += 1
+                else:
+                    rep.failures.append(("cache beyond a 1-ulp bias change", b, i, int(v),
+                                         int(d[v])))
+            ndiff = int((d >= 1).sum())
+            rep.cache_ulp_diffs += int((d == 1).sum())
             gt = int(gpu_tokens[b, i])
             sel, _, _ = oracle.select(g, T, mode, seed, b, i)
             if sel != gt:

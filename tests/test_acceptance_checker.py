@@ -59,3 +59,32 @@ def test_checker_inverse_cdf_softcap():
     t2 = toks.copy()
     t2[0, 3] = (t2[0, 3] + 3) % 400
     assert not _chk(w, inp, hb, eb, t2, cache).ok()
+
+
+def test_checker_bias_ulp_rule():
+    # A cache element equal to the epilogue of the oracle's bias moved by one
+    # BF16 ulp is accepted at any distance; 3 ulps away otherwise is not.
+    from tests.acceptance import bf16_nudges
+    w = W.small(256, 32, 1, 1, W.GUMBEL, seed=23, temperatures=(1.0,))
+    inp, hb, eb, toks, cache = _run(w)
+    base = oracle.bf16_bits(inp["base"])
+    p = int(inp["anchor"][0])
+    planted = 0
+    for v in range(256):
+        bias = oracle.bias_one(hb, eb, v, p)
+        for nb in bf16_nudges(bias)[::2]:
+            l = oracle.lib().orc_logit(int(base[0, 0, v]), int(nb), 0, 1.0, 0, 1.0, 1.0)
+            if l != cache[0, 0, v] and v != toks[0, 0]:
+                c2 = cache.copy()
+                c2[0, 0, v] = l
+                rep = _chk(w, inp, hb, eb, toks, c2)
+                assert rep.ok(), rep.summary()
+                planted += 1
+                break
+        if planted >= 3:
+            break
+    assert planted >= 1
+    c3 = cache.copy()
+    v = (int(toks[0, 0]) + 1) % 256
+    c3[0, 0, v] = int(c3[0, 0, v]) + (3 if c3[0, 0, v] < 0x7000 else -3)
+    assert not _chk(w, inp, hb, eb, toks, c3).ok()
