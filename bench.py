@@ -2,8 +2,8 @@
 
 A step is one whole Markov call of the DeepSeek-V4.1-shaped workload
 (V=129280, r=256, 8 request rows of which 2 are padding, N=8 draft
-positions, Gumbel mode): the noise kernel plus the persistent chain kernel,
-over inputs already resident in HBM.  L2 is flushed (a 256 MB write) before
+positions, Gumbel mode) over inputs already resident in HBM: one launch of
+the persistent chain kernel, which also draws the call's Gumbel noise.  L2 is flushed (a 256 MB write) before
 every timed step and the flush is not timed.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -221,18 +221,15 @@ def run_gpu(args):
     L = api.lib()
 
     def step(evs=None):
-        # the noise kernel, then the chain; events between them time the chain
+        # one call: the persistent chain kernel draws the noise itself while
+        # the head streams in, so a step is a single launch
         if evs:
             evs[0].record(stream)
-        api.markov_noise_fork(plan, d["seeds"], d["temperature"], d["row_state_idx"], stream)
-        api.markov_noise_join(plan, stream)
-        if evs:
-            evs[1].record(stream)
         api.markov_chain_sample(plan, d["base"], head, embed, d["anchor"], d["temperature"],
                                 d["seeds"], d["row_state_idx"], w.mode, w.mult, w.cap, toks,
                                 cache, stream)
         if evs:
-            evs[2].record(stream)
+            evs[1].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
@@ -241,9 +238,10 @@ def run_gpu(args):
     st = api.markov_plan_status(plan)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
-    launches_per_step = plan.query(api.Q_LAST_LAUNCHES) + 1   # + the forked noise kernel
+    launches_per_step = plan.query(api.Q_LAST_LAUNCHES)
+    path = {1: "tcgen05 chain", 2: "batch", 3: "simple chain"}.get(plan.query(api.Q_LAST_PATH), "?")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -257,8 +255,8 @@ def run_gpu(args):
     st = api.markov_plan_status(plan)
     if st != 0:
         raise RuntimeError(f"device status {st} in the timed region")
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    chain_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    chain_ms = step_ms
     total_ms = sum(step_ms)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -304,14 +302,15 @@ def run_gpu(args):
                 "random weights)",
         "config": {"workload": w.name, "rows": R, "live_rows": live, "vocab": V, "rank": w.rank,
                    "steps_per_call": N, "mode": "gumbel", "l2": "flushed before every step",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "path": path,
+                   "resident_head_bytes": plan.query(api.Q_RESIDENT_HEAD_BYTES)},
         "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
                         "p99": sorted(step_ms)[min(len(step_ms) - 1,
                                                    int(0.99 * len(step_ms)))] * 1000.0,
                         "chain_kernel_median": statistics.median(chain_ms) * 1000.0},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "chain_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel": "chain_tc_kernel", "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens_per_step / (e2e_step / 1000.0), "unit": UNIT,

@@ -18,7 +18,7 @@ from . import build as _build
 
 GUMBEL = 0
 INVCDF = 1
-PATH_AUTO, PATH_CHAIN, PATH_BATCH = 0, 1, 2
+PATH_AUTO, PATH_CHAIN, PATH_BATCH, PATH_CHAIN_SIMPLE = 0, 1, 2, 3
 Q_CHAIN_CTAS, Q_RESIDENT_HEAD_BYTES, Q_LAST_LAUNCHES, Q_LAST_PATH, Q_SM_COUNT = range(5)
 
 STATUS = {0: "MARKOV_OK", 1: "MARKOV_EINVAL", 2: "MARKOV_EUNSUPPORTED", 3: "MARKOV_ECUDA",

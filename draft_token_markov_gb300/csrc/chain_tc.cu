@@ -1,0 +1,662 @@
+// chain_tc.cu -- the Blackwell persistent Markov chain kernel: all N draft
+// positions of up to 8 request rows in one cooperative launch, with the whole
+// Markov head resident on chip across positions.
+//
+// Sources: sharded_markov page, module docstring (one cooperative kernel per
+// shard runs the whole chain and keeps its head rows on chip, so the head is
+// read once; up to 8 request rows are the MMA columns; shards agree on each
+// position's winner by exchanging one 64-bit (score, index) key; the noise
+// is drawn beside the chain) and _shard_noise_kernel (counter-based noise).
+// Here the shards are the CTAs of one GPU.
+//
+// Per CTA: a contiguous run of 128-id vocab tiles (at most 28 chunks of
+// [128 ids x 64 K]).  The first 15 chunks live in Tensor Memory as MMA A
+// operands (32 columns each), the rest in shared memory in the 128-byte
+// swizzled K-major layout the TMA writes; two 16-column TMEM accumulators
+// take the bias tiles.  Measured on GB300: an M=128, N=16, K=16 BF16 MMA
+// costs ~9 cycles with A in TMEM (enough issuing threads) and ~39 with A in
+// shared memory (bandwidth), and all MMA paths share one tensor pipe, so TMEM
+// holds as much of the head as fits.
+//
+// Warp roles (16 warps):
+//   0, 1   lane 0 issues the MMAs of the even / odd tiles into accumulator
+//          0 / 1 (one issuing thread per accumulator)
+//   2      lane 0: TMA producer of the head chunks (position 0 only)
+//   3      lane 0: copies the TMEM-resident chunks from their shared-memory
+//          staging slot into TMEM (position 0 only)
+//   4-7    epilogue of accumulator 0; 8-11 epilogue of accumulator 1
+//   4-15   at position 0, before the epilogue: Gumbel noise of this CTA's ids
+//          for every position (ALU work hidden behind the head's HBM load)
+//   0-7    after each position: warp b exchanges row b's key with every CTA
+//          and stages markov_embed[token] as the next position's B operand
+// Cross-CTA exchange: each CTA stores its per-row best key, tagged with the
+// call's position epoch, in its own slot of a per-position array; every CTA
+// polls all slots until every tag is current (bounded) and takes the maximum.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace dtm {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kTmemChunks = 15;           // A chunks in TMEM (32 columns each)
+constexpr int kSmemChunks = 13;           // A chunks in shared memory (16 KB each)
+constexpr int kMaxChunks = kTmemChunks + kSmemChunks;
+constexpr uint32_t kChunkBytes = 128 * 128;   // 128 rows x 64 BF16
+constexpr uint32_t kDCol = 480;           // accumulators: columns 480..495, 496..511
+constexpr uint32_t kBChunkBytes = 16 * 128;   // B operand: 16 rows x 64 BF16 per K-chunk
+constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
+constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
+constexpr uint32_t kSmemB = 4 * kBChunkBytes;
+constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
+
+struct Ctl {
+    uint64_t full[kSmemChunks];      // TMA landed in slot s
+    uint64_t cpdone[kSmemChunks];    // slot s copied into TMEM
+    uint64_t dfull[2];               // accumulator b holds a finished tile
+    uint64_t dfree[2];               // accumulator b read out by its epilogue
+    uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
+    uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
+    uint64_t win[kChainRows];
+    unsigned long long sum[kChainRows];
+    uint64_t scan[kThreads / 32];
+    uint64_t tot, pre;
+    uint32_t tmem_base;
+    uint32_t tmem_ready;             // chunks copied into TMEM so far
+    uint32_t abort;
+    uint32_t call;                   // the plan's call counter at launch
+    int live[kChainRows];
+    int sampling[kChainRows];
+    float T[kChainRows];
+    uint64_t seed[kChainRows];
+    int64_t prev[kChainRows];
+};
+
+__device__ __forceinline__ void fail(Ctl &c, const SampleArgs &a, uint32_t code, uint32_t where) {
+    set_status(a.status, code, where);
+    c.abort = 1u;
+}
+
+__device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &a) {
+    return *(volatile const uint32_t *)&c.abort != 0u ||
+           ld_acquire_u32(a.status) != 0u;
+}
+
+// packed key: ordered key (32) | 0x3FFFF - id (18) | epoch tag (14)
+__device__ __forceinline__ uint64_t pack_tc(float key, uint32_t v) {
+    return ((uint64_t)ordered_key(key) << 32) | ((uint64_t)(0x3FFFFu - v) << 14);
+}
+__device__ __forceinline__ uint32_t unpack_id(uint64_t p) {
+    return 0x3FFFFu - (uint32_t)((p >> 14) & 0x3FFFFu);
+}
+
+// Row b's maximum over all CTAs' slots, once every slot carries `tag`.
+__device__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t deadline,
+                         const SampleArgs &a, uint64_t &out) {
+    const int lane = threadIdx.x & 31;
+    for (uint32_t spin = 0;; ++spin) {
+        bool fresh = true;
+        uint64_t m = 0ull;
+        for (int c = lane; c < G; c += 32) {
+            uint64_t k = tc::ld_relaxed_u64(slots + c);
+            if ((uint32_t)(k & 0x3FFFu) != tag) fresh = false;
+            m = k > m ? k : m;
+        }
+        if (__all_sync(0xffffffffu, fresh)) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                uint64_t w = __shfl_xor_sync(0xffffffffu, m, o);
+                m = w > m ? w : m;
+            }
+            out = m;
+            return true;
+        }
+        if ((spin & 15u) == 15u) {
+            bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
+            if (__any_sync(0xffffffffu, bad)) return false;
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+// Stage markov_embed[p] as row b of the B operand (16 rows x RANK, K-major,
+// 128-byte swizzle, one 2 KB block per 64-element K-chunk).
+template <int RANK>
+__device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__restrict__ embed,
+                                            int64_t p, int b, int lane) {
+    if (lane < RANK / 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(embed + p * RANK + 8 * lane);
+        const int chunk = lane >> 3, piece = lane & 7;
+        *reinterpret_cast<uint4 *>(b_s + chunk * kBChunkBytes + b * 128 + ((piece ^ b) << 4)) = v;
+    }
+}
+
+}  // namespace
+
+template <int RANK>
+__global__ void __launch_bounds__(kThreads, 1)
+chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, int noise_ready) {
+    constexpr int cpt = RANK / 64;                 // K-chunks per 128-id tile
+    extern __shared__ uint8_t dsm_raw[];
+    __shared__ Ctl c;
+    uint8_t *dsm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint8_t *head_s = dsm;
+    uint8_t *b_s = dsm + kSmemHead;
+    const uint32_t head_sa = tc::smem_u32(head_s), b_sa = tc::smem_u32(b_s);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int R = a.rows, N = a.N, V = a.V;
+    const int T_total = (V + 127) / 128;
+    const int t0 = (int)((int64_t)cta * T_total / G);
+    const int t1 = (int)((int64_t)(cta + 1) * T_total / G);
+    const int nt = t1 - t0;
+    const int nch = nt * cpt;
+    const int ntm = nch < kTmemChunks ? nch : kTmemChunks;
+    const int v_begin = t0 * 128;
+    const int v_end = t1 * 128 < V ? t1 * 128 : V;
+    const int Gp = (G + kKeyPad - 1) / kKeyPad * kKeyPad;
+
+    // ------------------------------------------------------------ set-up
+    if (tid == 0) {
+        for (int s = 0; s < kSmemChunks; ++s) {
+            tc::mbar_init(tc::smem_u32(&c.full[s]), 1);
+            tc::mbar_init(tc::smem_u32(&c.cpdone[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tc::smem_u32(&c.dfull[b]), 1);
+            tc::mbar_init(tc::smem_u32(&c.dfree[b]), 4);
+            tc::mbar_init(tc::smem_u32(&c.fin[b]), 1);
+        }
+        tc::mbar_init_fence();
+        c.tmem_ready = 0u;
+        c.abort = ld_acquire_u32(a.status) != 0u ? 1u : 0u;
+        c.call = *(volatile const uint32_t *)a.call_counter;
+    }
+    if (tid < kChainRows) {
+        const int b = tid;
+        const bool live = b < R && a.row_state_idx[b] >= 0;
+        c.live[b] = live;
+        const float T = live ? a.temperature[b] : 0.0f;
+        c.T[b] = T;
+        c.sampling[b] = live && samples(T);
+        c.seed[b] = live ? (uint64_t)a.seeds[b] : 0ull;
+        int64_t p = live ? (int64_t)a.anchor[b] : 0;
+        if (p < 0 || p >= V) {
+            set_status(a.status, 1u /* MARKOV_EINVAL */, 0x100u + b);
+            p = 0;
+        }
+        c.prev[b] = p;
+    }
+    for (int o = tid * 16; o < (int)kSmemB; o += kThreads * 16)
+        *reinterpret_cast<uint4 *>(b_s + o) = make_uint4(0u, 0u, 0u, 0u);
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&c.tmem_base), 512);
+    __syncthreads();
+    if (warp < kChainRows && c.live[warp]) stage_embed<RANK>(b_s, a.embed, c.prev[warp], warp, lane);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = c.tmem_base;
+    const uint64_t timeout = a.timeout_ns;
+
+    // per-role persistent state
+    uint32_t uses = 0;          // issuer: tiles issued into its accumulator
+    uint32_t dcount = 0;        // epilogue: tiles consumed from its accumulator
+    uint32_t issued[kSmemChunks];   // producer: loads issued per slot
+#pragma unroll
+    for (int s = 0; s < kSmemChunks; ++s) issued[s] = 0u;
+
+    bool stop = __syncthreads_or(c.abort != 0u);
+    for (int i = 0; i < N && !stop; ++i) {
+        // ------------------------------------- phase A: MMA and epilogue
+        if (warp < 2) {
+            if (lane == 0) {
+                const int w = warp;
+                const uint32_t d = tmem + kDCol + 16u * w;
+                for (int k = w; k < nt; k += 2) {
+                    if (aborted(c, a)) break;
+                    if (uses > 0 && !tc::mbar_wait(tc::smem_u32(&c.dfree[w]), (uses - 1) & 1u,
+                                                   tc::now_ns() + timeout)) {
+                        fail(c, a, 4u, 0x1000u + i);
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    bool ok = true;
+                    for (int kc = 0; kc < cpt && ok; ++kc) {
+                        const int j = k * cpt + kc;
+                        if (i == 0) {
+                            const uint64_t dl = tc::now_ns() + timeout;
+                            if (j < kTmemChunks) {
+                                while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
+                                    if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                                }
+                                tc::fence_after_sync();
+                            } else {
+                                // a parity wait only tells phases apart one at a time:
+                                // every earlier load of this slot (the TMEM chunks
+                                // staged in it) must be complete first
+                                while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
+                                    if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                                }
+                                const int s = j - kTmemChunks;
+                                const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
+                                if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
+                            }
+                            if (!ok) { fail(c, a, 4u, 0x2000u + j); break; }
+                        }
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bd = tc::sw128_desc(b_sa + kc * kBChunkBytes + 32 * ks);
+                            const uint32_t acc = (kc | ks) != 0;
+                            if (j < kTmemChunks)
+                                tc::mma_tmemA(d, tmem + 32u * j + 8u * ks, bd, kIdesc, acc);
+                            else
+                                tc::mma_smemA(d, tc::sw128_desc(head_sa + (j - kTmemChunks) * kChunkBytes +
+                                                                32 * ks),
+                                              bd, kIdesc, acc);
+                        }
+                    }
+                    if (!ok) break;
+                    tc::commit(tc::smem_u32(&c.dfull[w]));
+                    ++uses;
+                }
+            }
+            __syncwarp();
+        } else if (warp == 2) {
+            if (lane == 0 && i == 0) {
+                for (int j = 0; j < nch; ++j) {
+                    if (aborted(c, a)) break;
+                    int s;
+                    bool ok = true;
+                    const uint64_t dl = tc::now_ns() + timeout;
+                    if (j < ntm) {
+                        s = j % kSmemChunks;
+                        if (j >= kSmemChunks) ok = tc::mbar_wait(tc::smem_u32(&c.cpdone[s]), 0u, dl);
+                    } else {
+                        s = j - kTmemChunks;
+                        ok = tc::mbar_wait(tc::smem_u32(&c.cpdone[s]),
+                                           (s + kSmemChunks < ntm) ? 1u : 0u, dl);
+                    }
+                    if (!ok) { fail(c, a, 4u, 0x3000u + j); break; }
+                    const uint32_t bar = tc::smem_u32(&c.full[s]);
+                    tc::mbar_expect_tx(bar, kChunkBytes);
+                    tc::tma_load_2d(head_sa + s * kChunkBytes, &tmap, (j % cpt) * 64,
+                                    (t0 + j / cpt) * 128, bar);
+                    ++issued[s];
+                }
+            }
+            __syncwarp();
+        } else if (warp == 3) {
+            if (lane == 0 && i == 0) {
+                for (int j = 0; j < ntm; ++j) {
+                    if (aborted(c, a)) break;
+                    const int s = j % kSmemChunks;
+                    const uint32_t par = (uint32_t)(j / kSmemChunks) & 1u;
+                    if (!tc::mbar_wait(tc::smem_u32(&c.full[s]), par, tc::now_ns() + timeout)) {
+                        fail(c, a, 4u, 0x4000u + j);
+                        break;
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::cp_128x256b(tmem + 32u * j + 8u * ks,
+                                        tc::sw128_desc(head_sa + s * kChunkBytes + 32 * ks));
+                    tc::commit(tc::smem_u32(&c.cpdone[s]));
+                    if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[s]), par, tc::now_ns() + timeout)) {
+                        fail(c, a, 4u, 0x5000u + j);
+                        break;
+                    }
+                    tc::fence_before_sync();
+                    *(volatile uint32_t *)&c.tmem_ready = (uint32_t)(j + 1);
+                }
+            }
+            __syncwarp();
+        } else {
+            // warps 4..15: at position 0 the noise of every position, then the epilogue
+            if (i == 0) {
+                const int t384 = tid - 128;
+                if (warp >= 12) {
+                    // warm L2 with this CTA's base-logit slices of every position
+                    for (int b = 0; b < R && b < kChainRows; ++b) {
+                        if (!c.live[b]) continue;
+                        for (int i2 = 0; i2 < N; ++i2) {
+                            const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
+                            for (int v = v_begin + (t384 - 256) * 64; v < v_end; v += 128 * 64)
+                                tc::prefetch_l2(row + v);
+                        }
+                    }
+                }
+                if (a.mode == 0 && !noise_ready) {
+                    for (int b = 0; b < R && b < kChainRows; ++b) {
+                        if (!c.sampling[b]) continue;
+                        for (int i2 = 0; i2 < N; ++i2) {
+                            const uint64_t hri = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
+                            float *dst = a.noise + (int64_t)(b * N + i2) * a.noise_s0;
+                            for (int v = v_begin + t384; v < v_end; v += 384)
+                                dst[v] = dm_gumbel(hri, (uint32_t)v);
+                        }
+                    }
+                }
+                asm volatile("bar.sync 1, 384;" ::: "memory");
+            }
+            if (warp < 12) {
+                const int wg = (warp - 4) >> 2, q = warp & 3;
+                uint64_t best[kChainRows];
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) best[b] = 0ull;
+                for (int k = wg; k < nt; k += 2) {
+                    const bool ab = __shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0);
+                    if (ab) break;
+                    bool ok = true;
+                    if (lane == 0)
+                        ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u,
+                                           tc::now_ns() + timeout);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) {
+                        if (lane == 0) fail(c, a, 4u, 0x6000u + i);
+                        break;
+                    }
+                    ++dcount;
+                    tc::fence_after_sync();
+                    uint32_t r[8];
+                    tc::ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg, r);
+                    tc::wait_ld();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
+                    const int v = (t0 + k) * 128 + q * 32 + lane;
+                    if (v < V) {
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b) {
+                            if (!c.live[b]) continue;
+                            const uint32_t bb = a.base[b * a.base_s0 + (int64_t)i * a.base_s1 + v];
+                            const uint32_t l = logit_bits(bb, __uint_as_float(r[b]), a.tf);
+                            a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
+                            float key = dm_bf16_f32(l);
+                            if (c.sampling[b]) {
+                                const float T = c.T[b];
+                                if (T != 1.0f) key = __fdiv_rn(key, T);
+                                if (a.mode == 0)
+                                    key = __fadd_rn(key, a.noise[(int64_t)(b * N + i) * a.noise_s0 + v]);
+                            }
+                            const uint64_t pk = pack_tc(key, (uint32_t)v);
+                            best[b] = pk > best[b] ? pk : best[b];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) {
+                    uint64_t m = best[b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
+                        m = w2 > m ? w2 : m;
+                    }
+                    if (lane == 0) c.wbest[warp - 4][b] = m;
+                }
+            }
+        }
+        stop = __syncthreads_or(aborted(c, a));
+        if (stop) break;
+
+        // ------------------------------- phase B: agree on every row's winner
+        const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
+        const uint32_t tag = epoch & 0x3FFFu;
+        if (warp < kChainRows) {
+            const int b = warp;
+            uint64_t m = lane < 8 ? c.wbest[lane][b] : 0ull;
+#pragma unroll
+            for (int o = 4; o > 0; o >>= 1) {
+                const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
+                m = w2 > m ? w2 : m;
+            }
+            uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * Gp;
+            if (lane == 0) tc::st_relaxed_u64(slots + cta, (m & ~0x3FFFull) | tag);
+            if (c.live[b]) {
+                if (lane == 0 && m != 0ull) {
+                    const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;
+                    for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(reinterpret_cast<const uint8_t *>(er) + o);
+                }
+                uint64_t w = 0ull;
+                if (!poll_max(slots, G, tag, tc::now_ns() + timeout, a, w)) {
+                    if (lane == 0) fail(c, a, 4u, 0x7000u + i);
+                } else if (lane == 0) {
+                    c.win[b] = w;
+                }
+            }
+        }
+        stop = __syncthreads_or(aborted(c, a));
+        if (stop) break;
+
+        // inverse CDF: rows whose maximum M is finite need the exact integer
+        // weight sums floor(exp(x - M) 2^40), then the CTA whose prefix range
+        // holds mulhi64(H, S) scans its ids for the token
+        bool cdf_any = false;
+        if (a.mode == 1) {
+            for (int b = 0; b < R && b < kChainRows; ++b) {
+                if (!c.sampling[b]) continue;
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                const float M = key_from_ordered(o);
+                if (o != 0xffffffffu && !isinf(M)) cdf_any = true;
+            }
+        }
+        if (cdf_any) {
+            const uint32_t tag32 = epoch;
+            if (tid < kChainRows) c.sum[tid] = 0ull;
+            __syncthreads();
+            for (int b = 0; b < R && b < kChainRows; ++b) {
+                if (!c.sampling[b]) continue;
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                const float M = key_from_ordered(o);
+                if (o == 0xffffffffu || isinf(M)) continue;
+                const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                uint64_t part = 0ull;
+                for (int v = v_begin + tid; v < v_end; v += kThreads) {
+                    const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                    part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+                if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
+            }
+            __syncthreads();
+            if (tid < kChainRows && c.sampling[tid]) {
+                const int64_t at = ((int64_t)i * kChainRows + tid) * Gp + cta;
+                tc::st_relaxed_u64(a.tc_sums + at, c.sum[tid]);
+                tc::st_release_u32g(a.sum_tags + at, tag32);
+            }
+            // every CTA learns every row's total and its own prefix
+            __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
+            if (warp < kChainRows && c.sampling[warp]) {
+                const int b = warp;
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                const float M = key_from_ordered(o);
+                if (o != 0xffffffffu && !isinf(M)) {
+                    const int64_t base_at = ((int64_t)i * kChainRows + b) * Gp;
+                    const uint64_t dl = tc::now_ns() + timeout;
+                    bool ok = true;
+                    for (uint32_t spin = 0;; ++spin) {
+                        bool fresh = true;
+                        for (int cc = lane; cc < G; cc += 32)
+                            if (ld_acquire_u32(a.sum_tags + base_at + cc) != tag32) fresh = false;
+                        if (__all_sync(0xffffffffu, fresh)) break;
+                        if ((spin & 15u) == 15u &&
+                            __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) {
+                        if (lane == 0) fail(c, a, 4u, 0x8000u + i);
+                    } else {
+                        uint64_t tot = 0ull, pre = 0ull;
+                        for (int cc = lane; cc < G; cc += 32) {
+                            const uint64_t s = tc::ld_relaxed_u64(a.tc_sums + base_at + cc);
+                            tot += s;
+                            if (cc < cta) pre += s;
+                        }
+#pragma unroll
+                        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                            tot += __shfl_xor_sync(0xffffffffu, tot, o2);
+                            pre += __shfl_xor_sync(0xffffffffu, pre, o2);
+                        }
+                        if (lane == 0) { s_tot[b] = tot; s_pre[b] = pre; }
+                    }
+                }
+            }
+            stop = __syncthreads_or(aborted(c, a));
+            if (stop) break;
+            for (int b = 0; b < R && b < kChainRows; ++b) {
+                if (!c.sampling[b]) continue;
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                const float M = key_from_ordered(o);
+                if (o == 0xffffffffu || isinf(M)) continue;
+                const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
+                const uint64_t H = dm_cdf_hash(dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i));
+                const uint64_t target = __umul64hi(H, S);
+                if (P <= target && target < P + Sc) {
+                    const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                    const int len = v_end - v_begin;
+                    const int chunk = (len + kThreads - 1) / kThreads;
+                    const int c0 = v_begin + tid * chunk;
+                    const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
+                    uint64_t mine = 0ull;
+                    for (int v = c0; v < c1; ++v) {
+                        const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                        mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                    }
+                    uint64_t incl = mine;
+#pragma unroll
+                    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+                        if (lane >= o2) incl += y;
+                    }
+                    if (lane == 31) c.scan[warp] = incl;
+                    __syncthreads();
+                    uint64_t wpre = 0ull;
+                    for (int w = 0; w < warp; ++w) wpre += c.scan[w];
+                    uint64_t run = P + wpre + incl - mine;
+                    if (run <= target && target < run + mine) {
+                        for (int v = c0; v < c1; ++v) {
+                            const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                            run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                            if (run > target) {
+                                tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
+                                                   ((uint64_t)v << 32) | tag32);
+                                break;
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+            // everyone learns the tokens the owners found
+            if (warp < kChainRows && c.sampling[warp] && lane == 0) {
+                const int b = warp;
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                const float M = key_from_ordered(o);
+                if (o != 0xffffffffu && !isinf(M)) {
+                    const uint64_t *slot = a.tok_slots + (int64_t)i * kChainRows + b;
+                    const uint64_t dl = tc::now_ns() + timeout;
+                    uint64_t t = 0ull;
+                    for (;;) {
+                        t = tc::ld_relaxed_u64(slot);
+                        if ((uint32_t)t == tag32) break;
+                        if (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u) {
+                            fail(c, a, 4u, 0x9000u + i);
+                            break;
+                        }
+                    }
+                    const uint32_t v = (uint32_t)(t >> 32);
+                    if ((uint32_t)t == tag32 && v < (uint32_t)V)
+                        c.win[b] = (c.win[b] & 0xffffffff00000000ull) |
+                                   ((uint64_t)(0x3FFFFu - v) << 14);
+                    else if ((uint32_t)t == tag32)
+                        fail(c, a, 6u, 0xA000u + i);
+                }
+            }
+            stop = __syncthreads_or(aborted(c, a));
+            if (stop) break;
+        }
+
+        // ------------------------- the token, and the next position's B operand
+        if (warp < kChainRows && c.live[warp]) {
+            const int b = warp;
+            uint32_t id = unpack_id(c.win[b]);
+            if (a.mode == 1 && c.sampling[b]) {
+                const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
+            }
+            if (lane == 0) {
+                c.prev[b] = (int64_t)id;
+                if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
+            }
+            if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
+        }
+        tc::fence_proxy_async_smem();
+        tc::fence_before_sync();
+        stop = __syncthreads_or(aborted(c, a));
+        tc::fence_after_sync();
+    }
+
+    // --------------------------------------------------------------- exit
+    // every async operation of this CTA completes before TMEM is released
+    if (warp < 2 && lane == 0) {
+        tc::commit(tc::smem_u32(&c.fin[warp]));
+        tc::mbar_wait(tc::smem_u32(&c.fin[warp]), 0u, tc::now_ns() + 1000000000ull);
+    }
+    if (warp == 2 && lane == 0) {
+        for (int s = 0; s < kSmemChunks; ++s) {
+            if (issued[s] == 0u) continue;
+            tc::mbar_wait(tc::smem_u32(&c.full[s]), (issued[s] - 1u) & 1u,
+                          tc::now_ns() + 1000000000ull);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+    if (cta == 0 && tid == 0 && !aborted(c, a))
+        *(volatile uint32_t *)a.call_counter = c.call + 1u;
+}
+
+size_t chain_tc_smem() { return kDynSmem; }
+
+int chain_tc_max_chunks() { return kMaxChunks; }
+
+cudaError_t chain_tc_prepare() {
+    cudaError_t e = cudaSuccess;
+    for (const void *fn : {(const void *)chain_tc_kernel<64>, (const void *)chain_tc_kernel<128>,
+                           (const void *)chain_tc_kernel<256>}) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+        if (e != cudaSuccess) return e;
+    }
+    return e;
+}
+
+cudaError_t chain_tc_occupancy(int *blocks_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, chain_tc_kernel<256>,
+                                                         kThreads, kDynSmem);
+}
+
+cudaError_t launch_chain_tc(const SampleArgs &a, const CUtensorMap &tmap, int noise_ready,
+                            cudaStream_t stream) {
+    void *args[] = {(void *)&a, (void *)&tmap, (void *)&noise_ready};
+    const void *fn = nullptr;
+    switch (a.r) {
+        case 64: fn = (const void *)chain_tc_kernel<64>; break;
+        case 128: fn = (const void *)chain_tc_kernel<128>; break;
+        case 256: fn = (const void *)chain_tc_kernel<256>; break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaLaunchCooperativeKernel(fn, dim3(a.grid), dim3(kThreads), args, kDynSmem, stream);
+}
+
+}  // namespace dtm

@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace dtm {
@@ -41,7 +42,7 @@ struct SampleArgs {
     int64_t tok_s0;
     uint16_t *cache;
     int64_t cache_s0, cache_s1;
-    const float *noise;        // [rows * N, V] fp32 Gumbel noise (Gumbel mode)
+    float *noise;              // [rows * N, V] fp32 Gumbel noise (Gumbel mode)
     int64_t noise_s0;          // row stride of the noise, in floats
     // plan scratch
     uint64_t *keys;            // cross-CTA key / partial slots
@@ -49,6 +50,11 @@ struct SampleArgs {
     uint32_t *bar_count;       // grid barrier counter
     uint32_t *bar_base;        // the counter's value at the start of a launch
     uint32_t *status;          // [2]: sticky device status, where it happened
+    uint32_t *call_counter;    // calls of the persistent tcgen05 chain so far
+    uint64_t *tc_keys;         // [N][8][Gp] tagged key slots of the tcgen05 chain
+    uint64_t *tc_sums;         // [N][8][Gp] inverse-CDF sum slots of the tcgen05 chain
+    uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
+    uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
     uint64_t timeout_ns;
     int grid;                  // persistent grid size (chain) or vocab blocks (batch)
 };
@@ -62,5 +68,11 @@ cudaError_t chain_occupancy(int *blocks_per_sm);
 cudaError_t launch_chain(const SampleArgs &a, cudaStream_t stream);
 cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches);
 int batch_blocks(int V);
+size_t chain_tc_smem();
+int chain_tc_max_chunks();
+cudaError_t chain_tc_prepare();
+cudaError_t chain_tc_occupancy(int *blocks_per_sm);
+cudaError_t launch_chain_tc(const SampleArgs &a, const CUtensorMap &tmap, int noise_ready,
+                            cudaStream_t stream);
 
 }  // namespace dtm

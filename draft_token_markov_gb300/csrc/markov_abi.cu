@@ -24,8 +24,19 @@ struct markov_plan {
     int64_t noise_s0 = 0;
     uint64_t *keys = nullptr;
     uint64_t *sums = nullptr;
-    uint32_t *ctrl = nullptr;     // [0] barrier count, [1] barrier base, [2..3] status
+    uint32_t *ctrl = nullptr;     // [0] barrier count, [1] barrier base, [2..3] status,
+                                  // [4] call counter of the tcgen05 chain
     size_t keys_n = 0;
+    // the tcgen05 chain: tagged exchange slots and the head's TMA descriptor
+    bool tc_ok = false;
+    int tc_grid = 0;
+    uint64_t *tc_keys = nullptr;
+    uint64_t *tc_sums = nullptr;
+    uint32_t *sum_tags = nullptr;
+    uint64_t *tok_slots = nullptr;
+    size_t tc_slots_n = 0;
+    CUtensorMap tmap;
+    const void *tmap_head = nullptr;
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_noise = nullptr;
     int noise_state = 0;          // 0 none, 1 forked, 2 forked and joined
@@ -62,10 +73,41 @@ void free_plan(markov_plan *p) {
     if (p->keys) cudaFree(p->keys);
     if (p->sums) cudaFree(p->sums);
     if (p->ctrl) cudaFree(p->ctrl);
+    if (p->tc_keys) cudaFree(p->tc_keys);
+    if (p->tc_sums) cudaFree(p->tc_sums);
+    if (p->sum_tags) cudaFree(p->sum_tags);
+    if (p->tok_slots) cudaFree(p->tok_slots);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_noise) cudaEventDestroy(p->ev_noise);
     if (p->side) cudaStreamDestroy(p->side);
     delete p;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The head [V, r] BF16 as 2-D tiles of 128 rows x 64 elements, 128-byte
+// swizzle (the K-major MMA operand layout); rows past V read as zero.
+bool encode_head_map(CUtensorMap *m, const void *head, int V, int r) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !f)
+            return false;
+        fn = (EncodeTiledFn)f;
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)V};
+    cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(head), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 Transform make_transform(float mult, float cap) {
@@ -127,6 +169,20 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     if (g > p->sm_count * p->chain_occ) g = p->sm_count * p->chain_occ;
     p->chain_grid = g;
     p->batch_grid = batch_blocks(d.vocab);
+    {
+        // the tcgen05 chain: one CTA per SM (at most one per 128-id tile); every
+        // CTA's tiles must fit the on-chip chunk budget
+        const int T_total = (d.vocab + 127) / 128;
+        int g = T_total < p->sm_count ? T_total : p->sm_count;
+        const int max_tiles = (T_total + g - 1) / g;
+        int occ = 0;
+        if (chain_tc_prepare() == cudaSuccess && chain_tc_occupancy(&occ) == cudaSuccess &&
+            occ >= 1 && max_tiles * (d.rank / 64) <= chain_tc_max_chunks()) {
+            p->tc_ok = true;
+            p->tc_grid = g;
+        }
+        cudaGetLastError();
+    }
 
     const int Gp = (p->chain_grid + kKeyPad - 1) / kKeyPad * kKeyPad;
     size_t chain_keys = (size_t)kMaxSteps * 2 * kChainRows * Gp;
@@ -134,10 +190,19 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     p->keys_n = chain_keys > batch_keys ? chain_keys : batch_keys;
     p->noise_s0 = d.vocab;
     const size_t noise_bytes = (size_t)d.max_rows * d.num_steps * d.vocab * sizeof(float);
+    const int Gtc = p->tc_grid > 0 ? p->tc_grid : 1;
+    p->tc_slots_n = (size_t)kMaxSteps * kChainRows * ((Gtc + kKeyPad - 1) / kKeyPad * kKeyPad);
     if (cudaMalloc(&p->noise, noise_bytes) != cudaSuccess ||
         cudaMalloc(&p->keys, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sums, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->ctrl, 8 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&p->tc_keys, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->tc_sums, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->sum_tags, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&p->tok_slots, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_keys, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->keys, 0, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
@@ -166,7 +231,8 @@ int32_t markov_chain_max_rows(const markov_plan *p) {
 
 markov_status markov_plan_set_path(markov_plan *p, markov_path path) {
     if (!p) return MARKOV_EINVAL;
-    if (path != MARKOV_PATH_AUTO && path != MARKOV_PATH_CHAIN && path != MARKOV_PATH_BATCH)
+    if (path != MARKOV_PATH_AUTO && path != MARKOV_PATH_CHAIN && path != MARKOV_PATH_BATCH &&
+        path != MARKOV_PATH_CHAIN_SIMPLE)
         return MARKOV_EINVAL;
     p->path = path;
     return MARKOV_OK;
@@ -229,8 +295,10 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     if (p->noise_state != 0 && p->forked_rows != rows) return MARKOV_EINVAL;
 
     bool chain = rows <= kChainRows;
-    if (p->path == MARKOV_PATH_CHAIN && !chain) return MARKOV_EUNSUPPORTED;
+    if ((p->path == MARKOV_PATH_CHAIN || p->path == MARKOV_PATH_CHAIN_SIMPLE) && !chain)
+        return MARKOV_EUNSUPPORTED;
     if (p->path == MARKOV_PATH_BATCH) chain = false;
+    const bool use_tc = chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE;
 
     DeviceGuard guard(p->d.device);
     if (!guard.ok) return MARKOV_EDEVICE;
@@ -264,14 +332,25 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     a.bar_count = p->ctrl;
     a.bar_base = p->ctrl + 1;
     a.status = p->ctrl + 2;
+    a.call_counter = p->ctrl + 4;
+    a.tc_keys = p->tc_keys;
+    a.tc_sums = p->tc_sums;
+    a.sum_tags = p->sum_tags;
+    a.tok_slots = p->tok_slots;
     a.timeout_ns = (uint64_t)p->d.timeout_ms * 1000000ull;
 
+    if (use_tc && p->tmap_head != head) {
+        if (!encode_head_map(&p->tmap, head, V, r)) return MARKOV_ECUDA;
+        p->tmap_head = head;
+    }
     int launches = 0;
+    const int noise_ready = p->noise_state != 0;
     if (p->noise_state == 1) {
         // join the forked noise (in inverse-CDF mode it is unused, but the
         // plan's buffer must not be rewritten while it is being drawn)
         if (cudaStreamWaitEvent(s, p->ev_noise, 0) != cudaSuccess) return MARKOV_ECUDA;
-    } else if (p->noise_state == 0 && mode == MARKOV_GUMBEL) {
+    } else if (p->noise_state == 0 && mode == MARKOV_GUMBEL && !use_tc) {
+        // the tcgen05 chain draws its own noise while the head loads
         if (launch_noise(seeds, temperature, row_state_idx, rows, N, V, p->noise, p->noise_s0, 1,
                          s) != cudaSuccess)
             return MARKOV_ECUDA;
@@ -279,14 +358,21 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     }
     p->noise_state = 0;
 
-    if (chain) {
+    if (use_tc) {
+        a.grid = p->tc_grid;
+        cudaError_t e = launch_chain_tc(a, p->tmap, noise_ready, s);
+        if (e == cudaErrorCooperativeLaunchTooLarge) { cudaGetLastError(); return MARKOV_ENOTRESIDENT; }
+        if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+        ++launches;
+        p->last_path = MARKOV_PATH_CHAIN;
+    } else if (chain) {
         if (p->chain_occ < 1) return MARKOV_ENOTRESIDENT;
         a.grid = p->chain_grid;
         cudaError_t e = launch_chain(a, s);
         if (e == cudaErrorCooperativeLaunchTooLarge) { cudaGetLastError(); return MARKOV_ENOTRESIDENT; }
         if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
         ++launches;
-        p->last_path = MARKOV_PATH_CHAIN;
+        p->last_path = MARKOV_PATH_CHAIN_SIMPLE;
     } else {
         a.grid = p->batch_grid;
         int n = 0;
@@ -308,8 +394,13 @@ markov_status markov_plan_status(markov_plan *p) {
     if (cudaMemcpy(ctrl, p->ctrl, sizeof(ctrl), cudaMemcpyDeviceToHost) != cudaSuccess)
         return MARKOV_ECUDA;
     if (ctrl[2] == 0u) return MARKOV_OK;
-    // a launch gave up: clear the status and restart the barrier counter
-    if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess) return MARKOV_ECUDA;
+    // a launch gave up: clear the status, restart the barrier and call
+    // counters, and forget every tagged exchange slot
+    if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->tc_keys, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess)
+        return MARKOV_ECUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MARKOV_ECUDA;
     return (markov_status)ctrl[2];
 }
@@ -335,8 +426,10 @@ markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n
 int64_t markov_plan_query(const markov_plan *p, int32_t key) {
     if (!p) return -1;
     switch (key) {
-        case MARKOV_Q_CHAIN_CTAS: return p->chain_grid;
-        case MARKOV_Q_RESIDENT_HEAD_BYTES: return 0;
+        case MARKOV_Q_CHAIN_CTAS: return p->tc_ok ? p->tc_grid : p->chain_grid;
+        case MARKOV_Q_RESIDENT_HEAD_BYTES:
+            // the tcgen05 chain keeps every head byte on chip across positions
+            return p->tc_ok ? (int64_t)p->d.vocab * p->d.rank * 2 : 0;
         case MARKOV_Q_LAST_LAUNCHES: return p->last_launches;
         case MARKOV_Q_LAST_PATH: return p->last_path;
         case MARKOV_Q_SM_COUNT: return p->sm_count;

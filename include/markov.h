@@ -60,8 +60,12 @@ typedef enum markov_mode {
 
 typedef enum markov_path {
     MARKOV_PATH_AUTO = 0,       /* chain up to markov_chain_max_rows rows, else batch */
-    MARKOV_PATH_CHAIN = 1,      /* the persistent single-launch chain kernel */
-    MARKOV_PATH_BATCH = 2       /* per-position kernels (the larger-batch loop) */
+    MARKOV_PATH_CHAIN = 1,      /* the persistent single-launch chain kernel (tcgen05, head
+                                   resident in TMEM and shared memory when it fits) */
+    MARKOV_PATH_BATCH = 2,      /* per-position kernels (the larger-batch loop) */
+    MARKOV_PATH_CHAIN_SIMPLE = 3 /* the persistent chain with mma.sync bias tiles and the
+                                   head re-read from L2 each position: the fallback when
+                                   the head does not fit on chip */
 } markov_path;
 
 /* Static configuration of a plan.  vocab % 16 == 0 and vocab <= 262144

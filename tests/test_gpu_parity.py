@@ -11,7 +11,7 @@ from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
 
-AUTO, CHAIN, BATCH = 0, 1, 2
+AUTO, CHAIN, BATCH, SIMPLE = 0, 1, 2, 3
 
 SMALL = [
     W.small(16, 64, 1, 1, W.GUMBEL, seed=1, temperatures=(1.0,)),
@@ -30,7 +30,7 @@ def _ids(ws):
     return [w.name.replace(" ", "_") for w in ws]
 
 
-@pytest.mark.parametrize("path", [CHAIN, BATCH])
+@pytest.mark.parametrize("path", [CHAIN, SIMPLE, BATCH])
 @pytest.mark.parametrize("w", SMALL, ids=_ids(SMALL))
 def test_small_parity(gpu_lib, w, path):
     inp = W.make_call(w)
@@ -63,7 +63,7 @@ def test_forced_chain_refuses_large_batch(gpu_lib):
     assert e.value.code == 2
 
 
-@pytest.mark.parametrize("path", [CHAIN, BATCH])
+@pytest.mark.parametrize("path", [CHAIN, SIMPLE, BATCH])
 def test_max_vocab_and_steps(gpu_lib, path):
     w = W.small(262144, 64, 2, 16, W.GUMBEL, seed=11, temperatures=(0.0, 1.0))
     inp = W.make_call(w)
@@ -72,7 +72,7 @@ def test_max_vocab_and_steps(gpu_lib, path):
     assert rep.ok(), rep.summary()
 
 
-@pytest.mark.parametrize("path", [CHAIN, BATCH])
+@pytest.mark.parametrize("path", [CHAIN, SIMPLE, BATCH])
 def test_infinities_and_empty_rows(gpu_lib, path):
     # row 0: every logit -inf (inverse CDF takes id 0); row 1: +inf at two
     # ids (the lowest wins); row 2: a NaN after a +inf (NaN first); row 3:
@@ -110,7 +110,7 @@ def test_closed_form_chain_on_gpu(gpu_lib):
     w = W.small(V, r, 3, N, W.GUMBEL, seed=13, temperatures=(0.0,))
     inp = W.make_call(w)
     inp["base"] = torch.zeros_like(inp["base"])
-    for path in (CHAIN, BATCH):
+    for path in (CHAIN, SIMPLE, BATCH):
         toks, _ = U.run(gpu_lib, w, inp, path, head=head.to(torch.bfloat16).cuda(),
                         embed=embed.to(torch.bfloat16).cuda())
         for b in range(3):
@@ -143,11 +143,12 @@ def test_repeated_calls_are_deterministic(gpu_lib):
     plan.close()
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 4, 5])
-def test_full_workload_parity(gpu_lib, cfg):
+@pytest.mark.parametrize("cfg,path", [(1, AUTO), (2, AUTO), (4, AUTO), (5, AUTO), (2, SIMPLE),
+                                      (4, SIMPLE)])
+def test_full_workload_parity(gpu_lib, cfg, path):
     w = W.CONFIGS[cfg]
     inp = W.make_call(w)
-    toks, cache = U.run(gpu_lib, w, inp, AUTO)
+    toks, cache = U.run(gpu_lib, w, inp, path)
     rep = U.check(w, inp, toks, cache)
     print(cfg, rep.summary())
     assert rep.ok(), rep.summary()
@@ -165,6 +166,20 @@ def test_latency_workload_calls(gpu_lib):
         rep = U.check(w, inp, toks, cache)
         assert rep.ok(), (call, rep.summary())
     plan.close()
+
+
+def test_tcgen05_chain_takes_the_chain_workloads(gpu_lib):
+    # the head of every chain workload fits on chip: the chain path runs the
+    # tcgen05 kernel and reports the whole head resident
+    for cfg in (1, 2, 3, 4):
+        w = W.CONFIGS[cfg]
+        plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+        assert plan.query(gpu_lib.Q_RESIDENT_HEAD_BYTES) == w.vocab * w.rank * 2
+        inp = W.make_call(w)
+        U.run(gpu_lib, w, inp, AUTO, plan=plan)
+        assert plan.query(gpu_lib.Q_LAST_PATH) == CHAIN
+        assert plan.query(gpu_lib.Q_LAST_LAUNCHES) == 1
+        plan.close()
 
 
 def test_bad_arguments_launch_nothing(gpu_lib):
