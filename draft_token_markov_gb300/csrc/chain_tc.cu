@@ -71,7 +71,9 @@ struct Ctl {
     int live[kChainRows];
     int sampling[kChainRows];
     float T[kChainRows];
+    float invT[kChainRows];          // 1 / T, only for bounds
     uint64_t seed[kChainRows];
+    uint64_t hri[kChainRows];        // row-step hash of the current position
     int64_t prev[kChainRows];
 };
 
@@ -80,9 +82,20 @@ __device__ __forceinline__ void fail(Ctl &c, const SampleArgs &a, uint32_t code,
     c.abort = 1u;
 }
 
-__device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &a) {
-    return *(volatile const uint32_t *)&c.abort != 0u ||
-           ld_acquire_u32(a.status) != 0u;
+// This CTA's abort flag (shared memory: cheap enough for hot loops).
+__device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &) {
+    return *(volatile const uint32_t *)&c.abort != 0u;
+}
+
+// At a CTA barrier: this CTA's flag, or (thread 0 only, one L2 load) an
+// error another CTA recorded.
+__device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a) {
+    bool s = *(volatile const uint32_t *)&c.abort != 0u;
+    if (threadIdx.x == 0 && !s && ld_acquire_u32(a.status) != 0u) {
+        c.abort = 1u;
+        s = true;
+    }
+    return s;
 }
 
 // packed key: ordered key (32) | 0x3FFFF - id (18) | epoch tag (14)
@@ -139,6 +152,27 @@ __device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__rest
 
 }  // namespace
 
+namespace {
+
+// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash.
+__device__ __forceinline__ float exact_key(float l, float T, uint64_t h) {
+    const float x = (T == 1.0f) ? l : __fdiv_rn(l, T);
+    return __fadd_rn(x, dm_gumbel_from_hash(h));
+}
+
+// An upper bound on gumbel = -log(-log u) for the u of hash h, from the fast
+// hardware log2 (relative error far below the 0.01 margin on every u it is
+// used for); 17 bounds every value the hash can produce (u <= 1 - 2^-24).
+__device__ __forceinline__ float gumbel_upper(uint64_t h) {
+    const uint32_t m = (uint32_t)(h >> 41);
+    const float u = __fsub_rn(__uint_as_float(0x3f800000u | m), 0x1.fffffep-1f);
+    if (u > 0.999f) return 17.0f;
+    const float w = -__log2f(u) * 0.6931472f;
+    return -__log2f(w) * 0.6931472f + 0.01f;
+}
+
+}  // namespace
+
 template <int RANK>
 __global__ void __launch_bounds__(kThreads, 1)
 chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, int noise_ready) {
@@ -188,6 +222,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         c.T[b] = T;
         c.sampling[b] = live && samples(T);
         c.seed[b] = live ? (uint64_t)a.seeds[b] : 0ull;
+        c.invT[b] = samples(T) ? 1.0f / T : 1.0f;
+        c.hri[b] = dm_row_step_hash(c.seed[b], (uint32_t)b, 0u);
         int64_t p = live ? (int64_t)a.anchor[b] : 0;
         if (p < 0 || p >= V) {
             set_status(a.status, 1u /* MARKOV_EINVAL */, 0x100u + b);
@@ -221,6 +257,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (lane == 0) {
                 const int w = warp;
                 const uint32_t d = tmem + kDCol + 16u * w;
+                const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
                 for (int k = w; k < nt; k += 2) {
                     if (aborted(c, a)) break;
                     if (uses > 0 && !tc::mbar_wait(tc::smem_u32(&c.dfree[w]), (uses - 1) & 1u,
@@ -252,16 +289,20 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                             }
                             if (!ok) { fail(c, a, 4u, 0x2000u + j); break; }
                         }
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t bd = tc::sw128_desc(b_sa + kc * kBChunkBytes + 32 * ks);
-                            const uint32_t acc = (kc | ks) != 0;
-                            if (j < kTmemChunks)
-                                tc::mma_tmemA(d, tmem + 32u * j + 8u * ks, bd, kIdesc, acc);
-                            else
-                                tc::mma_smemA(d, tc::sw128_desc(head_sa + (j - kTmemChunks) * kChunkBytes +
-                                                                32 * ks),
-                                              bd, kIdesc, acc);
+                        // descriptors advance by (bytes >> 4) in their address field
+                        const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
+                        if (j < kTmemChunks) {
+                            const uint32_t at = tmem + 32u * j;
+                            tc::mma_tmemA(d, at, bd, kIdesc, kc != 0);
+                            tc::mma_tmemA(d, at + 8u, bd + 2u, kIdesc, 1u);
+                            tc::mma_tmemA(d, at + 16u, bd + 4u, kIdesc, 1u);
+                            tc::mma_tmemA(d, at + 24u, bd + 6u, kIdesc, 1u);
+                        } else {
+                            const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
+                            tc::mma_smemA(d, ad, bd, kIdesc, kc != 0);
+                            tc::mma_smemA(d, ad + 2u, bd + 2u, kIdesc, 1u);
+                            tc::mma_smemA(d, ad + 4u, bd + 4u, kIdesc, 1u);
+                            tc::mma_smemA(d, ad + 6u, bd + 6u, kIdesc, 1u);
                         }
                     }
                     if (!ok) break;
@@ -319,41 +360,58 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             __syncwarp();
         } else {
-            // warps 4..15: at position 0 the noise of every position, then the epilogue
-            if (i == 0) {
-                const int t384 = tid - 128;
-                if (warp >= 12) {
-                    // warm L2 with this CTA's base-logit slices of every position
-                    for (int b = 0; b < R && b < kChainRows; ++b) {
-                        if (!c.live[b]) continue;
-                        for (int i2 = 0; i2 < N; ++i2) {
-                            const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
-                            for (int v = v_begin + (t384 - 256) * 64; v < v_end; v += 128 * 64)
-                                tc::prefetch_l2(row + v);
-                        }
+            if (i == 0 && warp >= 12) {
+                // warm L2 with this CTA's base-logit slices of every position
+                const int t128 = tid - 384;
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.live[b]) continue;
+                    for (int i2 = 0; i2 < N; ++i2) {
+                        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
+                        for (int v = v_begin + t128 * 64; v < v_end; v += 128 * 64)
+                            tc::prefetch_l2(row + v);
                     }
                 }
-                if (a.mode == 0 && !noise_ready) {
-                    for (int b = 0; b < R && b < kChainRows; ++b) {
-                        if (!c.sampling[b]) continue;
-                        for (int i2 = 0; i2 < N; ++i2) {
-                            const uint64_t hri = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
-                            float *dst = a.noise + (int64_t)(b * N + i2) * a.noise_s0;
-                            for (int v = v_begin + t384; v < v_end; v += 384)
-                                dst[v] = dm_gumbel(hri, (uint32_t)v);
-                        }
-                    }
-                }
-                asm volatile("bar.sync 1, 384;" ::: "memory");
             }
             if (warp < 12) {
+                // Epilogue of accumulator wg.  Gumbel rows draw their noise here,
+                // on demand: per warp, row and tile the id with the largest logit
+                // gets its exact key first, a lower bound L on the row's best
+                // key; any other id whose key is provably below L (its logit /
+                // T plus an upper bound on its Gumbel value) cannot be the
+                // maximum and gets no exact key.  The maximum, and so the token,
+                // is exactly that of keys computed for every id.
                 const int wg = (warp - 4) >> 2, q = warp & 3;
-                uint64_t best[kChainRows];
+                uint32_t live_m = 0u, samp_m = 0u;
 #pragma unroll
-                for (int b = 0; b < kChainRows; ++b) best[b] = 0ull;
+                for (int b = 0; b < kChainRows; ++b) {
+                    live_m |= c.live[b] ? (1u << b) : 0u;
+                    samp_m |= c.sampling[b] ? (1u << b) : 0u;
+                }
+                const bool gumbel = a.mode == 0;
+                uint64_t best[kChainRows];
+                float Lb[kChainRows];
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) {
+                    best[b] = 0ull;
+                    Lb[b] = __uint_as_float(0xff800000u);
+                }
+                uint32_t nb[kChainRows];
+                auto load_tile = [&](int k, uint32_t (&bb)[kChainRows]) {
+                    const int v = (t0 + k) * 128 + q * 32 + lane;
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) {
+                        bb[b] = 0u;
+                        if (k < nt && v < V && ((live_m >> b) & 1u))
+                            bb[b] = __ldg(a.base + b * a.base_s0 + (int64_t)i * a.base_s1 + v);
+                    }
+                };
+                load_tile(wg, nb);
                 for (int k = wg; k < nt; k += 2) {
-                    const bool ab = __shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0);
-                    if (ab) break;
+                    uint32_t cb[kChainRows];
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) cb[b] = nb[b];
+                    load_tile(k + 2, nb);
+                    if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) break;
                     bool ok = true;
                     if (lane == 0)
                         ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u,
@@ -372,20 +430,54 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
                     const int v = (t0 + k) * 128 + q * 32 + lane;
-                    if (v < V) {
+                    const bool valid = v < V;
 #pragma unroll
-                        for (int b = 0; b < kChainRows; ++b) {
-                            if (!c.live[b]) continue;
-                            const uint32_t bb = a.base[b * a.base_s0 + (int64_t)i * a.base_s1 + v];
-                            const uint32_t l = logit_bits(bb, __uint_as_float(r[b]), a.tf);
+                    for (int b = 0; b < kChainRows; ++b) {
+                        if (!((live_m >> b) & 1u)) continue;
+                        uint32_t l = 0u;
+                        if (valid) {
+                            l = logit_bits(cb[b], __uint_as_float(r[b]), a.tf);
                             a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
-                            float key = dm_bf16_f32(l);
-                            if (c.sampling[b]) {
-                                const float T = c.T[b];
-                                if (T != 1.0f) key = __fdiv_rn(key, T);
-                                if (a.mode == 0)
-                                    key = __fadd_rn(key, a.noise[(int64_t)(b * N + i) * a.noise_s0 + v]);
+                        }
+                        const float lf = dm_bf16_f32(l);
+                        const float T = c.T[b];
+                        if (!(gumbel && ((samp_m >> b) & 1u))) {
+                            if (valid) {
+                                float key = lf;
+                                if (((samp_m >> b) & 1u) && T != 1.0f) key = __fdiv_rn(key, T);
+                                const uint64_t pk = pack_tc(key, (uint32_t)v);
+                                best[b] = pk > best[b] ? pk : best[b];
                             }
+                            continue;
+                        }
+                        const uint64_t hri = c.hri[b];
+                        const uint32_t o = valid ? ordered_key(lf) : 0u;
+                        const uint32_t omax = __reduce_max_sync(0xffffffffu, o);
+                        const uint32_t lead = __ballot_sync(0xffffffffu, valid && o == omax);
+                        const int leader = lead ? __ffs(lead) - 1 : -1;
+                        float key = 0.0f;
+                        bool have = false;
+                        if (lane == leader) {
+                            key = exact_key(lf, T, dm_splitmix64(hri ^ (uint64_t)v));
+                            have = true;
+                        }
+                        if (leader >= 0) {
+                            const float kl = __shfl_sync(0xffffffffu, key, leader);
+                            Lb[b] = (kl != kl || Lb[b] != Lb[b]) ? __uint_as_float(0x7fffffffu)
+                                                                 : fmaxf(Lb[b], kl);
+                        }
+                        if (valid && lane != leader) {
+                            const float xa = (T == 1.0f) ? lf : lf * c.invT[b];
+                            const float xu = xa + fabsf(xa) * 1e-5f;
+                            if (!(xu + 17.0f < Lb[b])) {
+                                const uint64_t h = dm_splitmix64(hri ^ (uint64_t)v);
+                                if (!(xu + gumbel_upper(h) < Lb[b])) {
+                                    key = exact_key(lf, T, h);
+                                    have = true;
+                                }
+                            }
+                        }
+                        if (have) {
                             const uint64_t pk = pack_tc(key, (uint32_t)v);
                             best[b] = pk > best[b] ? pk : best[b];
                         }
@@ -403,7 +495,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 }
             }
         }
-        stop = __syncthreads_or(aborted(c, a));
+        stop = __syncthreads_or(stop_vote(c, a));
         if (stop) break;
 
         // ------------------------------- phase B: agree on every row's winner
@@ -432,7 +524,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 }
             }
         }
-        stop = __syncthreads_or(aborted(c, a));
+        stop = __syncthreads_or(stop_vote(c, a));
         if (stop) break;
 
         // inverse CDF: rows whose maximum M is finite need the exact integer
@@ -511,7 +603,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                 }
             }
-            stop = __syncthreads_or(aborted(c, a));
+            stop = __syncthreads_or(stop_vote(c, a));
             if (stop) break;
             for (int b = 0; b < R && b < kChainRows; ++b) {
                 if (!c.sampling[b]) continue;
@@ -582,7 +674,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         fail(c, a, 6u, 0xA000u + i);
                 }
             }
-            stop = __syncthreads_or(aborted(c, a));
+            stop = __syncthreads_or(stop_vote(c, a));
             if (stop) break;
         }
 
@@ -600,9 +692,11 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
         }
+        if (tid < kChainRows && i + 1 < N)
+            c.hri[tid] = dm_row_step_hash(c.seed[tid], (uint32_t)tid, (uint32_t)(i + 1));
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
-        stop = __syncthreads_or(aborted(c, a));
+        stop = __syncthreads_or(stop_vote(c, a));
         tc::fence_after_sync();
     }
 
@@ -623,7 +717,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
-    if (cta == 0 && tid == 0 && !aborted(c, a))
+    if (cta == 0 && tid == 0 && !aborted(c, a) && ld_acquire_u32(a.status) == 0u)
         *(volatile uint32_t *)a.call_counter = c.call + 1u;
 }
 
