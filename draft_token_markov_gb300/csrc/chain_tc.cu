@@ -61,6 +61,8 @@ struct Ctl {
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
     uint64_t win[kChainRows];
+    unsigned long long lmax[kChainRows];   // per row: packed (largest logit, id) of this CTA
+    float L[kChainRows];                   // per row: exact key of that id (a lower bound)
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
     uint64_t tot, pre;
@@ -154,8 +156,21 @@ __device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__rest
 
 namespace {
 
-// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash.
-__device__ __forceinline__ float exact_key(float l, float T, uint64_t h) {
+// One byte per id holding an upper bound on its Gumbel value:
+// q = ceil((bound + 4) * 12) (every Gumbel value the hash can give lies in
+// (-3, 17), so q fits a byte); q / 12 - 4 >= bound >= the exact value.
+__device__ __forceinline__ uint32_t quantize_upper(float g_up) {
+    const float t = ceilf(__fmul_rn(__fadd_rn(g_up, 4.0f), 12.0f));
+    return t < 0.0f ? 0u : (t > 255.0f ? 255u : (uint32_t)t);
+}
+__device__ __forceinline__ float dequantize_upper(uint32_t q) {
+    return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f) + 0.001f;
+}
+
+// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash
+// (out of line: few ids reach it, and inlining it everywhere would bloat the
+// kernel past the instruction cache).
+__device__ __noinline__ float exact_key(float l, float T, uint64_t h) {
     const float x = (T == 1.0f) ? l : __fdiv_rn(l, T);
     return __fadd_rn(x, dm_gumbel_from_hash(h));
 }
@@ -166,9 +181,9 @@ __device__ __forceinline__ float exact_key(float l, float T, uint64_t h) {
 __device__ __forceinline__ float gumbel_upper(uint64_t h) {
     const uint32_t m = (uint32_t)(h >> 41);
     const float u = __fsub_rn(__uint_as_float(0x3f800000u | m), 0x1.fffffep-1f);
-    if (u > 0.999f) return 17.0f;
     const float w = -__log2f(u) * 0.6931472f;
-    return -__log2f(w) * 0.6931472f + 0.01f;
+    const float g = -__log2f(w) * 0.6931472f + 0.01f;
+    return u > 0.999f ? 17.0f : g;   // branch-free
 }
 
 }  // namespace
@@ -254,61 +269,67 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     for (int i = 0; i < N && !stop; ++i) {
         // ------------------------------------- phase A: MMA and epilogue
         if (warp < 2) {
-            if (lane == 0) {
-                const int w = warp;
-                const uint32_t d = tmem + kDCol + 16u * w;
-                const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
-                for (int k = w; k < nt; k += 2) {
-                    if (aborted(c, a)) break;
-                    if (uses > 0 && !tc::mbar_wait(tc::smem_u32(&c.dfree[w]), (uses - 1) & 1u,
-                                                   tc::now_ns() + timeout)) {
-                        fail(c, a, 4u, 0x1000u + i);
-                        break;
-                    }
-                    tc::fence_after_sync();
-                    bool ok = true;
-                    for (int kc = 0; kc < cpt && ok; ++kc) {
-                        const int j = k * cpt + kc;
-                        if (i == 0) {
-                            const uint64_t dl = tc::now_ns() + timeout;
-                            if (j < kTmemChunks) {
-                                while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
-                                    if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
-                                }
-                                tc::fence_after_sync();
-                            } else {
-                                // a parity wait only tells phases apart one at a time:
-                                // every earlier load of this slot (the TMEM chunks
-                                // staged in it) must be complete first
-                                while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
-                                    if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
-                                }
-                                const int s = j - kTmemChunks;
-                                const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
-                                if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
-                            }
-                            if (!ok) { fail(c, a, 4u, 0x2000u + j); break; }
-                        }
-                        // descriptors advance by (bytes >> 4) in their address field
-                        const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
-                        if (j < kTmemChunks) {
-                            const uint32_t at = tmem + 32u * j;
-                            tc::mma_tmemA(d, at, bd, kIdesc, kc != 0);
-                            tc::mma_tmemA(d, at + 8u, bd + 2u, kIdesc, 1u);
-                            tc::mma_tmemA(d, at + 16u, bd + 4u, kIdesc, 1u);
-                            tc::mma_tmemA(d, at + 24u, bd + 6u, kIdesc, 1u);
-                        } else {
-                            const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
-                            tc::mma_smemA(d, ad, bd, kIdesc, kc != 0);
-                            tc::mma_smemA(d, ad + 2u, bd + 2u, kIdesc, 1u);
-                            tc::mma_smemA(d, ad + 4u, bd + 4u, kIdesc, 1u);
-                            tc::mma_smemA(d, ad + 6u, bd + 6u, kIdesc, 1u);
-                        }
-                    }
-                    if (!ok) break;
-                    tc::commit(tc::smem_u32(&c.dfull[w]));
-                    ++uses;
+            // the whole warp runs the issue loop; one elected lane issues
+            const int w = warp;
+            const uint32_t d = tmem + kDCol + 16u * w;
+            const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
+            for (int k = w; k < nt; k += 2) {
+                if (__any_sync(0xffffffffu, aborted(c, a))) break;
+                bool freed = true;
+                if (uses > 0)
+                    freed = tc::mbar_wait(tc::smem_u32(&c.dfree[w]), (uses - 1) & 1u,
+                                          tc::now_ns() + timeout);
+                if (!__all_sync(0xffffffffu, freed)) {
+                    if (lane == 0) fail(c, a, 4u, 0x1000u + i);
+                    break;
                 }
+                tc::fence_after_sync();
+                bool ok = true;
+                for (int kc = 0; kc < cpt; ++kc) {
+                    const int j = k * cpt + kc;
+                    if (i == 0) {
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        if (j < kTmemChunks) {
+                            while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
+                                if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                            }
+                            tc::fence_after_sync();
+                        } else {
+                            // a parity wait only tells phases apart one at a time:
+                            // every earlier load of this slot (the TMEM chunks
+                            // staged in it) must be complete first
+                            while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
+                                if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                            }
+                            const int s = j - kTmemChunks;
+                            const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
+                            if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
+                        }
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) {
+                            if (lane == 0) fail(c, a, 4u, 0x2000u + j);
+                            break;
+                        }
+                    }
+                    // descriptors advance by (bytes >> 4) in their address field
+                    const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
+                    if (j < kTmemChunks) {
+                        const uint32_t at = tmem + 32u * j;
+                        tc::mma_tmemA_elect(d, at, bd, kIdesc, kc != 0);
+                        tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
+                        tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
+                        tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
+                    } else {
+                        const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
+                        tc::mma_smemA_elect(d, ad, bd, kIdesc, kc != 0);
+                        tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
+                        tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
+                        tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
+                    }
+                }
+                if (!ok) break;
+                tc::commit_elect(tc::smem_u32(&c.dfull[w]));
+                ++uses;
             }
             __syncwarp();
         } else if (warp == 2) {
@@ -360,59 +381,102 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             __syncwarp();
         } else {
-            if (i == 0 && warp >= 12) {
-                // warm L2 with this CTA's base-logit slices of every position
-                const int t128 = tid - 384;
-                for (int b = 0; b < R && b < kChainRows; ++b) {
-                    if (!c.live[b]) continue;
-                    for (int i2 = 0; i2 < N; ++i2) {
-                        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
-                        for (int v = v_begin + t128 * 64; v < v_end; v += 128 * 64)
-                            tc::prefetch_l2(row + v);
+            if (i == 0) {
+                const int t384 = tid - 128;
+                if (warp >= 12) {
+                    // warm L2 with this CTA's base-logit slices of every position
+                    const int t128 = tid - 384;
+                    for (int b = 0; b < R && b < kChainRows; ++b) {
+                        if (!c.live[b]) continue;
+                        for (int i2 = 0; i2 < N; ++i2) {
+                            const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
+                            for (int v = v_begin + t128 * 64; v < v_end; v += 128 * 64)
+                                tc::prefetch_l2(row + v);
+                        }
                     }
                 }
+                if (a.mode == 0) {
+                    // the noise bound of every Gumbel (row, position, id) of this
+                    // CTA, while the head streams in; the noise itself depends on
+                    // seeds and positions only, never on the chain
+                    uint8_t *gq = reinterpret_cast<uint8_t *>(a.noise);
+                    for (int b = 0; b < R && b < kChainRows; ++b) {
+                        if (!c.sampling[b]) continue;
+                        for (int i2 = 0; i2 < N; ++i2) {
+                            const uint64_t hri = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
+                            uint8_t *dst = gq + (int64_t)(b * N + i2) * V;
+                            for (int v = v_begin + t384; v < v_end; v += 4 * 384) {
+                                uint32_t qv[4];
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    qv[u] = quantize_upper(gumbel_upper(dm_splitmix64(hri ^ (uint64_t)(v + u * 384))));
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    if (v + u * 384 < v_end) dst[v + u * 384] = (uint8_t)qv[u];
+                            }
+                        }
+                    }
+                }
+                asm volatile("bar.sync 2, 384;" ::: "memory");
             }
             if (warp < 12) {
-                // Epilogue of accumulator wg.  Gumbel rows draw their noise here,
-                // on demand: per warp, row and tile the id with the largest logit
-                // gets its exact key first, a lower bound L on the row's best
-                // key; any other id whose key is provably below L (its logit /
-                // T plus an upper bound on its Gumbel value) cannot be the
-                // maximum and gets no exact key.  The maximum, and so the token,
-                // is exactly that of keys computed for every id.
-                const int wg = (warp - 4) >> 2, q = warp & 3;
+                // Epilogue of accumulator wg, in two passes.
+                // Pass 1, as each tile's bias arrives: the cached logits, the
+                // keys of greedy and inverse-CDF rows, and for Gumbel rows the
+                // CTA's largest logit.  The exact key of that id is a lower
+                // bound L on the row's best key over this CTA.
+                // Pass 2, Gumbel rows: every id's key is bounded above by its
+                // logit / T plus an upper bound on its Gumbel value (the hash
+                // plus a fast logarithm); only ids whose bound reaches L can be
+                // the maximum, and only they get the exact key.  The maximum,
+                // and so the token, is exactly that of keys computed for every id.
+                constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per WG, at most
+                const int wg = (warp - 4) >> 2, q = warp & 3, ew = warp - 4;
                 uint32_t live_m = 0u, samp_m = 0u;
 #pragma unroll
                 for (int b = 0; b < kChainRows; ++b) {
                     live_m |= c.live[b] ? (1u << b) : 0u;
                     samp_m |= c.sampling[b] ? (1u << b) : 0u;
                 }
-                const bool gumbel = a.mode == 0;
-                uint64_t best[kChainRows];
-                float Lb[kChainRows];
+                const uint32_t gum_m = a.mode == 0 ? (samp_m & live_m) : 0u;
+                if (tid == 128 && (gum_m != 0u)) {
 #pragma unroll
-                for (int b = 0; b < kChainRows; ++b) {
-                    best[b] = 0ull;
-                    Lb[b] = __uint_as_float(0xff800000u);
+                    for (int b = 0; b < kChainRows; ++b) c.lmax[b] = 0ull;
                 }
-                uint32_t nb[kChainRows];
-                auto load_tile = [&](int k, uint32_t (&bb)[kChainRows]) {
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                uint64_t best[kChainRows], lmax[kChainRows];
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) { best[b] = 0ull; lmax[b] = 0ull; }
+                uint16_t keep[kTilesWG][kChainRows];   // this thread's logits of its tiles
+                uint8_t keepq[kTilesWG][kChainRows];   // and their noise bounds
+                const uint8_t *gq = reinterpret_cast<const uint8_t *>(a.noise);
+                uint32_t nb[kChainRows], nq[kChainRows];
+                auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint32_t (&qq)[kChainRows]) {
                     const int v = (t0 + k) * 128 + q * 32 + lane;
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) {
                         bb[b] = 0u;
-                        if (k < nt && v < V && ((live_m >> b) & 1u))
+                        qq[b] = 0u;
+                        if (k < nt && v < V && ((live_m >> b) & 1u)) {
                             bb[b] = __ldg(a.base + b * a.base_s0 + (int64_t)i * a.base_s1 + v);
+                            if ((gum_m >> b) & 1u) qq[b] = __ldcg(gq + (int64_t)(b * N + i) * V + v);
+                        }
                     }
                 };
-                load_tile(wg, nb);
-                for (int k = wg; k < nt; k += 2) {
+                load_tile(wg, nb, nq);
+                bool ok = true;
+#pragma unroll 1
+                for (int kk = 0; kk < kTilesWG; ++kk) {
+                    const int k = wg + 2 * kk;
+                    if (k >= nt) break;
                     uint32_t cb[kChainRows];
 #pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) cb[b] = nb[b];
-                    load_tile(k + 2, nb);
-                    if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) break;
-                    bool ok = true;
+                    for (int b = 0; b < kChainRows; ++b) {
+                        cb[b] = nb[b];
+                        keepq[kk][b] = (uint8_t)nq[b];
+                    }
+                    load_tile(k + 2, nb, nq);
+                    if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
                     if (lane == 0)
                         ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u,
                                            tc::now_ns() + timeout);
@@ -433,53 +497,81 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     const bool valid = v < V;
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) {
-                        if (!((live_m >> b) & 1u)) continue;
                         uint32_t l = 0u;
-                        if (valid) {
+                        if (valid && ((live_m >> b) & 1u)) {
                             l = logit_bits(cb[b], __uint_as_float(r[b]), a.tf);
                             a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
-                        }
-                        const float lf = dm_bf16_f32(l);
-                        const float T = c.T[b];
-                        if (!(gumbel && ((samp_m >> b) & 1u))) {
-                            if (valid) {
+                            const float lf = dm_bf16_f32(l);
+                            if ((gum_m >> b) & 1u) {
+                                const uint64_t pl = pack_tc(lf, (uint32_t)v);
+                                lmax[b] = pl > lmax[b] ? pl : lmax[b];
+                            } else {
                                 float key = lf;
-                                if (((samp_m >> b) & 1u) && T != 1.0f) key = __fdiv_rn(key, T);
+                                if (((samp_m >> b) & 1u) && c.T[b] != 1.0f) key = __fdiv_rn(key, c.T[b]);
                                 const uint64_t pk = pack_tc(key, (uint32_t)v);
                                 best[b] = pk > best[b] ? pk : best[b];
                             }
-                            continue;
                         }
-                        const uint64_t hri = c.hri[b];
-                        const uint32_t o = valid ? ordered_key(lf) : 0u;
-                        const uint32_t omax = __reduce_max_sync(0xffffffffu, o);
-                        const uint32_t lead = __ballot_sync(0xffffffffu, valid && o == omax);
-                        const int leader = lead ? __ffs(lead) - 1 : -1;
-                        float key = 0.0f;
-                        bool have = false;
-                        if (lane == leader) {
-                            key = exact_key(lf, T, dm_splitmix64(hri ^ (uint64_t)v));
-                            have = true;
+                        keep[kk][b] = (uint16_t)l;
+                    }
+                }
+                if (gum_m != 0u) {
+                    // the CTA's largest logit per Gumbel row, and its exact key
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) {
+                        if (!((gum_m >> b) & 1u)) continue;
+                        uint64_t m = lmax[b];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
+                            m = w2 > m ? w2 : m;
                         }
-                        if (leader >= 0) {
-                            const float kl = __shfl_sync(0xffffffffu, key, leader);
-                            Lb[b] = (kl != kl || Lb[b] != Lb[b]) ? __uint_as_float(0x7fffffffu)
-                                                                 : fmaxf(Lb[b], kl);
-                        }
-                        if (valid && lane != leader) {
-                            const float xa = (T == 1.0f) ? lf : lf * c.invT[b];
-                            const float xu = xa + fabsf(xa) * 1e-5f;
-                            if (!(xu + 17.0f < Lb[b])) {
-                                const uint64_t h = dm_splitmix64(hri ^ (uint64_t)v);
-                                if (!(xu + gumbel_upper(h) < Lb[b])) {
-                                    key = exact_key(lf, T, h);
-                                    have = true;
-                                }
+                        if (lane == 0 && m != 0ull) atomicMax(&c.lmax[b], (unsigned long long)m);
+                    }
+                    asm volatile("bar.sync 1, 256;" ::: "memory");
+                    if (warp == 4 && lane < kChainRows) {
+                        const int b = lane;
+                        if ((gum_m >> b) & 1u) {
+                            const uint64_t m = c.lmax[b];
+                            float Lv = __uint_as_float(0xff800000u);
+                            if (m != 0ull) {
+                                const uint32_t vm = unpack_id(m);
+                                const float lm = key_from_ordered((uint32_t)(m >> 32));
+                                Lv = exact_key(lm, c.T[b], dm_splitmix64(c.hri[b] ^ (uint64_t)vm));
                             }
+                            c.L[b] = Lv;
                         }
-                        if (have) {
-                            const uint64_t pk = pack_tc(key, (uint32_t)v);
-                            best[b] = pk > best[b] ? pk : best[b];
+                    }
+                    asm volatile("bar.sync 1, 256;" ::: "memory");
+                    if (ok) {
+                        // branch-free bounds for every row (independent hash chains
+                        // the scheduler interleaves), then exact keys for the rare
+                        // survivors
+#pragma unroll 1
+                        for (int kk = 0; kk < kTilesWG; ++kk) {
+                            const int k = wg + 2 * kk;
+                            if (k >= nt) break;
+                            const int v = (t0 + k) * 128 + q * 32 + lane;
+                            if (v >= V) continue;
+                            uint32_t surv = 0u;
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b) {
+                                const float lf = dm_bf16_f32(keep[kk][b]);
+                                const float T = c.T[b];
+                                const float xa = (T == 1.0f) ? lf : lf * c.invT[b];
+                                const float xu = xa + fabsf(xa) * 1e-5f;
+                                const bool in = ((gum_m >> b) & 1u) &&
+                                                !(xu + dequantize_upper(keepq[kk][b]) < c.L[b]);
+                                surv |= in ? (1u << b) : 0u;
+                            }
+                            while (surv != 0u) {
+                                const int b = __ffs(surv) - 1;
+                                surv &= surv - 1u;
+                                const float lf = dm_bf16_f32(keep[kk][b]);
+                                const uint64_t h = dm_splitmix64(c.hri[b] ^ (uint64_t)v);
+                                const uint64_t pk = pack_tc(exact_key(lf, c.T[b], h), (uint32_t)v);
+                                best[b] = pk > best[b] ? pk : best[b];
+                            }
                         }
                     }
                 }
@@ -491,7 +583,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
                         m = w2 > m ? w2 : m;
                     }
-                    if (lane == 0) c.wbest[warp - 4][b] = m;
+                    if (lane == 0) c.wbest[ew][b] = m;
                 }
             }
         }
@@ -702,8 +794,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
 
     // --------------------------------------------------------------- exit
     // every async operation of this CTA completes before TMEM is released
-    if (warp < 2 && lane == 0) {
-        tc::commit(tc::smem_u32(&c.fin[warp]));
+    if (warp < 2) {
+        __syncwarp();
+        tc::commit_elect(tc::smem_u32(&c.fin[warp]));
         tc::mbar_wait(tc::smem_u32(&c.fin[warp]), 0u, tc::now_ns() + 1000000000ull);
     }
     if (warp == 2 && lane == 0) {

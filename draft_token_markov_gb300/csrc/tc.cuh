@@ -144,6 +144,33 @@ __device__ __forceinline__ void mma_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// Warp-collective forms: the whole (converged) warp executes them and one
+// elected lane issues, so the surrounding loop stays warp-uniform.
+__device__ __forceinline__ void mma_tmemA_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 q, %4, 0; elect.sync _|p, 0xffffffff;\n"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_smemA_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p, q; setp.ne.u32 q, %4, 0; elect.sync _|p, 0xffffffff;\n"
+        "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q; }" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit_elect(uint32_t bar) {
+    asm volatile(
+        "{ .reg .pred p; elect.sync _|p, 0xffffffff;\n"
+        "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued before
 // has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
