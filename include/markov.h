@@ -156,6 +156,42 @@ markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits
                                   uint16_t *logit_cache, int64_t cache_s0,
                                   int64_t cache_s1, void *stream);
 
+/* markov_chain_sample without a plan, for callers that cannot allocate
+ * device memory: code running while a CUDA graph is captured on a stream
+ * that forbids allocation, servers and plugins that must draw every byte
+ * from their own pre-sized pool, processes whose allocator belongs to
+ * another runtime.  No counterpart on the documentation pages: it is an
+ * addition of this library.
+ *   Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   Its scratch (Gumbel noise, cross-CTA slots, barrier and status words)
+ *   is one file-scope device array of 33 MiB that every GPU loading the
+ *   library holds until the process exits; the calling thread's current
+ *   device is used.  The first call on a device looks up that array's
+ *   address (cudaGetSymbolAddress); make that first call before any stream
+ *   capture.
+ *   Arguments, layouts and results are those of markov_chain_sample with
+ *   vocab, rank and num_steps given directly; it runs the noise kernel and
+ *   the simple persistent chain (the MARKOV_PATH_CHAIN_SIMPLE path), so its
+ *   outputs equal that path's bit for bit.
+ *   Limits: rows <= 8, and rows * num_steps * vocab <= 8388608 (the noise
+ *   must fit 32 MiB); larger calls return MARKOV_EUNSUPPORTED before any
+ *   work is enqueued.  Every call clears the array's control words on
+ *   `stream` first.  All calls share the array, which keeps the last call's
+ *   contents: calls that may overlap on the GPU (other streams, other host
+ *   threads) race and must be serialized by the caller.  A device-side bounded
+ *   wait that gives up leaves that call's outputs incomplete; it is not
+ *   reported (markov_plan_status needs a plan). */
+markov_status markov_chain_sample_static(int32_t vocab, int32_t rank, int32_t num_steps,
+                                         const uint16_t *base_logits, int64_t base_s0,
+                                         int64_t base_s1, const uint16_t *head,
+                                         const uint16_t *embed, const int32_t *anchor_tokens,
+                                         const float *temperature, const int64_t *seeds,
+                                         const int64_t *row_state_idx, int32_t rows,
+                                         markov_mode mode, float output_multiplier,
+                                         float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
+                                         uint16_t *logit_cache, int64_t cache_s0,
+                                         int64_t cache_s1, void *stream);
+
 /* Synchronize the plan's device and return (then clear) the sticky device
  * status: MARKOV_OK, or MARKOV_ETIMEOUT when a bounded wait gave up, in
  * which case the plan's barrier words are re-zeroed so the next call starts
