@@ -41,7 +41,7 @@ namespace dtm {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 384;      // 12 warps: 4 control warps, 8 epilogue warps
 constexpr int kTmemChunks = 15;           // A chunks in TMEM (32 columns each)
 constexpr int kSmemChunks = 13;           // A chunks in shared memory (16 KB each)
 constexpr int kMaxChunks = kTmemChunks + kSmemChunks;
@@ -61,8 +61,7 @@ struct Ctl {
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
     uint64_t win[kChainRows];
-    unsigned long long lmax[kChainRows];   // per row: packed (largest logit, id) of this CTA
-    float L[kChainRows];                   // per row: exact key of that id (a lower bound)
+    unsigned int lbmax[kChainRows];        // per row: ordered max over this CTA of key lower bounds
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
     uint64_t tot, pre;
@@ -121,12 +120,7 @@ __device__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t de
             m = k > m ? k : m;
         }
         if (__all_sync(0xffffffffu, fresh)) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                uint64_t w = __shfl_xor_sync(0xffffffffu, m, o);
-                m = w > m ? w : m;
-            }
-            out = m;
+            out = tc::warp_max_u64(m);
             return true;
         }
         if ((spin & 15u) == 15u) {
@@ -165,6 +159,13 @@ __device__ __forceinline__ uint32_t quantize_upper(float g_up) {
 }
 __device__ __forceinline__ float dequantize_upper(uint32_t q) {
     return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f) + 0.001f;
+}
+// A lower bound on the Gumbel value from the same byte: the fast estimate
+// lies within 1e-4 of the exact value and q - 1 < (estimate + 0.01 + 4) 12,
+// so the value exceeds (q - 1) / 12 - 4 - 0.0101.  q = 252 is the 17 cap of
+// u > 0.999, whose values exceed -log(-log 0.999) = 6.907.
+__device__ __forceinline__ float dequantize_lower(uint32_t q) {
+    return q == 252u ? 6.88f : __fmaf_rn((float)q - 1.0f, 1.0f / 12.0f, -4.0f) - 0.02f;
 }
 
 // The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash
@@ -381,56 +382,56 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             __syncwarp();
         } else {
+            // warps 4..11
+            const int t256 = tid - 128;
             if (i == 0) {
-                const int t384 = tid - 128;
-                if (warp >= 12) {
-                    // warm L2 with this CTA's base-logit slices of every position
-                    const int t128 = tid - 384;
-                    for (int b = 0; b < R && b < kChainRows; ++b) {
-                        if (!c.live[b]) continue;
-                        for (int i2 = 0; i2 < N; ++i2) {
-                            const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
-                            for (int v = v_begin + t128 * 64; v < v_end; v += 128 * 64)
-                                tc::prefetch_l2(row + v);
-                        }
+                // warm L2 with this CTA's base-logit slices of every position
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.live[b]) continue;
+                    for (int i2 = 0; i2 < N; ++i2) {
+                        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
+                        for (int v = v_begin + t256 * 64; v < v_end; v += 256 * 64)
+                            tc::prefetch_l2(row + v);
                     }
                 }
                 if (a.mode == 0) {
-                    // the noise bound of every Gumbel (row, position, id) of this
-                    // CTA, while the head streams in; the noise itself depends on
-                    // seeds and positions only, never on the chain
+                    // a one-byte bound on the noise of every Gumbel (row,
+                    // position, id) of this CTA, while the head streams in; the
+                    // noise depends on seeds and positions only, not on the chain
                     uint8_t *gq = reinterpret_cast<uint8_t *>(a.noise);
                     for (int b = 0; b < R && b < kChainRows; ++b) {
                         if (!c.sampling[b]) continue;
                         for (int i2 = 0; i2 < N; ++i2) {
                             const uint64_t hri = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
                             uint8_t *dst = gq + (int64_t)(b * N + i2) * V;
-                            for (int v = v_begin + t384; v < v_end; v += 4 * 384) {
+                            for (int v = v_begin + t256; v < v_end; v += 4 * 256) {
                                 uint32_t qv[4];
 #pragma unroll
                                 for (int u = 0; u < 4; ++u)
-                                    qv[u] = quantize_upper(gumbel_upper(dm_splitmix64(hri ^ (uint64_t)(v + u * 384))));
+                                    qv[u] = quantize_upper(gumbel_upper(dm_splitmix64(hri ^ (uint64_t)(v + u * 256))));
 #pragma unroll
                                 for (int u = 0; u < 4; ++u)
-                                    if (v + u * 384 < v_end) dst[v + u * 384] = (uint8_t)qv[u];
+                                    if (v + u * 256 < v_end) dst[v + u * 256] = (uint8_t)qv[u];
                             }
                         }
                     }
                 }
-                asm volatile("bar.sync 2, 384;" ::: "memory");
+                asm volatile("bar.sync 2, 256;" ::: "memory");
             }
-            if (warp < 12) {
-                // Epilogue of accumulator wg, in two passes.
-                // Pass 1, as each tile's bias arrives: the cached logits, the
-                // keys of greedy and inverse-CDF rows, and for Gumbel rows the
-                // CTA's largest logit.  The exact key of that id is a lower
-                // bound L on the row's best key over this CTA.
-                // Pass 2, Gumbel rows: every id's key is bounded above by its
-                // logit / T plus an upper bound on its Gumbel value (the hash
-                // plus a fast logarithm); only ids whose bound reaches L can be
-                // the maximum, and only they get the exact key.  The maximum,
-                // and so the token, is exactly that of keys computed for every id.
+            {
+                // Epilogue of accumulator wg, in two passes over this thread's
+                // ids (one per tile), their values kept in registers.
+                // Pass 1, as each tile's bias arrives: the cached logits and
+                // the keys of greedy and inverse-CDF rows; for Gumbel rows a
+                // lower bound on every id's key (logit / T plus the lower end
+                // of its noise byte), whose maximum over the CTA, L, is a lower
+                // bound on the row's best key.
+                // Pass 2, Gumbel rows: only ids whose key upper bound reaches L
+                // can be the maximum, and only they get the exact key, so the
+                // maximum (the token) is exactly that of keys computed for
+                // every id.
                 constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per WG, at most
+                constexpr bool kRegs = kTilesWG <= 4;                  // values kept in registers
                 const int wg = (warp - 4) >> 2, q = warp & 3, ew = warp - 4;
                 uint32_t live_m = 0u, samp_m = 0u;
 #pragma unroll
@@ -439,42 +440,37 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     samp_m |= c.sampling[b] ? (1u << b) : 0u;
                 }
                 const uint32_t gum_m = a.mode == 0 ? (samp_m & live_m) : 0u;
-                if (tid == 128 && (gum_m != 0u)) {
+                const uint8_t *gq = reinterpret_cast<const uint8_t *>(a.noise);
+                if (tid == 128) {
 #pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) c.lmax[b] = 0ull;
+                    for (int b = 0; b < kChainRows; ++b) c.lbmax[b] = 0u;
                 }
                 asm volatile("bar.sync 1, 256;" ::: "memory");
-                uint64_t best[kChainRows], lmax[kChainRows];
+                uint64_t best[kChainRows];
+                uint32_t lbm[kChainRows];
 #pragma unroll
-                for (int b = 0; b < kChainRows; ++b) { best[b] = 0ull; lmax[b] = 0ull; }
-                uint16_t keep[kTilesWG][kChainRows];   // this thread's logits of its tiles
-                uint8_t keepq[kTilesWG][kChainRows];   // and their noise bounds
-                const uint8_t *gq = reinterpret_cast<const uint8_t *>(a.noise);
+                for (int b = 0; b < kChainRows; ++b) { best[b] = 0ull; lbm[b] = 0u; }
+                uint32_t keep[kRegs ? kTilesWG : 1][kChainRows];   // logit | noise byte << 16
                 uint32_t nb[kChainRows], nq[kChainRows];
                 auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint32_t (&qq)[kChainRows]) {
                     const int v = (t0 + k) * 128 + q * 32 + lane;
+                    const bool ok2 = k < nt && v < V;
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) {
-                        bb[b] = 0u;
-                        qq[b] = 0u;
-                        if (k < nt && v < V && ((live_m >> b) & 1u)) {
-                            bb[b] = __ldg(a.base + b * a.base_s0 + (int64_t)i * a.base_s1 + v);
-                            if ((gum_m >> b) & 1u) qq[b] = __ldcg(gq + (int64_t)(b * N + i) * V + v);
-                        }
+                        const bool lv = ok2 && ((live_m >> b) & 1u);
+                        bb[b] = lv ? (uint32_t)__ldg(a.base + b * a.base_s0 + (int64_t)i * a.base_s1 + v) : 0u;
+                        qq[b] = (lv && ((gum_m >> b) & 1u)) ? (uint32_t)__ldcg(gq + (int64_t)(b * N + i) * V + v) : 0u;
                     }
                 };
                 load_tile(wg, nb, nq);
                 bool ok = true;
-#pragma unroll 1
+#pragma unroll
                 for (int kk = 0; kk < kTilesWG; ++kk) {
                     const int k = wg + 2 * kk;
-                    if (k >= nt) break;
-                    uint32_t cb[kChainRows];
+                    if (k >= nt || !ok) break;
+                    uint32_t cb[kChainRows], cq[kChainRows];
 #pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) {
-                        cb[b] = nb[b];
-                        keepq[kk][b] = (uint8_t)nq[b];
-                    }
+                    for (int b = 0; b < kChainRows; ++b) { cb[b] = nb[b]; cq[b] = nq[b]; }
                     load_tile(k + 2, nb, nq);
                     if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
                     if (lane == 0)
@@ -495,79 +491,94 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
                     const int v = (t0 + k) * 128 + q * 32 + lane;
                     const bool valid = v < V;
+                    // straight-line over the rows so their chains interleave
+                    uint32_t lb[kChainRows];
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) {
-                        uint32_t l = 0u;
-                        if (valid && ((live_m >> b) & 1u)) {
-                            l = logit_bits(cb[b], __uint_as_float(r[b]), a.tf);
-                            a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
-                            const float lf = dm_bf16_f32(l);
-                            if ((gum_m >> b) & 1u) {
-                                const uint64_t pl = pack_tc(lf, (uint32_t)v);
-                                lmax[b] = pl > lmax[b] ? pl : lmax[b];
-                            } else {
-                                float key = lf;
-                                if (((samp_m >> b) & 1u) && c.T[b] != 1.0f) key = __fdiv_rn(key, c.T[b]);
-                                const uint64_t pk = pack_tc(key, (uint32_t)v);
-                                best[b] = pk > best[b] ? pk : best[b];
-                            }
+                        const uint32_t bias = dm_bf16_bits(__uint_as_float(r[b]));
+                        lb[b] = dm_bf16_bits(__fadd_rn(dm_bf16_f32(cb[b]), dm_bf16_f32(bias)));
+                    }
+                    if (a.tf.has_transform) {
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b) {
+                            float y = __fmul_rn(dm_bf16_f32(lb[b]), a.tf.mult);
+                            if (a.tf.has_cap) y = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y, a.tf.inv_cap)));
+                            lb[b] = dm_bf16_bits(y);
                         }
-                        keep[kk][b] = (uint16_t)l;
+                    }
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b)
+                        if (valid && ((live_m >> b) & 1u))
+                            a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)lb[b];
+                    if (kRegs) {
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b) keep[kRegs ? kk : 0][b] = lb[b] | (cq[b] << 16);
+                    }
+                    float key[kChainRows];
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) key[b] = dm_bf16_f32(lb[b]);
+                    if (a.mode == 1) {
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b)
+                            if (((samp_m >> b) & 1u) && c.T[b] != 1.0f) key[b] = __fdiv_rn(key[b], c.T[b]);
+                    }
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) {
+                        const bool use = valid && ((live_m >> b) & 1u);
+                        if ((gum_m >> b) & 1u) {
+                            const float xa = key[b] * c.invT[b];
+                            const float xl = xa - fabsf(xa) * 1e-5f;
+                            const uint32_t o = ordered_key(xl + dequantize_lower(cq[b]));
+                            lbm[b] = (use && o > lbm[b]) ? o : lbm[b];
+                        } else {
+                            const uint64_t pk = pack_tc(key[b], (uint32_t)v);
+                            best[b] = (use && pk > best[b]) ? pk : best[b];
+                        }
                     }
                 }
                 if (gum_m != 0u) {
-                    // the CTA's largest logit per Gumbel row, and its exact key
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) {
-                        if (!((gum_m >> b) & 1u)) continue;
-                        uint64_t m = lmax[b];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
-                            m = w2 > m ? w2 : m;
-                        }
-                        if (lane == 0 && m != 0ull) atomicMax(&c.lmax[b], (unsigned long long)m);
-                    }
-                    asm volatile("bar.sync 1, 256;" ::: "memory");
-                    if (warp == 4 && lane < kChainRows) {
-                        const int b = lane;
-                        if ((gum_m >> b) & 1u) {
-                            const uint64_t m = c.lmax[b];
-                            float Lv = __uint_as_float(0xff800000u);
-                            if (m != 0ull) {
-                                const uint32_t vm = unpack_id(m);
-                                const float lm = key_from_ordered((uint32_t)(m >> 32));
-                                Lv = exact_key(lm, c.T[b], dm_splitmix64(c.hri[b] ^ (uint64_t)vm));
-                            }
-                            c.L[b] = Lv;
-                        }
+                        const uint32_t m = __reduce_max_sync(0xffffffffu, lbm[b]);
+                        if (lane == 0 && ((gum_m >> b) & 1u) && m != 0u) atomicMax(&c.lbmax[b], m);
                     }
                     asm volatile("bar.sync 1, 256;" ::: "memory");
                     if (ok) {
-                        // branch-free bounds for every row (independent hash chains
-                        // the scheduler interleaves), then exact keys for the rare
-                        // survivors
-#pragma unroll 1
+                        float Lr[kChainRows];
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b) Lr[b] = key_from_ordered(c.lbmax[b]);
+#pragma unroll
                         for (int kk = 0; kk < kTilesWG; ++kk) {
                             const int k = wg + 2 * kk;
                             if (k >= nt) break;
                             const int v = (t0 + k) * 128 + q * 32 + lane;
                             if (v >= V) continue;
+                            uint32_t kv[kChainRows];
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b) {
+                                if (kRegs) {
+                                    kv[b] = keep[kRegs ? kk : 0][b];
+                                } else {
+                                    const bool g = (gum_m >> b) & 1u;
+                                    const uint32_t lq = g ? (uint32_t)__ldcg(a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1 + v) : 0u;
+                                    const uint32_t qq = g ? (uint32_t)__ldcg(gq + (int64_t)(b * N + i) * V + v) : 0u;
+                                    kv[b] = lq | (qq << 16);
+                                }
+                            }
                             uint32_t surv = 0u;
 #pragma unroll
                             for (int b = 0; b < kChainRows; ++b) {
-                                const float lf = dm_bf16_f32(keep[kk][b]);
-                                const float T = c.T[b];
-                                const float xa = (T == 1.0f) ? lf : lf * c.invT[b];
+                                const float lf = dm_bf16_f32(kv[b] & 0xffffu);
+                                const float xa = lf * c.invT[b];
                                 const float xu = xa + fabsf(xa) * 1e-5f;
                                 const bool in = ((gum_m >> b) & 1u) &&
-                                                !(xu + dequantize_upper(keepq[kk][b]) < c.L[b]);
+                                                !(xu + dequantize_upper(kv[b] >> 16) < Lr[b]);
                                 surv |= in ? (1u << b) : 0u;
                             }
                             while (surv != 0u) {
                                 const int b = __ffs(surv) - 1;
                                 surv &= surv - 1u;
-                                const float lf = dm_bf16_f32(keep[kk][b]);
+                                const float lf = dm_bf16_f32(kv[b] & 0xffffu);
                                 const uint64_t h = dm_splitmix64(c.hri[b] ^ (uint64_t)v);
                                 const uint64_t pk = pack_tc(exact_key(lf, c.T[b], h), (uint32_t)v);
                                 best[b] = pk > best[b] ? pk : best[b];
@@ -577,12 +588,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 }
 #pragma unroll
                 for (int b = 0; b < kChainRows; ++b) {
-                    uint64_t m = best[b];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
-                        m = w2 > m ? w2 : m;
-                    }
+                    const uint64_t m = tc::warp_max_u64(best[b]);
                     if (lane == 0) c.wbest[ew][b] = m;
                 }
             }
@@ -595,12 +601,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         const uint32_t tag = epoch & 0x3FFFu;
         if (warp < kChainRows) {
             const int b = warp;
-            uint64_t m = lane < 8 ? c.wbest[lane][b] : 0ull;
-#pragma unroll
-            for (int o = 4; o > 0; o >>= 1) {
-                const uint64_t w2 = __shfl_xor_sync(0xffffffffu, m, o);
-                m = w2 > m ? w2 : m;
-            }
+            const uint64_t m = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b] : 0ull);
             uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * Gp;
             if (lane == 0) tc::st_relaxed_u64(slots + cta, (m & ~0x3FFFull) | tag);
             if (c.live[b]) {

@@ -41,9 +41,9 @@ __device__ __forceinline__ void set_status(uint32_t *status, uint32_t code, uint
 // +inf so that the lowest NaN id wins the maximum; -0 maps to +0.
 __device__ __forceinline__ uint32_t ordered_key(float k) {
     uint32_t b = __float_as_uint(k);
-    if ((b & 0x7fffffffu) > 0x7f800000u) return 0xffffffffu;   // NaN
-    if (b == 0x80000000u) b = 0u;                              // -0 == +0
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    b = (b == 0x80000000u) ? 0u : b;                           // -0 == +0
+    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((b & 0x7fffffffu) > 0x7f800000u) ? 0xffffffffu : o;   // NaN above all
 }
 
 __device__ __forceinline__ float key_from_ordered(uint32_t o) {

@@ -56,12 +56,34 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_test, but the thread may sleep (up to ~20 us) until the phase
+// completes instead of returning at once, so waiting warps leave the issue
+// slots to the warps that work.
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of the given parity; false after `deadline` (globaltimer ns).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t deadline) {
-    while (!mbar_test(bar, parity)) {
+    while (!mbar_test_sleep(bar, parity)) {
         if (now_ns() > deadline) return false;
     }
     return true;
+}
+
+// Warp maximum of a 64-bit key in two 32-bit reductions (high word, then
+// the low word among the lanes holding the highest high word).
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t x) {
+    const uint32_t hi = (uint32_t)(x >> 32), lo = (uint32_t)x;
+    const uint32_t hm = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t lm = __reduce_max_sync(0xffffffffu, hi == hm ? lo : 0u);
+    return ((uint64_t)hm << 32) | lm;
 }
 
 // ------------------------------------------------------------------ TMA
