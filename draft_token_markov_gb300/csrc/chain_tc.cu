@@ -52,6 +52,7 @@ constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
 constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
 constexpr uint32_t kSmemB = 4 * kBChunkBytes;
 constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
+constexpr int kSurvCap = 256;             // Gumbel survivors listed per CTA and position
 
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
@@ -60,6 +61,9 @@ struct Ctl {
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
+    unsigned long long gbest[kChainRows];  // Gumbel rows: this CTA's best packed key
+    uint32_t nsurv;                  // Gumbel ids left after the bound test
+    uint64_t surv[kSurvCap];         // (id << 32) | (row << 16) | cached logit
     uint64_t win[kChainRows];
     unsigned int lbmax[kChainRows];        // per row: ordered max over this CTA of key lower bounds
     unsigned long long sum[kChainRows];
@@ -74,7 +78,7 @@ struct Ctl {
     float T[kChainRows];
     float invT[kChainRows];          // 1 / T, only for bounds
     uint64_t seed[kChainRows];
-    uint64_t hri[kChainRows];        // row-step hash of the current position
+    uint64_t hri[kMaxSteps][kChainRows];   // row-step hash of every position
     int64_t prev[kChainRows];
 };
 
@@ -100,15 +104,12 @@ __device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a) {
 }
 
 // packed key: ordered key (32) | 0x3FFFF - id (18) | epoch tag (14)
-__device__ __forceinline__ uint64_t pack_tc(float key, uint32_t v) {
-    return ((uint64_t)ordered_key(key) << 32) | ((uint64_t)(0x3FFFFu - v) << 14);
-}
 __device__ __forceinline__ uint32_t unpack_id(uint64_t p) {
     return 0x3FFFFu - (uint32_t)((p >> 14) & 0x3FFFFu);
 }
 
 // Row b's maximum over all CTAs' slots, once every slot carries `tag`.
-__device__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t deadline,
+__device__ __forceinline__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t deadline,
                          const SampleArgs &a, uint64_t &out) {
     const int lane = threadIdx.x & 31;
     for (uint32_t spin = 0;; ++spin) {
@@ -125,6 +126,38 @@ __device__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t de
         }
         if ((spin & 15u) == 15u) {
             bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
+            if (__any_sync(0xffffffffu, bad)) return false;
+        }
+    }
+}
+
+// Two rows' maxima at once (a row that is not live is skipped).
+__device__ __forceinline__ bool poll_max2(const uint64_t *s0, const uint64_t *s1, bool l0, bool l1,
+                                          int G, uint32_t tag, uint64_t deadline,
+                                          const SampleArgs &a, uint64_t &o0, uint64_t &o1) {
+    const int lane = threadIdx.x & 31;
+    for (uint32_t spin = 0;; ++spin) {
+        bool fresh = true;
+        uint64_t m0 = 0ull, m1 = 0ull;
+        for (int c = lane; c < G; c += 32) {
+            if (l0) {
+                const uint64_t k = tc::ld_relaxed_u64(s0 + c);
+                fresh = fresh && (uint32_t)(k & 0x3FFFu) == tag;
+                m0 = k > m0 ? k : m0;
+            }
+            if (l1) {
+                const uint64_t k = tc::ld_relaxed_u64(s1 + c);
+                fresh = fresh && (uint32_t)(k & 0x3FFFu) == tag;
+                m1 = k > m1 ? k : m1;
+            }
+        }
+        if (__all_sync(0xffffffffu, fresh)) {
+            o0 = tc::warp_max_u64(m0);
+            o1 = tc::warp_max_u64(m1);
+            return true;
+        }
+        if ((spin & 15u) == 15u) {
+            const bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
             if (__any_sync(0xffffffffu, bad)) return false;
         }
     }
@@ -150,9 +183,9 @@ __device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__rest
 
 namespace {
 
-// One byte per id holding an upper bound on its Gumbel value:
-// q = ceil((bound + 4) * 12) (every Gumbel value the hash can give lies in
-// (-3, 17), so q fits a byte); q / 12 - 4 >= bound >= the exact value.
+// One byte per (position, id, row) holding an upper bound on the Gumbel
+// value: q = ceil((bound + 4) * 12).  Every value the hash can give lies in
+// (-2.8, 16.7), so q fits a byte; q / 12 - 4 >= bound >= the exact value.
 __device__ __forceinline__ uint32_t quantize_upper(float g_up) {
     const float t = ceilf(__fmul_rn(__fadd_rn(g_up, 4.0f), 12.0f));
     return t < 0.0f ? 0u : (t > 255.0f ? 255u : (uint32_t)t);
@@ -161,11 +194,10 @@ __device__ __forceinline__ float dequantize_upper(uint32_t q) {
     return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f) + 0.001f;
 }
 // A lower bound on the Gumbel value from the same byte: the fast estimate
-// lies within 1e-4 of the exact value and q - 1 < (estimate + 0.01 + 4) 12,
-// so the value exceeds (q - 1) / 12 - 4 - 0.0101.  q = 252 is the 17 cap of
-// u > 0.999, whose values exceed -log(-log 0.999) = 6.907.
+// lies within 2e-4 of the exact value and q - 1 < (estimate + 0.01 + 4) 12,
+// so the value exceeds (q - 1) / 12 - 4 - 0.0103.
 __device__ __forceinline__ float dequantize_lower(uint32_t q) {
-    return q == 252u ? 6.88f : __fmaf_rn((float)q - 1.0f, 1.0f / 12.0f, -4.0f) - 0.02f;
+    return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f - 1.0f / 12.0f - 0.02f);
 }
 
 // The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash
@@ -176,15 +208,305 @@ __device__ __noinline__ float exact_key(float l, float T, uint64_t h) {
     return __fadd_rn(x, dm_gumbel_from_hash(h));
 }
 
-// An upper bound on gumbel = -log(-log u) for the u of hash h, from the fast
-// hardware log2 (relative error far below the 0.01 margin on every u it is
-// used for); 17 bounds every value the hash can produce (u <= 1 - 2^-24).
+// An upper bound on gumbel = -log(-log u) for the u of hash h.  w = -ln u
+// from the hardware log2 (absolute error <= 2^-22 on [1/2, 2), 2 ulp
+// elsewhere) while u <= 0.999, where w >= 1e-3 keeps its relative error
+// below 2e-4; above, the series d + d^2/2 + d^3/3 of -ln(1 - d), d = 1 - u
+// (exact) <= 1e-3.  Then -ln w adds at most ~3e-6, so the estimate is within
+// 2e-4 of the exact value and the 0.01 margin makes it a bound.
 __device__ __forceinline__ float gumbel_upper(uint64_t h) {
     const uint32_t m = (uint32_t)(h >> 41);
     const float u = __fsub_rn(__uint_as_float(0x3f800000u | m), 0x1.fffffep-1f);
-    const float w = -__log2f(u) * 0.6931472f;
-    const float g = -__log2f(w) * 0.6931472f + 0.01f;
-    return u > 0.999f ? 17.0f : g;   // branch-free
+    const float d = __fsub_rn(1.0f, u);
+    const float ws = d * (1.0f + d * (0.5f + d * (1.0f / 3.0f)));
+    const float wl = -__log2f(u) * 0.6931472f;
+    const float w = u > 0.999f ? ws : wl;
+    return -__log2f(w) * 0.6931472f + 0.01f;
+}
+
+// The noise-bound bytes of position p for this CTA's ids, 8 row bytes per
+// id, written by the 256 threads of warps 4-11 (thread t256 takes ids
+// v_begin + t256 + 256 j, four at a time so that their hash and log chains
+// overlap).  The noise depends on seeds and positions only, so it is drawn
+// while the chain waits: position 0 while the head streams in, position
+// p + 1 while position p's winners are exchanged.
+__device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, int p,
+                                             uint32_t gum_m, int v_begin, int v_end, int t256) {
+    uint2 *gq = reinterpret_cast<uint2 *>(a.noise) + (int64_t)p * a.V;
+    uint64_t hr[kChainRows];
+#pragma unroll
+    for (int b = 0; b < kChainRows; ++b) hr[b] = c.hri[p][b];
+    for (int v0 = v_begin + t256; v0 < v_end; v0 += 4 * 256) {
+        uint32_t w[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            w[u][0] = 0u;
+            w[u][1] = 0u;
+        }
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) {
+            if (!((gum_m >> b) & 1u)) continue;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint64_t h = dm_splitmix64(hr[b] ^ (uint64_t)(v0 + 256 * u));
+                w[u][b >> 2] |= quantize_upper(gumbel_upper(h)) << (8 * (b & 3));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (v0 + 256 * u < v_end) gq[v0 + 256 * u] = make_uint2(w[u][0], w[u][1]);
+    }
+}
+
+// The epilogue of one position, run by warps 4-11: accumulator wg = 0 / 1
+// (warps 4-7 / 8-11) takes the even / odd tiles; warp quarter q of a group
+// reads TMEM lanes 32q..32q+31, so each thread owns one id per tile and the
+// 8 rows of that id (the MMA's N columns).
+//
+// Pass 1, as each tile's bias arrives: the cached logits (two rows per
+// packed BF16 conversion), written out and kept in registers; for rows whose
+// key is exact here (greedy rows, inverse-CDF rows) the running maximum key
+// with the lowest id; for Gumbel rows a lower bound on every id's key
+// (logit / T plus the lower end of its noise byte), whose maximum over the
+// CTA, L, is a lower bound on the row's best key.
+// Pass 2, Gumbel rows: only ids whose key upper bound reaches L can be the
+// maximum, and only they get the exact key, so the maximum (the token) is
+// exactly that of keys computed for every id.
+// Leaves each warp's per-row best packed key in c.wbest.
+template <int RANK, bool kCdf>
+__device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
+                                         const int i, const int t0, const int nt,
+                                         const uint64_t timeout, uint32_t &dcount) {
+    constexpr int cpt = RANK / 64;
+    constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
+    constexpr bool kRegs = kTilesWG <= 4;                  // tiles kept in registers
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wg = (warp - 4) >> 2, q = warp & 3, ew = warp - 4;
+    const int V = a.V;
+    uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;
+#pragma unroll
+    for (int b = 0; b < kChainRows; ++b) {
+        live_m |= c.live[b] ? (1u << b) : 0u;
+        samp_m |= c.sampling[b] ? (1u << b) : 0u;
+        div_m |= (c.sampling[b] && c.T[b] != 1.0f) ? (1u << b) : 0u;
+    }
+    // Gumbel rows get the bound treatment; inverse-CDF rows divide by T
+    const uint32_t gum_m = kCdf ? 0u : (samp_m & live_m);
+    div_m = kCdf ? (div_m & live_m) : 0u;
+    const uint2 *gq = reinterpret_cast<const uint2 *>(a.noise) + (int64_t)i * V;
+    const uint16_t *base_i = a.base + (int64_t)i * a.base_s1;
+    uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1;
+    if (tid == 128) {
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) {
+            c.lbmax[b] = 0u;
+            c.gbest[b] = 0ull;
+        }
+        c.nsurv = 0u;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+
+    uint32_t bo[kChainRows], bv[kChainRows];   // best ordered key and its id
+    float lbm[kChainRows];                      // Gumbel rows: maximum key lower bound
+#pragma unroll
+    for (int b = 0; b < kChainRows; ++b) {
+        bo[b] = 0u;
+        bv[b] = 0u;
+        lbm[b] = __uint_as_float(0xff800000u);
+    }
+    uint32_t keepl[kRegs ? kTilesWG : 1][kChainRows / 2];   // packed logits
+    uint2 keepq[kRegs ? kTilesWG : 1];                       // noise bytes
+    uint32_t nb[kChainRows];
+    uint2 nq;
+    auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint2 &qq) {
+        const int v = (t0 + k) * 128 + q * 32 + lane;
+        const bool ok2 = k < nt && v < V;
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b)
+            bb[b] = (ok2 && ((live_m >> b) & 1u)) ? (uint32_t)__ldg(base_i + b * a.base_s0 + v) : 0u;
+        qq = (ok2 && gum_m != 0u) ? __ldcg(gq + v) : make_uint2(0u, 0u);
+    };
+    load_tile(wg, nb, nq);
+    bool ok = true;
+#pragma unroll
+    for (int kk = 0; kk < kTilesWG; ++kk) {
+        const int k = wg + 2 * kk;
+        if (k >= nt || !ok) break;
+        uint32_t cb[kChainRows];
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) cb[b] = nb[b];
+        const uint2 cq = nq;
+        load_tile(k + 2, nb, nq);
+        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
+        if (lane == 0)
+            ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+            if (lane == 0) fail(c, a, 4u, 0x6000u + i);
+            break;
+        }
+        ++dcount;
+        tc::fence_after_sync();
+        uint32_t r[8];
+        tc::ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg, r);
+        tc::wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
+        const int v = (t0 + k) * 128 + q * 32 + lane;
+        const bool valid = v < V;
+        // bias = bf16(sum); logit = bf16(f32(base) + f32(bias)), two rows a time
+        uint32_t lp[kChainRows / 2];
+#pragma unroll
+        for (int j = 0; j < kChainRows / 2; ++j) {
+            const uint32_t bb = bf16x2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            const float s0 = __fadd_rn(__uint_as_float(cb[2 * j] << 16), __uint_as_float(bb << 16));
+            const float s1 = __fadd_rn(__uint_as_float(cb[2 * j + 1] << 16),
+                                       __uint_as_float(bb & 0xffff0000u));
+            lp[j] = bf16x2_rn(s0, s1);
+        }
+        if (a.tf.has_transform) {
+#pragma unroll
+            for (int j = 0; j < kChainRows / 2; ++j) {
+                float y0 = __fmul_rn(__uint_as_float(lp[j] << 16), a.tf.mult);
+                float y1 = __fmul_rn(__uint_as_float(lp[j] & 0xffff0000u), a.tf.mult);
+                if (a.tf.has_cap) {
+                    y0 = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y0, a.tf.inv_cap)));
+                    y1 = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y1, a.tf.inv_cap)));
+                }
+                lp[j] = bf16x2_rn(y0, y1);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b)
+            if (valid && ((live_m >> b) & 1u))
+                cache_i[b * a.cache_s0 + v] = (uint16_t)(lp[b >> 1] >> (16 * (b & 1)));
+        if (kRegs) {
+#pragma unroll
+            for (int j = 0; j < kChainRows / 2; ++j) keepl[kRegs ? kk : 0][j] = lp[j];
+            keepq[kRegs ? kk : 0] = cq;
+        }
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) {
+            const float lf = __uint_as_float((b & 1) ? (lp[b >> 1] & 0xffff0000u) : (lp[b >> 1] << 16));
+            if ((gum_m >> b) & 1u) {
+                const float xa = lf * c.invT[b];
+                const float xl = __fmaf_rn(fabsf(xa), -1e-5f, xa);
+                const uint32_t qb = ((b < 4 ? cq.x : cq.y) >> (8 * (b & 3))) & 0xffu;
+                const float kl = __fadd_rn(xl, dequantize_lower(qb));
+                lbm[b] = (valid && kl > lbm[b]) ? kl : lbm[b];
+            } else {
+                float key = lf;
+                if (kCdf && ((div_m >> b) & 1u)) key = __fdiv_rn(lf, c.T[b]);
+                const uint32_t o = ordered_key(key);
+                const bool better = valid && ((live_m >> b) & 1u) && o > bo[b];
+                bo[b] = better ? o : bo[b];
+                bv[b] = better ? (uint32_t)v : bv[b];
+            }
+        }
+    }
+    if (gum_m != 0u) {
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) {
+            if ((gum_m >> b) & 1u) {
+                const uint32_t m = __reduce_max_sync(0xffffffffu, ordered_key(lbm[b]));
+                if (lane == 0) atomicMax(&c.lbmax[b], m);
+            }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (ok) {
+            // the bound test; survivors go to a shared list
+            float Lr[kChainRows];
+#pragma unroll
+            for (int b = 0; b < kChainRows; ++b) Lr[b] = key_from_ordered(c.lbmax[b]);
+#pragma unroll
+            for (int kk = 0; kk < kTilesWG; ++kk) {
+                const int k = wg + 2 * kk;
+                if (k >= nt) break;
+                const int v = (t0 + k) * 128 + q * 32 + lane;
+                if (v >= V) continue;
+                uint32_t lp[kChainRows / 2];
+                uint2 qk;
+                if (kRegs) {
+#pragma unroll
+                    for (int j = 0; j < kChainRows / 2; ++j) lp[j] = keepl[kRegs ? kk : 0][j];
+                    qk = keepq[kRegs ? kk : 0];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kChainRows / 2; ++j) {
+                        const uint32_t l0 = ((gum_m >> (2 * j)) & 1u)
+                                                ? (uint32_t)__ldcg(cache_i + (2 * j) * a.cache_s0 + v)
+                                                : 0u;
+                        const uint32_t l1 = ((gum_m >> (2 * j + 1)) & 1u)
+                                                ? (uint32_t)__ldcg(cache_i + (2 * j + 1) * a.cache_s0 + v)
+                                                : 0u;
+                        lp[j] = l0 | (l1 << 16);
+                    }
+                    qk = __ldcg(gq + v);
+                }
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) {
+                    if (!((gum_m >> b) & 1u)) continue;
+                    const uint32_t l16 = (lp[b >> 1] >> (16 * (b & 1))) & 0xffffu;
+                    const float xa = __uint_as_float(l16 << 16) * c.invT[b];
+                    const float xu = __fmaf_rn(fabsf(xa), 1e-5f, xa);
+                    const uint32_t qb = ((b < 4 ? qk.x : qk.y) >> (8 * (b & 3))) & 0xffu;
+                    if (!(__fadd_rn(xu, dequantize_upper(qb)) < Lr[b])) {
+                        const uint32_t at = atomicAdd(&c.nsurv, 1u);
+                        if (at < (uint32_t)kSurvCap)
+                            c.surv[at] = ((uint64_t)v << 32) | ((uint64_t)b << 16) | l16;
+                    }
+                }
+            }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        // exact keys of the listed ids, one per thread (one code site)
+        const uint32_t ns = c.nsurv;
+        const int t256 = tid - 128;
+        for (int j = t256; j < (int)(ns < (uint32_t)kSurvCap ? ns : (uint32_t)kSurvCap); j += 256) {
+            const uint64_t e = c.surv[j];
+            const uint32_t v = (uint32_t)(e >> 32), b = (uint32_t)(e >> 16) & 7u;
+            const float lf = __uint_as_float((uint32_t)(e & 0xffffu) << 16);
+            const float T = c.T[b];
+            const float x = (T == 1.0f) ? lf : __fdiv_rn(lf, T);
+            const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
+            const uint32_t o = ordered_key(__fadd_rn(x, dm_gumbel_from_hash(h)));
+            atomicMax(&c.gbest[b], ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
+        }
+        if (ns > (uint32_t)kSurvCap && ok) {
+            // list overflow (bounds too loose to prune, e.g. non-finite
+            // logits): every thread redoes its own ids without the list
+#pragma unroll 1
+            for (int kk = 0; kk < kTilesWG; ++kk) {
+                const int k = wg + 2 * kk;
+                if (k >= nt) break;
+                const int v = (t0 + k) * 128 + q * 32 + lane;
+                if (v >= V) continue;
+#pragma unroll 1
+                for (int b = 0; b < kChainRows; ++b) {
+                    if (!((gum_m >> b) & 1u)) continue;
+                    const uint32_t l16 = (uint32_t)__ldcg(cache_i + b * a.cache_s0 + v);
+                    const float lf = __uint_as_float(l16 << 16);
+                    const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
+                    const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
+                    atomicMax(&c.gbest[b], ((unsigned long long)o << 32) |
+                                               ((unsigned long long)(0x3FFFFu - (uint32_t)v) << 14));
+                }
+            }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+    }
+#pragma unroll
+    for (int b = 0; b < kChainRows; ++b) {
+        if ((gum_m >> b) & 1u) {
+            if (lane == 0) c.wbest[ew][b] = ew == 0 ? (uint64_t)c.gbest[b] : 0ull;
+        } else {
+            const uint64_t pk =
+                bo[b] != 0u ? (((uint64_t)bo[b] << 32) | ((uint64_t)(0x3FFFFu - bv[b]) << 14)) : 0ull;
+            const uint64_t m = tc::warp_max_u64(pk);
+            if (lane == 0) c.wbest[ew][b] = m;
+        }
+    }
 }
 
 }  // namespace
@@ -239,7 +561,6 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         c.sampling[b] = live && samples(T);
         c.seed[b] = live ? (uint64_t)a.seeds[b] : 0ull;
         c.invT[b] = samples(T) ? 1.0f / T : 1.0f;
-        c.hri[b] = dm_row_step_hash(c.seed[b], (uint32_t)b, 0u);
         int64_t p = live ? (int64_t)a.anchor[b] : 0;
         if (p < 0 || p >= V) {
             set_status(a.status, 1u /* MARKOV_EINVAL */, 0x100u + b);
@@ -251,6 +572,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         *reinterpret_cast<uint4 *>(b_s + o) = make_uint4(0u, 0u, 0u, 0u);
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(&c.tmem_base), 512);
     __syncthreads();
+    if (tid < N * kChainRows) {
+        const int b = tid % kChainRows, i2 = tid / kChainRows;
+        c.hri[i2][b] = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
+    }
     if (warp < kChainRows && c.live[warp]) stage_embed<RANK>(b_s, a.embed, c.prev[warp], warp, lane);
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
@@ -258,6 +583,11 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     tc::fence_after_sync();
     const uint32_t tmem = c.tmem_base;
     const uint64_t timeout = a.timeout_ns;
+    uint32_t gum_mask = 0u;   // Gumbel rows (sampling rows of the Gumbel mode)
+#pragma unroll
+    for (int b = 0; b < kChainRows; ++b) gum_mask |= c.sampling[b] ? (1u << b) : 0u;
+    if (a.mode != 0) gum_mask = 0u;
+    const bool gum_any = gum_mask != 0u;
 
     // per-role persistent state
     uint32_t uses = 0;          // issuer: tiles issued into its accumulator
@@ -383,8 +713,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             __syncwarp();
         } else {
             // warps 4..11
-            const int t256 = tid - 128;
             if (i == 0) {
+                const int t256 = tid - 128;
                 // warm L2 with this CTA's base-logit slices of every position
                 for (int b = 0; b < R && b < kChainRows; ++b) {
                     if (!c.live[b]) continue;
@@ -394,204 +724,14 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                             tc::prefetch_l2(row + v);
                     }
                 }
-                if (a.mode == 0) {
-                    // a one-byte bound on the noise of every Gumbel (row,
-                    // position, id) of this CTA, while the head streams in; the
-                    // noise depends on seeds and positions only, not on the chain
-                    uint8_t *gq = reinterpret_cast<uint8_t *>(a.noise);
-                    for (int b = 0; b < R && b < kChainRows; ++b) {
-                        if (!c.sampling[b]) continue;
-                        for (int i2 = 0; i2 < N; ++i2) {
-                            const uint64_t hri = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
-                            uint8_t *dst = gq + (int64_t)(b * N + i2) * V;
-                            for (int v = v_begin + t256; v < v_end; v += 4 * 256) {
-                                uint32_t qv[4];
-#pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    qv[u] = quantize_upper(gumbel_upper(dm_splitmix64(hri ^ (uint64_t)(v + u * 256))));
-#pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    if (v + u * 256 < v_end) dst[v + u * 256] = (uint8_t)qv[u];
-                            }
-                        }
-                    }
-                }
+                if (a.mode == 0 && gum_any)
+                    noise_bounds(c, a, 0, gum_mask, v_begin, v_end, t256);
                 asm volatile("bar.sync 2, 256;" ::: "memory");
             }
-            {
-                // Epilogue of accumulator wg, in two passes over this thread's
-                // ids (one per tile), their values kept in registers.
-                // Pass 1, as each tile's bias arrives: the cached logits and
-                // the keys of greedy and inverse-CDF rows; for Gumbel rows a
-                // lower bound on every id's key (logit / T plus the lower end
-                // of its noise byte), whose maximum over the CTA, L, is a lower
-                // bound on the row's best key.
-                // Pass 2, Gumbel rows: only ids whose key upper bound reaches L
-                // can be the maximum, and only they get the exact key, so the
-                // maximum (the token) is exactly that of keys computed for
-                // every id.
-                constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per WG, at most
-                constexpr bool kRegs = kTilesWG <= 4;                  // values kept in registers
-                const int wg = (warp - 4) >> 2, q = warp & 3, ew = warp - 4;
-                uint32_t live_m = 0u, samp_m = 0u;
-#pragma unroll
-                for (int b = 0; b < kChainRows; ++b) {
-                    live_m |= c.live[b] ? (1u << b) : 0u;
-                    samp_m |= c.sampling[b] ? (1u << b) : 0u;
-                }
-                const uint32_t gum_m = a.mode == 0 ? (samp_m & live_m) : 0u;
-                const uint8_t *gq = reinterpret_cast<const uint8_t *>(a.noise);
-                if (tid == 128) {
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) c.lbmax[b] = 0u;
-                }
-                asm volatile("bar.sync 1, 256;" ::: "memory");
-                uint64_t best[kChainRows];
-                uint32_t lbm[kChainRows];
-#pragma unroll
-                for (int b = 0; b < kChainRows; ++b) { best[b] = 0ull; lbm[b] = 0u; }
-                uint32_t keep[kRegs ? kTilesWG : 1][kChainRows];   // logit | noise byte << 16
-                uint32_t nb[kChainRows], nq[kChainRows];
-                auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint32_t (&qq)[kChainRows]) {
-                    const int v = (t0 + k) * 128 + q * 32 + lane;
-                    const bool ok2 = k < nt && v < V;
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) {
-                        const bool lv = ok2 && ((live_m >> b) & 1u);
-                        bb[b] = lv ? (uint32_t)__ldg(a.base + b * a.base_s0 + (int64_t)i * a.base_s1 + v) : 0u;
-                        qq[b] = (lv && ((gum_m >> b) & 1u)) ? (uint32_t)__ldcg(gq + (int64_t)(b * N + i) * V + v) : 0u;
-                    }
-                };
-                load_tile(wg, nb, nq);
-                bool ok = true;
-#pragma unroll
-                for (int kk = 0; kk < kTilesWG; ++kk) {
-                    const int k = wg + 2 * kk;
-                    if (k >= nt || !ok) break;
-                    uint32_t cb[kChainRows], cq[kChainRows];
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) { cb[b] = nb[b]; cq[b] = nq[b]; }
-                    load_tile(k + 2, nb, nq);
-                    if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
-                    if (lane == 0)
-                        ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u,
-                                           tc::now_ns() + timeout);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) {
-                        if (lane == 0) fail(c, a, 4u, 0x6000u + i);
-                        break;
-                    }
-                    ++dcount;
-                    tc::fence_after_sync();
-                    uint32_t r[8];
-                    tc::ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg, r);
-                    tc::wait_ld();
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
-                    const int v = (t0 + k) * 128 + q * 32 + lane;
-                    const bool valid = v < V;
-                    // straight-line over the rows so their chains interleave
-                    uint32_t lb[kChainRows];
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) {
-                        const uint32_t bias = dm_bf16_bits(__uint_as_float(r[b]));
-                        lb[b] = dm_bf16_bits(__fadd_rn(dm_bf16_f32(cb[b]), dm_bf16_f32(bias)));
-                    }
-                    if (a.tf.has_transform) {
-#pragma unroll
-                        for (int b = 0; b < kChainRows; ++b) {
-                            float y = __fmul_rn(dm_bf16_f32(lb[b]), a.tf.mult);
-                            if (a.tf.has_cap) y = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y, a.tf.inv_cap)));
-                            lb[b] = dm_bf16_bits(y);
-                        }
-                    }
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b)
-                        if (valid && ((live_m >> b) & 1u))
-                            a.cache[b * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)lb[b];
-                    if (kRegs) {
-#pragma unroll
-                        for (int b = 0; b < kChainRows; ++b) keep[kRegs ? kk : 0][b] = lb[b] | (cq[b] << 16);
-                    }
-                    float key[kChainRows];
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) key[b] = dm_bf16_f32(lb[b]);
-                    if (a.mode == 1) {
-#pragma unroll
-                        for (int b = 0; b < kChainRows; ++b)
-                            if (((samp_m >> b) & 1u) && c.T[b] != 1.0f) key[b] = __fdiv_rn(key[b], c.T[b]);
-                    }
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) {
-                        const bool use = valid && ((live_m >> b) & 1u);
-                        if ((gum_m >> b) & 1u) {
-                            const float xa = key[b] * c.invT[b];
-                            const float xl = xa - fabsf(xa) * 1e-5f;
-                            const uint32_t o = ordered_key(xl + dequantize_lower(cq[b]));
-                            lbm[b] = (use && o > lbm[b]) ? o : lbm[b];
-                        } else {
-                            const uint64_t pk = pack_tc(key[b], (uint32_t)v);
-                            best[b] = (use && pk > best[b]) ? pk : best[b];
-                        }
-                    }
-                }
-                if (gum_m != 0u) {
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) {
-                        const uint32_t m = __reduce_max_sync(0xffffffffu, lbm[b]);
-                        if (lane == 0 && ((gum_m >> b) & 1u) && m != 0u) atomicMax(&c.lbmax[b], m);
-                    }
-                    asm volatile("bar.sync 1, 256;" ::: "memory");
-                    if (ok) {
-                        float Lr[kChainRows];
-#pragma unroll
-                        for (int b = 0; b < kChainRows; ++b) Lr[b] = key_from_ordered(c.lbmax[b]);
-#pragma unroll
-                        for (int kk = 0; kk < kTilesWG; ++kk) {
-                            const int k = wg + 2 * kk;
-                            if (k >= nt) break;
-                            const int v = (t0 + k) * 128 + q * 32 + lane;
-                            if (v >= V) continue;
-                            uint32_t kv[kChainRows];
-#pragma unroll
-                            for (int b = 0; b < kChainRows; ++b) {
-                                if (kRegs) {
-                                    kv[b] = keep[kRegs ? kk : 0][b];
-                                } else {
-                                    const bool g = (gum_m >> b) & 1u;
-                                    const uint32_t lq = g ? (uint32_t)__ldcg(a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1 + v) : 0u;
-                                    const uint32_t qq = g ? (uint32_t)__ldcg(gq + (int64_t)(b * N + i) * V + v) : 0u;
-                                    kv[b] = lq | (qq << 16);
-                                }
-                            }
-                            uint32_t surv = 0u;
-#pragma unroll
-                            for (int b = 0; b < kChainRows; ++b) {
-                                const float lf = dm_bf16_f32(kv[b] & 0xffffu);
-                                const float xa = lf * c.invT[b];
-                                const float xu = xa + fabsf(xa) * 1e-5f;
-                                const bool in = ((gum_m >> b) & 1u) &&
-                                                !(xu + dequantize_upper(kv[b] >> 16) < Lr[b]);
-                                surv |= in ? (1u << b) : 0u;
-                            }
-                            while (surv != 0u) {
-                                const int b = __ffs(surv) - 1;
-                                surv &= surv - 1u;
-                                const float lf = dm_bf16_f32(kv[b] & 0xffffu);
-                                const uint64_t h = dm_splitmix64(c.hri[b] ^ (uint64_t)v);
-                                const uint64_t pk = pack_tc(exact_key(lf, c.T[b], h), (uint32_t)v);
-                                best[b] = pk > best[b] ? pk : best[b];
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < kChainRows; ++b) {
-                    const uint64_t m = tc::warp_max_u64(best[b]);
-                    if (lane == 0) c.wbest[ew][b] = m;
-                }
-            }
+            if (a.mode == 1)
+                epilogue<RANK, true>(c, a, tmem, i, t0, nt, timeout, dcount);
+            else
+                epilogue<RANK, false>(c, a, tmem, i, t0, nt, timeout, dcount);
         }
         stop = __syncthreads_or(stop_vote(c, a));
         if (stop) break;
@@ -599,194 +739,241 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         // ------------------------------- phase B: agree on every row's winner
         const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
         const uint32_t tag = epoch & 0x3FFFu;
-        if (warp < kChainRows) {
-            const int b = warp;
-            const uint64_t m = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b] : 0ull);
-            uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * Gp;
-            if (lane == 0) tc::st_relaxed_u64(slots + cta, (m & ~0x3FFFull) | tag);
-            if (c.live[b]) {
-                if (lane == 0 && m != 0ull) {
-                    const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;
-                    for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(reinterpret_cast<const uint8_t *>(er) + o);
+        if (a.mode == 0) {
+            // Gumbel and greedy rows: warps 0-3 exchange rows w and w + 4 and
+            // stage the winners' embeddings as the next B operand; warps 4-11
+            // draw the next position's noise meanwhile
+            if (warp < 4) {
+                const int b0 = warp, b1 = warp + 4;
+                uint64_t *s0 = a.tc_keys + ((int64_t)i * kChainRows + b0) * Gp;
+                uint64_t *s1 = a.tc_keys + ((int64_t)i * kChainRows + b1) * Gp;
+                const uint64_t m0 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b0] : 0ull);
+                const uint64_t m1 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b1] : 0ull);
+                if (lane == 0) {
+                    tc::st_relaxed_u64(s0 + cta, (m0 & ~0x3FFFull) | tag);
+                    tc::st_relaxed_u64(s1 + cta, (m1 & ~0x3FFFull) | tag);
                 }
-                uint64_t w = 0ull;
-                if (!poll_max(slots, G, tag, tc::now_ns() + timeout, a, w)) {
-                    if (lane == 0) fail(c, a, 4u, 0x7000u + i);
-                } else if (lane == 0) {
-                    c.win[b] = w;
+                const bool l0 = c.live[b0] != 0, l1 = c.live[b1] != 0;
+                // this CTA's candidates' embeddings into L2 while the others report
+                if (lane < 2 && (lane == 0 ? l0 : l1)) {
+                    const uint64_t m = lane == 0 ? m0 : m1;
+                    if (m != 0ull) {
+                        const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)unpack_id(m) * RANK);
+                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
+                    }
                 }
-            }
-        }
-        stop = __syncthreads_or(stop_vote(c, a));
-        if (stop) break;
-
-        // inverse CDF: rows whose maximum M is finite need the exact integer
-        // weight sums floor(exp(x - M) 2^40), then the CTA whose prefix range
-        // holds mulhi64(H, S) scans its ids for the token
-        bool cdf_any = false;
-        if (a.mode == 1) {
-            for (int b = 0; b < R && b < kChainRows; ++b) {
-                if (!c.sampling[b]) continue;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                const float M = key_from_ordered(o);
-                if (o != 0xffffffffu && !isinf(M)) cdf_any = true;
-            }
-        }
-        if (cdf_any) {
-            const uint32_t tag32 = epoch;
-            if (tid < kChainRows) c.sum[tid] = 0ull;
-            __syncthreads();
-            for (int b = 0; b < R && b < kChainRows; ++b) {
-                if (!c.sampling[b]) continue;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                const float M = key_from_ordered(o);
-                if (o == 0xffffffffu || isinf(M)) continue;
-                const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                uint64_t part = 0ull;
-                for (int v = v_begin + tid; v < v_end; v += kThreads) {
-                    const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
-                    part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-                }
+                if (l0 || l1) {
+                    uint64_t w0 = 0ull, w1 = 0ull;
+                    if (!poll_max2(s0, s1, l0, l1, G, tag, tc::now_ns() + timeout, a, w0, w1)) {
+                        if (lane == 0) fail(c, a, 4u, 0x7000u + i);
+                    } else {
 #pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-                if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
-            }
-            __syncthreads();
-            if (tid < kChainRows && c.sampling[tid]) {
-                const int64_t at = ((int64_t)i * kChainRows + tid) * Gp + cta;
-                tc::st_relaxed_u64(a.tc_sums + at, c.sum[tid]);
-                tc::st_release_u32g(a.sum_tags + at, tag32);
-            }
-            // every CTA learns every row's total and its own prefix
-            __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
-            if (warp < kChainRows && c.sampling[warp]) {
-                const int b = warp;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                const float M = key_from_ordered(o);
-                if (o != 0xffffffffu && !isinf(M)) {
-                    const int64_t base_at = ((int64_t)i * kChainRows + b) * Gp;
-                    const uint64_t dl = tc::now_ns() + timeout;
-                    bool ok = true;
-                    for (uint32_t spin = 0;; ++spin) {
-                        bool fresh = true;
-                        for (int cc = lane; cc < G; cc += 32)
-                            if (ld_acquire_u32(a.sum_tags + base_at + cc) != tag32) fresh = false;
-                        if (__all_sync(0xffffffffu, fresh)) break;
-                        if ((spin & 15u) == 15u &&
-                            __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
-                            ok = false;
-                            break;
+                        for (int h = 0; h < 2; ++h) {
+                            const bool lv = h == 0 ? l0 : l1;
+                            if (!lv) continue;
+                            const int b = h == 0 ? b0 : b1;
+                            const uint64_t w = h == 0 ? w0 : w1;
+                            const uint32_t id = unpack_id(w);
+                            if (lane == 0) {
+                                c.win[b] = w;
+                                c.prev[b] = (int64_t)id;
+                                if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
+                            }
+                            if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
                         }
                     }
-                    if (!ok) {
-                        if (lane == 0) fail(c, a, 4u, 0x8000u + i);
-                    } else {
-                        uint64_t tot = 0ull, pre = 0ull;
-                        for (int cc = lane; cc < G; cc += 32) {
-                            const uint64_t s = tc::ld_relaxed_u64(a.tc_sums + base_at + cc);
-                            tot += s;
-                            if (cc < cta) pre += s;
-                        }
-#pragma unroll
-                        for (int o2 = 16; o2 > 0; o2 >>= 1) {
-                            tot += __shfl_xor_sync(0xffffffffu, tot, o2);
-                            pre += __shfl_xor_sync(0xffffffffu, pre, o2);
-                        }
-                        if (lane == 0) { s_tot[b] = tot; s_pre[b] = pre; }
+                }
+            } else if (i + 1 < N && gum_any) {
+                noise_bounds(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
+            }
+        } else {
+            if (warp < kChainRows) {
+                const int b = warp;
+                const uint64_t m = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b] : 0ull);
+                uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * Gp;
+                if (lane == 0) tc::st_relaxed_u64(slots + cta, (m & ~0x3FFFull) | tag);
+                if (c.live[b]) {
+                    if (lane == 0 && m != 0ull) {
+                        const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;
+                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(reinterpret_cast<const uint8_t *>(er) + o);
+                    }
+                    uint64_t w = 0ull;
+                    if (!poll_max(slots, G, tag, tc::now_ns() + timeout, a, w)) {
+                        if (lane == 0) fail(c, a, 4u, 0x7000u + i);
+                    } else if (lane == 0) {
+                        c.win[b] = w;
                     }
                 }
             }
             stop = __syncthreads_or(stop_vote(c, a));
             if (stop) break;
-            for (int b = 0; b < R && b < kChainRows; ++b) {
-                if (!c.sampling[b]) continue;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                const float M = key_from_ordered(o);
-                if (o == 0xffffffffu || isinf(M)) continue;
-                const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
-                const uint64_t H = dm_cdf_hash(dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i));
-                const uint64_t target = __umul64hi(H, S);
-                if (P <= target && target < P + Sc) {
+
+            // inverse CDF: rows whose maximum M is finite need the exact integer
+            // weight sums floor(exp(x - M) 2^40), then the CTA whose prefix range
+            // holds mulhi64(H, S) scans its ids for the token
+            bool cdf_any = false;
+            if (a.mode == 1) {
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.sampling[b]) continue;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) cdf_any = true;
+                }
+            }
+            if (cdf_any) {
+                const uint32_t tag32 = epoch;
+                if (tid < kChainRows) c.sum[tid] = 0ull;
+                __syncthreads();
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.sampling[b]) continue;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o == 0xffffffffu || isinf(M)) continue;
                     const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                    const int len = v_end - v_begin;
-                    const int chunk = (len + kThreads - 1) / kThreads;
-                    const int c0 = v_begin + tid * chunk;
-                    const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
-                    uint64_t mine = 0ull;
-                    for (int v = c0; v < c1; ++v) {
+                    uint64_t part = 0ull;
+                    for (int v = v_begin + tid; v < v_end; v += kThreads) {
                         const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
-                        mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                        part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                     }
-                    uint64_t incl = mine;
-#pragma unroll
-                    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                        if (lane >= o2) incl += y;
-                    }
-                    if (lane == 31) c.scan[warp] = incl;
-                    __syncthreads();
-                    uint64_t wpre = 0ull;
-                    for (int w = 0; w < warp; ++w) wpre += c.scan[w];
-                    uint64_t run = P + wpre + incl - mine;
-                    if (run <= target && target < run + mine) {
-                        for (int v = c0; v < c1; ++v) {
-                            const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
-                            run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-                            if (run > target) {
-                                tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
-                                                   ((uint64_t)v << 32) | tag32);
+    #pragma unroll
+                    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+                    if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
+                }
+                __syncthreads();
+                if (tid < kChainRows && c.sampling[tid]) {
+                    const int64_t at = ((int64_t)i * kChainRows + tid) * Gp + cta;
+                    tc::st_relaxed_u64(a.tc_sums + at, c.sum[tid]);
+                    tc::st_release_u32g(a.sum_tags + at, tag32);
+                }
+                // every CTA learns every row's total and its own prefix
+                __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
+                if (warp < kChainRows && c.sampling[warp]) {
+                    const int b = warp;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) {
+                        const int64_t base_at = ((int64_t)i * kChainRows + b) * Gp;
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        bool ok = true;
+                        for (uint32_t spin = 0;; ++spin) {
+                            bool fresh = true;
+                            for (int cc = lane; cc < G; cc += 32)
+                                if (ld_acquire_u32(a.sum_tags + base_at + cc) != tag32) fresh = false;
+                            if (__all_sync(0xffffffffu, fresh)) break;
+                            if ((spin & 15u) == 15u &&
+                                __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                                ok = false;
                                 break;
                             }
                         }
-                    }
-                }
-                __syncthreads();
-            }
-            // everyone learns the tokens the owners found
-            if (warp < kChainRows && c.sampling[warp] && lane == 0) {
-                const int b = warp;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                const float M = key_from_ordered(o);
-                if (o != 0xffffffffu && !isinf(M)) {
-                    const uint64_t *slot = a.tok_slots + (int64_t)i * kChainRows + b;
-                    const uint64_t dl = tc::now_ns() + timeout;
-                    uint64_t t = 0ull;
-                    for (;;) {
-                        t = tc::ld_relaxed_u64(slot);
-                        if ((uint32_t)t == tag32) break;
-                        if (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u) {
-                            fail(c, a, 4u, 0x9000u + i);
-                            break;
+                        if (!ok) {
+                            if (lane == 0) fail(c, a, 4u, 0x8000u + i);
+                        } else {
+                            uint64_t tot = 0ull, pre = 0ull;
+                            for (int cc = lane; cc < G; cc += 32) {
+                                const uint64_t s = tc::ld_relaxed_u64(a.tc_sums + base_at + cc);
+                                tot += s;
+                                if (cc < cta) pre += s;
+                            }
+    #pragma unroll
+                            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                                tot += __shfl_xor_sync(0xffffffffu, tot, o2);
+                                pre += __shfl_xor_sync(0xffffffffu, pre, o2);
+                            }
+                            if (lane == 0) { s_tot[b] = tot; s_pre[b] = pre; }
                         }
                     }
-                    const uint32_t v = (uint32_t)(t >> 32);
-                    if ((uint32_t)t == tag32 && v < (uint32_t)V)
-                        c.win[b] = (c.win[b] & 0xffffffff00000000ull) |
-                                   ((uint64_t)(0x3FFFFu - v) << 14);
-                    else if ((uint32_t)t == tag32)
-                        fail(c, a, 6u, 0xA000u + i);
                 }
+                stop = __syncthreads_or(stop_vote(c, a));
+                if (stop) break;
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.sampling[b]) continue;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o == 0xffffffffu || isinf(M)) continue;
+                    const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
+                    const uint64_t H = dm_cdf_hash(c.hri[i][b]);
+                    const uint64_t target = __umul64hi(H, S);
+                    if (P <= target && target < P + Sc) {
+                        const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                        const int len = v_end - v_begin;
+                        const int chunk = (len + kThreads - 1) / kThreads;
+                        const int c0 = v_begin + tid * chunk;
+                        const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
+                        uint64_t mine = 0ull;
+                        for (int v = c0; v < c1; ++v) {
+                            const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                            mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                        }
+                        uint64_t incl = mine;
+    #pragma unroll
+                        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+                            if (lane >= o2) incl += y;
+                        }
+                        if (lane == 31) c.scan[warp] = incl;
+                        __syncthreads();
+                        uint64_t wpre = 0ull;
+                        for (int w = 0; w < warp; ++w) wpre += c.scan[w];
+                        uint64_t run = P + wpre + incl - mine;
+                        if (run <= target && target < run + mine) {
+                            for (int v = c0; v < c1; ++v) {
+                                const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                                run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                                if (run > target) {
+                                    tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
+                                                       ((uint64_t)v << 32) | tag32);
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+                // everyone learns the tokens the owners found
+                if (warp < kChainRows && c.sampling[warp] && lane == 0) {
+                    const int b = warp;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) {
+                        const uint64_t *slot = a.tok_slots + (int64_t)i * kChainRows + b;
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        uint64_t t = 0ull;
+                        for (;;) {
+                            t = tc::ld_relaxed_u64(slot);
+                            if ((uint32_t)t == tag32) break;
+                            if (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u) {
+                                fail(c, a, 4u, 0x9000u + i);
+                                break;
+                            }
+                        }
+                        const uint32_t v = (uint32_t)(t >> 32);
+                        if ((uint32_t)t == tag32 && v < (uint32_t)V)
+                            c.win[b] = (c.win[b] & 0xffffffff00000000ull) |
+                                       ((uint64_t)(0x3FFFFu - v) << 14);
+                        else if ((uint32_t)t == tag32)
+                            fail(c, a, 6u, 0xA000u + i);
+                    }
+                }
+                stop = __syncthreads_or(stop_vote(c, a));
+                if (stop) break;
             }
-            stop = __syncthreads_or(stop_vote(c, a));
-            if (stop) break;
-        }
 
-        // ------------------------- the token, and the next position's B operand
-        if (warp < kChainRows && c.live[warp]) {
-            const int b = warp;
-            uint32_t id = unpack_id(c.win[b]);
-            if (a.mode == 1 && c.sampling[b]) {
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
+            // ------------------------- the token, and the next position's B operand
+            if (warp < kChainRows && c.live[warp]) {
+                const int b = warp;
+                uint32_t id = unpack_id(c.win[b]);
+                if (a.mode == 1 && c.sampling[b]) {
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
+                }
+                if (lane == 0) {
+                    c.prev[b] = (int64_t)id;
+                    if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
+                }
+                if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
             }
-            if (lane == 0) {
-                c.prev[b] = (int64_t)id;
-                if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
-            }
-            if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
         }
-        if (tid < kChainRows && i + 1 < N)
-            c.hri[tid] = dm_row_step_hash(c.seed[tid], (uint32_t)tid, (uint32_t)(i + 1));
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         stop = __syncthreads_or(stop_vote(c, a));

@@ -80,6 +80,15 @@ __device__ __forceinline__ uint32_t logit_bits(uint32_t base_bits, float bias_su
     return dm_bf16_bits(y);
 }
 
+// Two fp32 values rounded to BF16 (nearest, ties to even) in one
+// instruction: lo in bits 0-15, hi in bits 16-31.  A NaN becomes a NaN
+// (the hardware's canonical one, not necessarily 0x7FC0).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Whether a temperature samples (T > 0); 0, negatives and NaN are greedy.
 __device__ __forceinline__ bool samples(float T) { return T > 0.0f; }
 

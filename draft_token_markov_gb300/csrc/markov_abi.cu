@@ -189,7 +189,11 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     size_t batch_keys = (size_t)d.max_rows * p->batch_grid;
     p->keys_n = chain_keys > batch_keys ? chain_keys : batch_keys;
     p->noise_s0 = d.vocab;
-    const size_t noise_bytes = (size_t)d.max_rows * d.num_steps * d.vocab * sizeof(float);
+    // fp32 noise of every row for the per-position kernels; the tcgen05 chain
+    // reuses the buffer for its 8 noise-bound bytes per (position, id)
+    size_t noise_bytes = (size_t)d.max_rows * d.num_steps * d.vocab * sizeof(float);
+    const size_t bound_bytes = (size_t)d.num_steps * d.vocab * kChainRows;
+    if (p->tc_ok && noise_bytes < bound_bytes) noise_bytes = bound_bytes;
     const int Gtc = p->tc_grid > 0 ? p->tc_grid : 1;
     p->tc_slots_n = (size_t)kMaxSteps * kChainRows * ((Gtc + kKeyPad - 1) / kKeyPad * kKeyPad);
     if (cudaMalloc(&p->noise, noise_bytes) != cudaSuccess ||
@@ -418,7 +422,7 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
 }
 
 markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n, void *stream) {
-    if (fn < 0 || fn > 4 || n < 0 || (n > 0 && (!x || !y))) return MARKOV_EINVAL;
+    if (fn < 0 || fn > 5 || n < 0 || (n > 0 && (!x || !y))) return MARKOV_EINVAL;
     if (launch_device_math(fn, x, y, n, (cudaStream_t)stream) != cudaSuccess) return MARKOV_ECUDA;
     return MARKOV_OK;
 }

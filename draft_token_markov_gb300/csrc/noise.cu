@@ -61,7 +61,14 @@ __global__ void device_math_kernel(int fn, const float *__restrict__ x, float *_
             case 1: r = dm_exp(v); break;
             case 2: r = dm_tanh(v); break;
             case 3: r = -dm_log(-dm_log(v)); break;
-            default: r = __uint_as_float(dm_bf16_bits(v)); break;
+            case 4: r = __uint_as_float(dm_bf16_bits(v)); break;
+            default: {
+                // the packed conversion of the tcgen05 epilogue: both halves
+                // must agree (0xDEAD, not a NaN, flags a disagreement)
+                const uint32_t p = bf16x2_rn(v, v);
+                r = __uint_as_float((p & 0xffffu) == (p >> 16) ? (p & 0xffffu) : 0xDEADu);
+                break;
+            }
         }
         y[j] = r;
     }

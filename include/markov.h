@@ -214,7 +214,9 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
 /* Evaluate the device's own scalar functions element-wise over n floats
  * (device pointers): fn 0 natural log, 1 exp, 2 tanh, 3 Gumbel transform
  * -log(-log x), 4 fp32 -> BF16 round-to-nearest-even (result bits in the
- * low 16 bits of the output word, read as uint32).  These are the
+ * low 16 bits of the output word, read as uint32), 5 the same rounding by
+ * the packed two-value conversion the tcgen05 chain's epilogue uses (a NaN
+ * gives some NaN; 0xDEAD if the two packed halves disagree).  These are the
  * functions the kernels use; exposed so they can be compared bit for bit with
  * an independent implementation.  EINVAL for an unknown fn. */
 markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n,

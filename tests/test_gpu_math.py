@@ -51,3 +51,19 @@ def test_bf16_rounding_bit_identical(gpu_lib):
     nan = np.isnan(x)
     assert np.array_equal(y[~nan], ref[~nan])
     assert np.all((y[nan] & 0x7FFF) > 0x7F80)
+
+
+def test_packed_bf16_rounding_bit_identical(gpu_lib):
+    # the epilogue's packed conversion: same bits as the oracle's rounding
+    # for every non-NaN input, some NaN for a NaN
+    rng = np.random.default_rng(2)
+    x = rng.integers(0, 1 << 32, size=1 << 22, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1.0, -1.0, 2.0**-133, -(2.0**-149),
+                        3.3895314e38, 3.4e38, -3.4e38, 1.00390625, 1.01171875],
+                       dtype=np.float32)
+    x = np.concatenate([x, special])
+    y = _dev(gpu_lib, 5, x).view(np.uint32)
+    ref = oracle.bf16_rne(x).astype(np.uint32)
+    nan = np.isnan(x)
+    assert np.array_equal(y[~nan], ref[~nan])
+    assert np.all((y[nan] & 0x7FFF) > 0x7F80)
