@@ -52,7 +52,6 @@ constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
 constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
 constexpr uint32_t kSmemB = 4 * kBChunkBytes;
 constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
-constexpr int kSurvCap = 256;             // Gumbel survivors listed per CTA and position
 
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
@@ -61,11 +60,8 @@ struct Ctl {
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
-    unsigned long long gbest[kChainRows];  // Gumbel rows: this CTA's best packed key
-    uint32_t nsurv;                  // Gumbel ids left after the bound test
-    uint64_t surv[kSurvCap];         // (id << 32) | (row << 16) | cached logit
+    uint64_t cbuf[8][32];            // per epilogue warp: Gumbel survivors (id, row, logit)
     uint64_t win[kChainRows];
-    unsigned int lbmax[kChainRows];        // per row: ordered max over this CTA of key lower bounds
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
     uint64_t tot, pre;
@@ -200,10 +196,8 @@ __device__ __forceinline__ float dequantize_lower(uint32_t q) {
     return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f - 1.0f / 12.0f - 0.02f);
 }
 
-// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash
-// (out of line: few ids reach it, and inlining it everywhere would bloat the
-// kernel past the instruction cache).
-__device__ __noinline__ float exact_key(float l, float T, uint64_t h) {
+// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash.
+__device__ __forceinline__ float exact_key(float l, float T, uint64_t h) {
     const float x = (T == 1.0f) ? l : __fdiv_rn(l, T);
     return __fadd_rn(x, dm_gumbel_from_hash(h));
 }
@@ -229,33 +223,147 @@ __device__ __forceinline__ float gumbel_upper(uint64_t h) {
 // v_begin + t256 + 256 j, four at a time so that their hash and log chains
 // overlap).  The noise depends on seeds and positions only, so it is drawn
 // while the chain waits: position 0 while the head streams in, position
-// p + 1 while position p's winners are exchanged.
+// p + 1 while position p's winners are exchanged.  The loops stay rolled:
+// the kernel's code must fit the instruction caches.
 __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, int p,
                                              uint32_t gum_m, int v_begin, int v_end, int t256) {
     uint2 *gq = reinterpret_cast<uint2 *>(a.noise) + (int64_t)p * a.V;
-    uint64_t hr[kChainRows];
-#pragma unroll
-    for (int b = 0; b < kChainRows; ++b) hr[b] = c.hri[p][b];
+#pragma unroll 1
     for (int v0 = v_begin + t256; v0 < v_end; v0 += 4 * 256) {
-        uint32_t w[4][2];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            w[u][0] = 0u;
-            w[u][1] = 0u;
-        }
-#pragma unroll
+        uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
         for (int b = 0; b < kChainRows; ++b) {
             if (!((gum_m >> b) & 1u)) continue;
+            const uint64_t hb = c.hri[p][b];
+            const int sh = 8 * (b & 3);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const uint64_t h = dm_splitmix64(hr[b] ^ (uint64_t)(v0 + 256 * u));
-                w[u][b >> 2] |= quantize_upper(gumbel_upper(h)) << (8 * (b & 3));
+                const uint32_t qv =
+                    quantize_upper(gumbel_upper(dm_splitmix64(hb ^ (uint64_t)(v0 + 256 * u)))) << sh;
+                lo[u] |= b < 4 ? qv : 0u;
+                hi[u] |= b < 4 ? 0u : qv;
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            if (v0 + 256 * u < v_end) gq[v0 + 256 * u] = make_uint2(w[u][0], w[u][1]);
+            if (v0 + 256 * u < v_end) gq[v0 + 256 * u] = make_uint2(lo[u], hi[u]);
     }
+}
+
+// The output-logit transform of two packed cached logits (out of line: only
+// soft-capped heads take it, and its tanh is long).
+__device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf) {
+    float y0 = __fmul_rn(__uint_as_float(lp << 16), tf.mult);
+    float y1 = __fmul_rn(__uint_as_float(lp & 0xffff0000u), tf.mult);
+    if (tf.has_cap) {
+        y0 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y0, tf.inv_cap)));
+        y1 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y1, tf.inv_cap)));
+    }
+    return bf16x2_rn(y0, y1);
+}
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&x)[4], int j) {
+    return j == 0 ? x[0] : j == 1 ? x[1] : j == 2 ? x[2] : x[3];
+}
+
+// The 4 MMAs (K = 4 x 16) of one 64-wide K chunk j of a tile into
+// accumulator d, with A in TMEM (j < kTmemChunks) or in shared memory.
+// Straight-line code with constant offsets: the operands stay in uniform
+// registers and one MMA issues every ~40 cycles per issuing thread (a
+// rolled loop here measured twice as slow).
+__device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t tmem, uint64_t adesc0, uint64_t bd,
+                                          int j, bool first) {
+    if (j < kTmemChunks) {
+        const uint32_t at = tmem + 32u * j;
+        tc::mma_tmemA_elect(d, at, bd, kIdesc, first ? 0u : 1u);
+        tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
+        tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
+        tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
+    } else {
+        const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
+        tc::mma_smemA_elect(d, ad, bd, kIdesc, first ? 0u : 1u);
+        tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
+        tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
+        tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
+    }
+}
+
+// The MMAs of accumulator W (warp W): tiles W, W + 2, ...; per tile, K
+// chunk by K chunk, 4 MMAs of K = 16 each.  The whole warp runs the loop and
+// one elected lane issues.  W is a template parameter so that the tile and
+// chunk indices, and with them the MMA operands, are warp-uniform values.
+// Position 0 awaits each chunk as the head streams in; later positions run
+// a loop with no waits inside (its code shape sets the issue rate).
+template <int RANK, int W>
+__device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const uint32_t tmem,
+                                            const int i, const int nt, const int ntm,
+                                            const uint32_t b_sa, const uint32_t head_sa,
+                                            const uint64_t timeout, uint32_t &uses) {
+    constexpr int cpt = RANK / 64;
+    const int lane = threadIdx.x & 31;
+    const uint32_t d = tmem + kDCol + 16u * W;
+    const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
+    for (int k = W; k < nt; k += 2) {
+        if (__any_sync(0xffffffffu, aborted(c, a))) break;
+        bool freed = true;
+        if (uses > 0)
+            freed = tc::mbar_wait(tc::smem_u32(&c.dfree[W]), (uses - 1) & 1u, tc::now_ns() + timeout);
+        if (!__all_sync(0xffffffffu, freed)) {
+            if (lane == 0) fail(c, a, 4u, 0x1000u + i);
+            break;
+        }
+        tc::fence_after_sync();
+        if (i == 0) {
+            bool ok = true;
+#pragma unroll 1
+            for (int kc = 0; kc < cpt; ++kc) {
+                const int j = k * cpt + kc;
+                const uint64_t dl = tc::now_ns() + timeout;
+                if (j < kTmemChunks) {
+                    while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
+                        if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                    }
+                    tc::fence_after_sync();
+                } else {
+                    // a parity wait only tells phases apart one at a time:
+                    // every earlier load of this slot (the TMEM chunks
+                    // staged in it) must be complete first
+                    while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
+                        if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                    }
+                    const int s = j - kTmemChunks;
+                    const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
+                    if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) fail(c, a, 4u, 0x2000u + j);
+                    break;
+                }
+                // descriptors advance by (bytes >> 4) in their address field
+                mma_chunk(d, tmem, adesc0, bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4), j, kc == 0);
+            }
+            if (!ok) break;
+        } else {
+#pragma unroll
+            for (int kc = 0; kc < cpt; ++kc)
+                mma_chunk(d, tmem, adesc0, bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4), k * cpt + kc,
+                          kc == 0);
+        }
+        tc::commit_elect(tc::smem_u32(&c.dfull[W]));
+        ++uses;
+    }
+    __syncwarp();
+}
+
+// The exact key of one Gumbel survivor (id v, row b, cached logit l16),
+// folded into warp ew's best key of row b.
+__device__ __forceinline__ void survivor_key(Ctl &c, int i, int ew, uint32_t v, int b, uint32_t l16) {
+    const float lf = __uint_as_float(l16 << 16);
+    const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
+    const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
+    atomicMax(reinterpret_cast<unsigned long long *>(&c.wbest[ew][b]),
+              ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
 }
 
 // The epilogue of one position, run by warps 4-11: accumulator wg = 0 / 1
@@ -264,15 +372,16 @@ __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, 
 // 8 rows of that id (the MMA's N columns).
 //
 // Pass 1, as each tile's bias arrives: the cached logits (two rows per
-// packed BF16 conversion), written out and kept in registers; for rows whose
-// key is exact here (greedy rows, inverse-CDF rows) the running maximum key
-// with the lowest id; for Gumbel rows a lower bound on every id's key
-// (logit / T plus the lower end of its noise byte), whose maximum over the
-// CTA, L, is a lower bound on the row's best key.
-// Pass 2, Gumbel rows: only ids whose key upper bound reaches L can be the
-// maximum, and only they get the exact key, so the maximum (the token) is
-// exactly that of keys computed for every id.
-// Leaves each warp's per-row best packed key in c.wbest.
+// packed BF16 conversion), written out and, for up to 4 tiles, kept in a
+// register queue; for rows whose key is exact here (greedy rows,
+// inverse-CDF rows) the running maximum key with the lowest id; for Gumbel
+// rows a lower bound on every id's key (logit / T plus the lower end of its
+// noise byte).
+// Pass 2, Gumbel rows: the warp's maximum lower bound L is a lower bound on
+// the warp's best key, so only ids whose key upper bound reaches L can be
+// the maximum; only they get the exact key, so the warp's maximum (and the
+// token) is exactly that of keys computed for every id.
+// Leaves each warp's per-row best packed key in c.wbest[warp - 4].
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
                                          const int i, const int t0, const int nt,
@@ -296,15 +405,8 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     const uint2 *gq = reinterpret_cast<const uint2 *>(a.noise) + (int64_t)i * V;
     const uint16_t *base_i = a.base + (int64_t)i * a.base_s1;
     uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1;
-    if (tid == 128) {
-#pragma unroll
-        for (int b = 0; b < kChainRows; ++b) {
-            c.lbmax[b] = 0u;
-            c.gbest[b] = 0ull;
-        }
-        c.nsurv = 0u;
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (lane < kChainRows) c.wbest[ew][lane] = 0ull;
+    __syncwarp();
 
     uint32_t bo[kChainRows], bv[kChainRows];   // best ordered key and its id
     float lbm[kChainRows];                      // Gumbel rows: maximum key lower bound
@@ -314,8 +416,10 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         bv[b] = 0u;
         lbm[b] = __uint_as_float(0xff800000u);
     }
-    uint32_t keepl[kRegs ? kTilesWG : 1][kChainRows / 2];   // packed logits
-    uint2 keepq[kRegs ? kTilesWG : 1];                       // noise bytes
+    // the last 4 tiles' packed logits and noise bytes, newest first
+    uint32_t k0[4] = {0u, 0u, 0u, 0u}, k1[4] = {0u, 0u, 0u, 0u}, k2[4] = {0u, 0u, 0u, 0u},
+             k3[4] = {0u, 0u, 0u, 0u};
+    uint2 g0 = make_uint2(0u, 0u), g1 = g0, g2 = g0, g3 = g0;
     uint32_t nb[kChainRows];
     uint2 nq;
     auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint2 &qq) {
@@ -328,10 +432,9 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     };
     load_tile(wg, nb, nq);
     bool ok = true;
-#pragma unroll
-    for (int kk = 0; kk < kTilesWG; ++kk) {
-        const int k = wg + 2 * kk;
-        if (k >= nt || !ok) break;
+    int ntw = 0;
+#pragma unroll 1
+    for (int k = wg; k < nt; k += 2) {
         uint32_t cb[kChainRows];
 #pragma unroll
         for (int b = 0; b < kChainRows; ++b) cb[b] = nb[b];
@@ -366,15 +469,13 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             lp[j] = bf16x2_rn(s0, s1);
         }
         if (a.tf.has_transform) {
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < kChainRows / 2; ++j) {
-                float y0 = __fmul_rn(__uint_as_float(lp[j] << 16), a.tf.mult);
-                float y1 = __fmul_rn(__uint_as_float(lp[j] & 0xffff0000u), a.tf.mult);
-                if (a.tf.has_cap) {
-                    y0 = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y0, a.tf.inv_cap)));
-                    y1 = __fmul_rn(a.tf.cap, dm_tanh(__fmul_rn(y1, a.tf.inv_cap)));
-                }
-                lp[j] = bf16x2_rn(y0, y1);
+                const uint32_t t = transform_pair(pick4(lp, j), a.tf);
+                lp[0] = j == 0 ? t : lp[0];
+                lp[1] = j == 1 ? t : lp[1];
+                lp[2] = j == 2 ? t : lp[2];
+                lp[3] = j == 3 ? t : lp[3];
             }
         }
 #pragma unroll
@@ -383,8 +484,16 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 cache_i[b * a.cache_s0 + v] = (uint16_t)(lp[b >> 1] >> (16 * (b & 1)));
         if (kRegs) {
 #pragma unroll
-            for (int j = 0; j < kChainRows / 2; ++j) keepl[kRegs ? kk : 0][j] = lp[j];
-            keepq[kRegs ? kk : 0] = cq;
+            for (int j = 0; j < 4; ++j) {
+                k3[j] = k2[j];
+                k2[j] = k1[j];
+                k1[j] = k0[j];
+                k0[j] = lp[j];
+            }
+            g3 = g2;
+            g2 = g1;
+            g1 = g0;
+            g0 = cq;
         }
 #pragma unroll
         for (int b = 0; b < kChainRows; ++b) {
@@ -404,108 +513,118 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 bv[b] = better ? (uint32_t)v : bv[b];
             }
         }
+        ++ntw;
     }
-    if (gum_m != 0u) {
+    if (gum_m != 0u && ok) {
+        float Lw[kChainRows];
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b) {
-            if ((gum_m >> b) & 1u) {
-                const uint32_t m = __reduce_max_sync(0xffffffffu, ordered_key(lbm[b]));
-                if (lane == 0) atomicMax(&c.lbmax[b], m);
+        for (int b = 0; b < kChainRows; ++b)
+            Lw[b] = ((gum_m >> b) & 1u)
+                        ? key_from_ordered(__reduce_max_sync(0xffffffffu, ordered_key(lbm[b])))
+                        : 0.0f;
+        float invT[kChainRows];
+#pragma unroll
+        for (int b = 0; b < kChainRows; ++b) invT[b] = c.invT[b];
+        // rows of one id whose key upper bound reaches the warp's L
+        auto test8 = [&](const uint32_t (&lq)[4], uint2 qq) -> uint32_t {
+            uint32_t m8 = 0u;
+#pragma unroll
+            for (int b = 0; b < kChainRows; ++b) {
+                if (!((gum_m >> b) & 1u)) continue;
+                const float lf = __uint_as_float((b & 1) ? (lq[b >> 1] & 0xffff0000u) : (lq[b >> 1] << 16));
+                const float xa = lf * invT[b];
+                const float xu = __fmaf_rn(fabsf(xa), 1e-5f, xa);
+                const uint32_t qb = ((b < 4 ? qq.x : qq.y) >> (8 * (b & 3))) & 0xffu;
+                m8 |= !(__fadd_rn(xu, dequantize_upper(qb)) < Lw[b]) ? (1u << b) : 0u;
             }
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (ok) {
-            // the bound test; survivors go to a shared list
-            float Lr[kChainRows];
-#pragma unroll
-            for (int b = 0; b < kChainRows; ++b) Lr[b] = key_from_ordered(c.lbmax[b]);
-#pragma unroll
-            for (int kk = 0; kk < kTilesWG; ++kk) {
-                const int k = wg + 2 * kk;
-                if (k >= nt) break;
+            return m8;
+        };
+        uint32_t cand = 0u;   // bit 8 r + b: queue slot r, row b survives
+        if (kRegs) {
+            // straight-line over the 4 queue slots (slot r holds tile
+            // wg + 2 (ntw - 1 - r)) so their tests overlap
+            auto slot = [&](int r, const uint32_t (&lq)[4], uint2 qq) {
+                const int k = wg + 2 * (ntw - 1 - r);
+                const int v = (t0 + k) * 128 + q * 32 + lane;
+                if (r < ntw && v < V) cand |= test8(lq, qq) << (8 * r);
+            };
+            slot(0, k0, g0);
+            slot(1, k1, g1);
+            slot(2, k2, g2);
+            slot(3, k3, g3);
+        } else {
+#pragma unroll 1
+            for (int r = 0; r < ntw; ++r) {
+                const int k = wg + 2 * (ntw - 1 - r);
                 const int v = (t0 + k) * 128 + q * 32 + lane;
                 if (v >= V) continue;
-                uint32_t lp[kChainRows / 2];
-                uint2 qk;
-                if (kRegs) {
+                uint32_t lq[4];
 #pragma unroll
-                    for (int j = 0; j < kChainRows / 2; ++j) lp[j] = keepl[kRegs ? kk : 0][j];
-                    qk = keepq[kRegs ? kk : 0];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < kChainRows / 2; ++j) {
-                        const uint32_t l0 = ((gum_m >> (2 * j)) & 1u)
-                                                ? (uint32_t)__ldcg(cache_i + (2 * j) * a.cache_s0 + v)
-                                                : 0u;
-                        const uint32_t l1 = ((gum_m >> (2 * j + 1)) & 1u)
-                                                ? (uint32_t)__ldcg(cache_i + (2 * j + 1) * a.cache_s0 + v)
-                                                : 0u;
-                        lp[j] = l0 | (l1 << 16);
-                    }
-                    qk = __ldcg(gq + v);
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t l0 = ((gum_m >> (2 * j)) & 1u)
+                                            ? (uint32_t)__ldcg(cache_i + (2 * j) * a.cache_s0 + v)
+                                            : 0u;
+                    const uint32_t l1 = ((gum_m >> (2 * j + 1)) & 1u)
+                                            ? (uint32_t)__ldcg(cache_i + (2 * j + 1) * a.cache_s0 + v)
+                                            : 0u;
+                    lq[j] = l0 | (l1 << 16);
                 }
-#pragma unroll
-                for (int b = 0; b < kChainRows; ++b) {
-                    if (!((gum_m >> b) & 1u)) continue;
-                    const uint32_t l16 = (lp[b >> 1] >> (16 * (b & 1))) & 0xffffu;
-                    const float xa = __uint_as_float(l16 << 16) * c.invT[b];
-                    const float xu = __fmaf_rn(fabsf(xa), 1e-5f, xa);
-                    const uint32_t qb = ((b < 4 ? qk.x : qk.y) >> (8 * (b & 3))) & 0xffu;
-                    if (!(__fadd_rn(xu, dequantize_upper(qb)) < Lr[b])) {
-                        const uint32_t at = atomicAdd(&c.nsurv, 1u);
-                        if (at < (uint32_t)kSurvCap)
-                            c.surv[at] = ((uint64_t)v << 32) | ((uint64_t)b << 16) | l16;
-                    }
+                uint32_t m8 = test8(lq, __ldcg(gq + v));
+                while (m8 != 0u) {
+                    const int b = __ffs(m8) - 1;
+                    m8 &= m8 - 1u;
+                    survivor_key(c, i, ew, (uint32_t)v, b, (pick4(lq, b >> 1) >> (16 * (b & 1))) & 0xffffu);
                 }
             }
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        // exact keys of the listed ids, one per thread (one code site)
-        const uint32_t ns = c.nsurv;
-        const int t256 = tid - 128;
-        for (int j = t256; j < (int)(ns < (uint32_t)kSurvCap ? ns : (uint32_t)kSurvCap); j += 256) {
-            const uint64_t e = c.surv[j];
-            const uint32_t v = (uint32_t)(e >> 32), b = (uint32_t)(e >> 16) & 7u;
-            const float lf = __uint_as_float((uint32_t)(e & 0xffffu) << 16);
-            const float T = c.T[b];
-            const float x = (T == 1.0f) ? lf : __fdiv_rn(lf, T);
-            const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
-            const uint32_t o = ordered_key(__fadd_rn(x, dm_gumbel_from_hash(h)));
-            atomicMax(&c.gbest[b], ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
-        }
-        if (ns > (uint32_t)kSurvCap && ok) {
-            // list overflow (bounds too loose to prune, e.g. non-finite
-            // logits): every thread redoes its own ids without the list
-#pragma unroll 1
-            for (int kk = 0; kk < kTilesWG; ++kk) {
-                const int k = wg + 2 * kk;
-                if (k >= nt) break;
-                const int v = (t0 + k) * 128 + q * 32 + lane;
-                if (v >= V) continue;
-#pragma unroll 1
-                for (int b = 0; b < kChainRows; ++b) {
-                    if (!((gum_m >> b) & 1u)) continue;
-                    const uint32_t l16 = (uint32_t)__ldcg(cache_i + b * a.cache_s0 + v);
-                    const float lf = __uint_as_float(l16 << 16);
-                    const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
-                    const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
-                    atomicMax(&c.gbest[b], ((unsigned long long)o << 32) |
-                                               ((unsigned long long)(0x3FFFFu - (uint32_t)v) << 14));
+        if (kRegs) {
+            // the warp's survivors, one per lane: a prefix count over the lanes
+            // gives each candidate a slot of the warp's list
+            const uint32_t cnt = __popc(cand);
+            uint32_t pre = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
+                if (lane >= o) pre += y;
+            }
+            const uint32_t total = __shfl_sync(0xffffffffu, pre, 31);
+            const uint32_t first = pre - cnt;
+            for (uint32_t base = 0; base < total; base += 32u) {
+                uint32_t cm = cand, sl = first;
+                while (cm != 0u) {
+                    const int bit = __ffs(cm) - 1;
+                    cm &= cm - 1u;
+                    if (sl >= base && sl < base + 32u) {
+                        const int r = bit >> 3, b = bit & 7;
+                        const int k = wg + 2 * (ntw - 1 - r);
+                        const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
+                        uint32_t lq[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            lq[j] = r == 0 ? k0[j] : r == 1 ? k1[j] : r == 2 ? k2[j] : k3[j];
+                        const uint32_t l16 = (pick4(lq, b >> 1) >> (16 * (b & 1))) & 0xffffu;
+                        c.cbuf[ew][sl - base] = ((uint64_t)v << 32) | ((uint64_t)b << 16) | l16;
+                    }
+                    ++sl;
                 }
+                __syncwarp();
+                if (base + (uint32_t)lane < total) {
+                    const uint64_t e = c.cbuf[ew][lane];
+                    survivor_key(c, i, ew, (uint32_t)(e >> 32), (int)((e >> 16) & 7u),
+                                 (uint32_t)(e & 0xffffu));
+                }
+                __syncwarp();
             }
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
     }
+    __syncwarp();
 #pragma unroll
     for (int b = 0; b < kChainRows; ++b) {
-        if ((gum_m >> b) & 1u) {
-            if (lane == 0) c.wbest[ew][b] = ew == 0 ? (uint64_t)c.gbest[b] : 0ull;
-        } else {
-            const uint64_t pk =
-                bo[b] != 0u ? (((uint64_t)bo[b] << 32) | ((uint64_t)(0x3FFFFu - bv[b]) << 14)) : 0ull;
-            const uint64_t m = tc::warp_max_u64(pk);
-            if (lane == 0) c.wbest[ew][b] = m;
-        }
+        if ((gum_m >> b) & 1u) continue;
+        const uint64_t pk =
+            bo[b] != 0u ? (((uint64_t)bo[b] << 32) | ((uint64_t)(0x3FFFFu - bv[b]) << 14)) : 0ull;
+        const uint64_t m = tc::warp_max_u64(pk);
+        if (lane == 0) c.wbest[ew][b] = m;
     }
 }
 
@@ -599,70 +718,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     bool stop = __syncthreads_or(c.abort != 0u);
     for (int i = 0; i < N && !stop; ++i) {
         // ------------------------------------- phase A: MMA and epilogue
-        if (warp < 2) {
-            // the whole warp runs the issue loop; one elected lane issues
-            const int w = warp;
-            const uint32_t d = tmem + kDCol + 16u * w;
-            const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
-            for (int k = w; k < nt; k += 2) {
-                if (__any_sync(0xffffffffu, aborted(c, a))) break;
-                bool freed = true;
-                if (uses > 0)
-                    freed = tc::mbar_wait(tc::smem_u32(&c.dfree[w]), (uses - 1) & 1u,
-                                          tc::now_ns() + timeout);
-                if (!__all_sync(0xffffffffu, freed)) {
-                    if (lane == 0) fail(c, a, 4u, 0x1000u + i);
-                    break;
-                }
-                tc::fence_after_sync();
-                bool ok = true;
-                for (int kc = 0; kc < cpt; ++kc) {
-                    const int j = k * cpt + kc;
-                    if (i == 0) {
-                        const uint64_t dl = tc::now_ns() + timeout;
-                        if (j < kTmemChunks) {
-                            while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
-                                if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
-                            }
-                            tc::fence_after_sync();
-                        } else {
-                            // a parity wait only tells phases apart one at a time:
-                            // every earlier load of this slot (the TMEM chunks
-                            // staged in it) must be complete first
-                            while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
-                                if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
-                            }
-                            const int s = j - kTmemChunks;
-                            const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
-                            if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
-                        }
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) {
-                            if (lane == 0) fail(c, a, 4u, 0x2000u + j);
-                            break;
-                        }
-                    }
-                    // descriptors advance by (bytes >> 4) in their address field
-                    const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
-                    if (j < kTmemChunks) {
-                        const uint32_t at = tmem + 32u * j;
-                        tc::mma_tmemA_elect(d, at, bd, kIdesc, kc != 0);
-                        tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
-                        tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
-                        tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
-                    } else {
-                        const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
-                        tc::mma_smemA_elect(d, ad, bd, kIdesc, kc != 0);
-                        tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
-                        tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
-                        tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
-                    }
-                }
-                if (!ok) break;
-                tc::commit_elect(tc::smem_u32(&c.dfull[w]));
-                ++uses;
-            }
-            __syncwarp();
+        if (warp == 0) {
+            issue_tiles<RANK, 0>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
+        } else if (warp == 1) {
+            issue_tiles<RANK, 1>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
         } else if (warp == 2) {
             if (lane == 0 && i == 0) {
                 for (int j = 0; j < nch; ++j) {
@@ -745,14 +804,19 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             // draw the next position's noise meanwhile
             if (warp < 4) {
                 const int b0 = warp, b1 = warp + 4;
-                uint64_t *s0 = a.tc_keys + ((int64_t)i * kChainRows + b0) * Gp;
-                uint64_t *s1 = a.tc_keys + ((int64_t)i * kChainRows + b1) * Gp;
+                // every CTA writes its key into all kTcReplicas copies of the
+                // slot array and polls copy cta % kTcReplicas, which spreads
+                // the polling over more L2 lines
+                uint64_t *s0 = a.tc_keys + ((int64_t)i * kChainRows + b0) * kTcReplicas * Gp;
+                uint64_t *s1 = a.tc_keys + ((int64_t)i * kChainRows + b1) * kTcReplicas * Gp;
                 const uint64_t m0 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b0] : 0ull);
                 const uint64_t m1 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b1] : 0ull);
-                if (lane == 0) {
-                    tc::st_relaxed_u64(s0 + cta, (m0 & ~0x3FFFull) | tag);
-                    tc::st_relaxed_u64(s1 + cta, (m1 & ~0x3FFFull) | tag);
+                if (lane < kTcReplicas) {
+                    tc::st_relaxed_u64(s0 + lane * Gp + cta, (m0 & ~0x3FFFull) | tag);
+                    tc::st_relaxed_u64(s1 + lane * Gp + cta, (m1 & ~0x3FFFull) | tag);
                 }
+                s0 += (cta % kTcReplicas) * Gp;
+                s1 += (cta % kTcReplicas) * Gp;
                 const bool l0 = c.live[b0] != 0, l1 = c.live[b1] != 0;
                 // this CTA's candidates' embeddings into L2 while the others report
                 if (lane < 2 && (lane == 0 ? l0 : l1)) {
@@ -790,8 +854,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (warp < kChainRows) {
                 const int b = warp;
                 const uint64_t m = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b] : 0ull);
-                uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * Gp;
-                if (lane == 0) tc::st_relaxed_u64(slots + cta, (m & ~0x3FFFull) | tag);
+                uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * kTcReplicas * Gp;
+                if (lane < kTcReplicas) tc::st_relaxed_u64(slots + lane * Gp + cta, (m & ~0x3FFFull) | tag);
+                slots += (cta % kTcReplicas) * Gp;
                 if (c.live[b]) {
                     if (lane == 0 && m != 0ull) {
                         const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;

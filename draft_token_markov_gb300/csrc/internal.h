@@ -15,6 +15,7 @@ constexpr int kChainThreads = 512;     // threads of a chain CTA (one CTA per SM
 constexpr int kBatchThreads = 256;
 constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
 constexpr int kKeyPad = 16;            // u64 slots per CTA-key block are padded to 128 B
+constexpr int kTcReplicas = 8;         // copies of each tcgen05-chain key slot array
 
 // The output-logit transform (muse_spark markov page, FusedMarkovParams):
 // multiplier and cap rounded to fp32, inv_cap = fp32(1) / fp32(cap).
@@ -51,7 +52,7 @@ struct SampleArgs {
     uint32_t *bar_base;        // the counter's value at the start of a launch
     uint32_t *status;          // [2]: sticky device status, where it happened
     uint32_t *call_counter;    // calls of the persistent tcgen05 chain so far
-    uint64_t *tc_keys;         // [N][8][Gp] tagged key slots of the tcgen05 chain
+    uint64_t *tc_keys;         // [N][8][kTcReplicas][Gp] tagged key slots of the tcgen05 chain
     uint64_t *tc_sums;         // [N][8][Gp] inverse-CDF sum slots of the tcgen05 chain
     uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch

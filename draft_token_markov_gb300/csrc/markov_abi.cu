@@ -35,6 +35,7 @@ struct markov_plan {
     uint32_t *sum_tags = nullptr;
     uint64_t *tok_slots = nullptr;
     size_t tc_slots_n = 0;
+    size_t tc_keys_n = 0;         // tc_slots_n * kTcReplicas
     CUtensorMap tmap;
     const void *tmap_head = nullptr;
     cudaStream_t side = nullptr;
@@ -196,15 +197,16 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     if (p->tc_ok && noise_bytes < bound_bytes) noise_bytes = bound_bytes;
     const int Gtc = p->tc_grid > 0 ? p->tc_grid : 1;
     p->tc_slots_n = (size_t)kMaxSteps * kChainRows * ((Gtc + kKeyPad - 1) / kKeyPad * kKeyPad);
+    p->tc_keys_n = p->tc_slots_n * kTcReplicas;
     if (cudaMalloc(&p->noise, noise_bytes) != cudaSuccess ||
         cudaMalloc(&p->keys, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sums, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->ctrl, 8 * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMalloc(&p->tc_keys, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->tc_keys, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->tc_sums, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sum_tags, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMalloc(&p->tok_slots, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->tc_keys, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
@@ -401,7 +403,7 @@ markov_status markov_plan_status(markov_plan *p) {
     // a launch gave up: clear the status, restart the barrier and call
     // counters, and forget every tagged exchange slot
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(p->tc_keys, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess)
         return MARKOV_ECUDA;
