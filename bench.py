@@ -84,17 +84,28 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            # nvidia-smi takes a while to start: wait for its first sample
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.window = [time.time(), None]
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.window[0] = time.time()
+
+    def mark_end(self):
+        self.window[1] = time.time()
 
     def __exit__(self, *exc):
         if self.proc:
@@ -108,7 +119,10 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        lo, hi = self.window[0], self.window[1] or time.time()
+        for t, line in self.lines:
+            if not (lo <= t <= hi + 0.05):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 6:
                 continue
@@ -254,10 +268,21 @@ def run_gpu(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # the same loop untimed for a few hundred ms first, so that the
+        # sampler (20 ms period) sees the load; its window covers this lead-in
+        # and the timed steps
+        clocks.mark_start()
+        t_lead = time.time()
+        while time.time() - t_lead < args.clock_lead_s:
+            for k in range(20):
+                flush_l2(k)
+                step()
+            torch.cuda.synchronize()
         for k in range(args.steps):
             flush_l2(k)
             step(ev[k])
         torch.cuda.synchronize()
+        clocks.mark_end()
     if world > 1:
         dist.barrier()
     st = api.markov_plan_status(plan)
@@ -338,6 +363,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--clock-lead-s", type=float, default=0.3,
+                    help="seconds of untimed steps inside the clock-sampling window before the "
+                         "timed steps")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -41,7 +41,10 @@ namespace dtm {
 
 namespace {
 
-constexpr int kThreads = 384;      // 12 warps: 4 control warps, 8 epilogue warps
+constexpr int kEpiWarps = 16;             // epilogue warps 4..19
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 128 + kEpiThreads;   // 4 control warps, then the epilogue warps
+constexpr int kRowsT = 4;                 // rows per epilogue thread
 constexpr int kTmemChunks = 15;           // A chunks in TMEM (32 columns each)
 constexpr int kSmemChunks = 13;           // A chunks in shared memory (16 KB each)
 constexpr int kMaxChunks = kTmemChunks + kSmemChunks;
@@ -59,8 +62,8 @@ struct Ctl {
     uint64_t dfull[2];               // accumulator b holds a finished tile
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
-    uint64_t wbest[8][kChainRows];   // per epilogue warp, per row: best packed key
-    uint64_t cbuf[8][32];            // per epilogue warp: Gumbel survivors (id, row, logit)
+    uint64_t wbest[kEpiWarps][kChainRows];   // per epilogue warp, per row: best packed key
+    uint64_t cbuf[kEpiWarps][32];    // per epilogue warp: Gumbel survivors (id, row, logit)
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
@@ -219,34 +222,46 @@ __device__ __forceinline__ float gumbel_upper(uint64_t h) {
 }
 
 // The noise-bound bytes of position p for this CTA's ids, 8 row bytes per
-// id, written by the 256 threads of warps 4-11 (thread t256 takes ids
-// v_begin + t256 + 256 j, four at a time so that their hash and log chains
-// overlap).  The noise depends on seeds and positions only, so it is drawn
-// while the chain waits: position 0 while the head streams in, position
-// p + 1 while position p's winners are exchanged.  The loops stay rolled:
-// the kernel's code must fit the instruction caches.
+// id, written by the kEpiThreads threads of the epilogue warps (thread te
+// takes ids v_begin + te + kEpiThreads j, two at a time so that their hash
+// and log chains overlap).  The noise depends on seeds and positions only,
+// so it is drawn while the chain waits: position 0 while the head streams
+// in, position p + 1 while position p's winners are exchanged.  The row
+// loop stays rolled: the kernel's code must fit the instruction caches.
 __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, int p,
-                                             uint32_t gum_m, int v_begin, int v_end, int t256) {
+                                             uint32_t gum_m, int v_begin, int v_end, int te) {
     uint2 *gq = reinterpret_cast<uint2 *>(a.noise) + (int64_t)p * a.V;
 #pragma unroll 1
-    for (int v0 = v_begin + t256; v0 < v_end; v0 += 4 * 256) {
-        uint32_t lo[4] = {0u, 0u, 0u, 0u}, hi[4] = {0u, 0u, 0u, 0u};
+    for (int v0 = v_begin + te; v0 < v_end; v0 += 2 * kEpiThreads) {
+        uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};
 #pragma unroll 1
         for (int b = 0; b < kChainRows; ++b) {
             if (!((gum_m >> b) & 1u)) continue;
             const uint64_t hb = c.hri[p][b];
             const int sh = 8 * (b & 3);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 2; ++u) {
                 const uint32_t qv =
-                    quantize_upper(gumbel_upper(dm_splitmix64(hb ^ (uint64_t)(v0 + 256 * u)))) << sh;
+                    quantize_upper(gumbel_upper(dm_splitmix64(hb ^ (uint64_t)(v0 + kEpiThreads * u)))) << sh;
                 lo[u] |= b < 4 ? qv : 0u;
                 hi[u] |= b < 4 ? 0u : qv;
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (v0 + 256 * u < v_end) gq[v0 + 256 * u] = make_uint2(lo[u], hi[u]);
+        for (int u = 0; u < 2; ++u)
+            if (v0 + kEpiThreads * u < v_end) gq[v0 + kEpiThreads * u] = make_uint2(lo[u], hi[u]);
+    }
+}
+
+// Warm L2 with this CTA's base logits of position p (every live row), one
+// 128-byte line per epilogue thread.
+__device__ __forceinline__ void prefetch_base(const Ctl &c, const SampleArgs &a, int p, int v_begin,
+                                              int v_end, int te) {
+#pragma unroll 1
+    for (int b = 0; b < a.rows && b < kChainRows; ++b) {
+        if (!c.live[b]) continue;
+        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)p * a.base_s1;
+        for (int v = v_begin + te * 64; v < v_end; v += kEpiThreads * 64) tc::prefetch_l2(row + v);
     }
 }
 
@@ -366,10 +381,12 @@ __device__ __forceinline__ void survivor_key(Ctl &c, int i, int ew, uint32_t v, 
               ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
 }
 
-// The epilogue of one position, run by warps 4-11: accumulator wg = 0 / 1
-// (warps 4-7 / 8-11) takes the even / odd tiles; warp quarter q of a group
-// reads TMEM lanes 32q..32q+31, so each thread owns one id per tile and the
-// 8 rows of that id (the MMA's N columns).
+// The epilogue of one position, run by the 16 warps 4-19: warp 4 + ew
+// serves accumulator wg = ew / 8 (the even / odd tiles), TMEM lane quarter
+// q = warp % 4 (the only lanes a warp may read) and rows rb..rb+3, rb =
+// 4 ((ew / 4) % 2), so each thread owns one id per tile and 4 of the 8 rows
+// (the MMA's N columns).  Two warps per lane quarter halve every thread's
+// dependent chains, which bound this code.
 //
 // Pass 1, as each tile's bias arrives: the cached logits (two rows per
 // packed BF16 conversion), written out and, for up to 4 tiles, kept in a
@@ -381,7 +398,8 @@ __device__ __forceinline__ void survivor_key(Ctl &c, int i, int ew, uint32_t v, 
 // the warp's best key, so only ids whose key upper bound reaches L can be
 // the maximum; only they get the exact key, so the warp's maximum (and the
 // token) is exactly that of keys computed for every id.
-// Leaves each warp's per-row best packed key in c.wbest[warp - 4].
+// Leaves each warp's per-row best packed key in c.wbest[ew] (0 for rows it
+// does not own).
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
                                          const int i, const int t0, const int nt,
@@ -390,55 +408,54 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
     constexpr bool kRegs = kTilesWG <= 4;                  // tiles kept in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wg = (warp - 4) >> 2, q = warp & 3, ew = warp - 4;
+    const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1, rb = kRowsT * hr;
     const int V = a.V;
-    uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;
+    uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;   // this thread's 4 rows, bit j = row rb + j
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        live_m |= c.live[b] ? (1u << b) : 0u;
-        samp_m |= c.sampling[b] ? (1u << b) : 0u;
-        div_m |= (c.sampling[b] && c.T[b] != 1.0f) ? (1u << b) : 0u;
+    for (int j = 0; j < kRowsT; ++j) {
+        live_m |= c.live[rb + j] ? (1u << j) : 0u;
+        samp_m |= c.sampling[rb + j] ? (1u << j) : 0u;
+        div_m |= (c.sampling[rb + j] && c.T[rb + j] != 1.0f) ? (1u << j) : 0u;
     }
     // Gumbel rows get the bound treatment; inverse-CDF rows divide by T
     const uint32_t gum_m = kCdf ? 0u : (samp_m & live_m);
     div_m = kCdf ? (div_m & live_m) : 0u;
-    const uint2 *gq = reinterpret_cast<const uint2 *>(a.noise) + (int64_t)i * V;
-    const uint16_t *base_i = a.base + (int64_t)i * a.base_s1;
-    uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1;
+    const uint32_t *gq = reinterpret_cast<const uint32_t *>(a.noise) + ((int64_t)i * V) * 2 + hr;
+    const uint16_t *base_i = a.base + (int64_t)i * a.base_s1 + rb * a.base_s0;
+    uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1 + rb * a.cache_s0;
     if (lane < kChainRows) c.wbest[ew][lane] = 0ull;
     __syncwarp();
 
-    uint32_t bo[kChainRows], bv[kChainRows];   // best ordered key and its id
-    float lbm[kChainRows];                      // Gumbel rows: maximum key lower bound
+    uint32_t bo[kRowsT], bv[kRowsT];   // best ordered key and its id
+    float lbm[kRowsT];                  // Gumbel rows: maximum key lower bound
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        bo[b] = 0u;
-        bv[b] = 0u;
-        lbm[b] = __uint_as_float(0xff800000u);
+    for (int j = 0; j < kRowsT; ++j) {
+        bo[j] = 0u;
+        bv[j] = 0u;
+        lbm[j] = __uint_as_float(0xff800000u);
     }
     // the last 4 tiles' packed logits and noise bytes, newest first
-    uint32_t k0[4] = {0u, 0u, 0u, 0u}, k1[4] = {0u, 0u, 0u, 0u}, k2[4] = {0u, 0u, 0u, 0u},
-             k3[4] = {0u, 0u, 0u, 0u};
-    uint2 g0 = make_uint2(0u, 0u), g1 = g0, g2 = g0, g3 = g0;
-    uint32_t nb[kChainRows];
-    uint2 nq;
-    auto load_tile = [&](int k, uint32_t (&bb)[kChainRows], uint2 &qq) {
+    uint32_t k0[2] = {0u, 0u}, k1[2] = {0u, 0u}, k2[2] = {0u, 0u}, k3[2] = {0u, 0u};
+    uint32_t g0 = 0u, g1 = 0u, g2 = 0u, g3 = 0u;
+    uint32_t nb[kRowsT];
+    uint32_t nq;
+    auto load_tile = [&](int k, uint32_t (&bb)[kRowsT], uint32_t &qq) {
         const int v = (t0 + k) * 128 + q * 32 + lane;
         const bool ok2 = k < nt && v < V;
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b)
-            bb[b] = (ok2 && ((live_m >> b) & 1u)) ? (uint32_t)__ldg(base_i + b * a.base_s0 + v) : 0u;
-        qq = (ok2 && gum_m != 0u) ? __ldcg(gq + v) : make_uint2(0u, 0u);
+        for (int j = 0; j < kRowsT; ++j)
+            bb[j] = (ok2 && ((live_m >> j) & 1u)) ? (uint32_t)__ldg(base_i + j * a.base_s0 + v) : 0u;
+        qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
     load_tile(wg, nb, nq);
     bool ok = true;
     int ntw = 0;
 #pragma unroll 1
     for (int k = wg; k < nt; k += 2) {
-        uint32_t cb[kChainRows];
+        uint32_t cb[kRowsT];
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b) cb[b] = nb[b];
-        const uint2 cq = nq;
+        for (int j = 0; j < kRowsT; ++j) cb[j] = nb[j];
+        const uint32_t cq = nq;
         load_tile(k + 2, nb, nq);
         if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
         if (lane == 0)
@@ -450,8 +467,8 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         }
         ++dcount;
         tc::fence_after_sync();
-        uint32_t r[8];
-        tc::ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg, r);
+        uint32_t r[4];
+        tc::ld_32x32b_x4(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg + (uint32_t)rb, r);
         tc::wait_ld();
         tc::fence_before_sync();
         __syncwarp();
@@ -459,9 +476,9 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         const int v = (t0 + k) * 128 + q * 32 + lane;
         const bool valid = v < V;
         // bias = bf16(sum); logit = bf16(f32(base) + f32(bias)), two rows a time
-        uint32_t lp[kChainRows / 2];
+        uint32_t lp[2];
 #pragma unroll
-        for (int j = 0; j < kChainRows / 2; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const uint32_t bb = bf16x2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
             const float s0 = __fadd_rn(__uint_as_float(cb[2 * j] << 16), __uint_as_float(bb << 16));
             const float s1 = __fadd_rn(__uint_as_float(cb[2 * j + 1] << 16),
@@ -469,22 +486,16 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             lp[j] = bf16x2_rn(s0, s1);
         }
         if (a.tf.has_transform) {
-#pragma unroll 1
-            for (int j = 0; j < kChainRows / 2; ++j) {
-                const uint32_t t = transform_pair(pick4(lp, j), a.tf);
-                lp[0] = j == 0 ? t : lp[0];
-                lp[1] = j == 1 ? t : lp[1];
-                lp[2] = j == 2 ? t : lp[2];
-                lp[3] = j == 3 ? t : lp[3];
-            }
+            lp[0] = transform_pair(lp[0], a.tf);
+            lp[1] = transform_pair(lp[1], a.tf);
         }
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b)
-            if (valid && ((live_m >> b) & 1u))
-                cache_i[b * a.cache_s0 + v] = (uint16_t)(lp[b >> 1] >> (16 * (b & 1)));
+        for (int j = 0; j < kRowsT; ++j)
+            if (valid && ((live_m >> j) & 1u))
+                cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
         if (kRegs) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 k3[j] = k2[j];
                 k2[j] = k1[j];
                 k1[j] = k0[j];
@@ -496,57 +507,57 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             g0 = cq;
         }
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b) {
-            const float lf = __uint_as_float((b & 1) ? (lp[b >> 1] & 0xffff0000u) : (lp[b >> 1] << 16));
-            if ((gum_m >> b) & 1u) {
+        for (int j = 0; j < kRowsT; ++j) {
+            const int b = rb + j;
+            const float lf = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
+            if ((gum_m >> j) & 1u) {
                 const float xa = lf * c.invT[b];
                 const float xl = __fmaf_rn(fabsf(xa), -1e-5f, xa);
-                const uint32_t qb = ((b < 4 ? cq.x : cq.y) >> (8 * (b & 3))) & 0xffu;
+                const uint32_t qb = (cq >> (8 * j)) & 0xffu;
                 const float kl = __fadd_rn(xl, dequantize_lower(qb));
-                lbm[b] = (valid && kl > lbm[b]) ? kl : lbm[b];
+                lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
             } else {
                 float key = lf;
-                if (kCdf && ((div_m >> b) & 1u)) key = __fdiv_rn(lf, c.T[b]);
+                if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[b]);
                 const uint32_t o = ordered_key(key);
-                const bool better = valid && ((live_m >> b) & 1u) && o > bo[b];
-                bo[b] = better ? o : bo[b];
-                bv[b] = better ? (uint32_t)v : bv[b];
+                const bool better = valid && ((live_m >> j) & 1u) && o > bo[j];
+                bo[j] = better ? o : bo[j];
+                bv[j] = better ? (uint32_t)v : bv[j];
             }
         }
         ++ntw;
     }
     if (gum_m != 0u && ok) {
-        float Lw[kChainRows];
+        float Lw[kRowsT], invT[kRowsT];
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b)
-            Lw[b] = ((gum_m >> b) & 1u)
-                        ? key_from_ordered(__reduce_max_sync(0xffffffffu, ordered_key(lbm[b])))
+        for (int j = 0; j < kRowsT; ++j) {
+            invT[j] = c.invT[rb + j];
+            Lw[j] = ((gum_m >> j) & 1u)
+                        ? key_from_ordered(__reduce_max_sync(0xffffffffu, ordered_key(lbm[j])))
                         : 0.0f;
-        float invT[kChainRows];
-#pragma unroll
-        for (int b = 0; b < kChainRows; ++b) invT[b] = c.invT[b];
+        }
         // rows of one id whose key upper bound reaches the warp's L
-        auto test8 = [&](const uint32_t (&lq)[4], uint2 qq) -> uint32_t {
-            uint32_t m8 = 0u;
+        auto test4 = [&](const uint32_t (&lq)[2], uint32_t qq) -> uint32_t {
+            uint32_t m4 = 0u;
 #pragma unroll
-            for (int b = 0; b < kChainRows; ++b) {
-                if (!((gum_m >> b) & 1u)) continue;
-                const float lf = __uint_as_float((b & 1) ? (lq[b >> 1] & 0xffff0000u) : (lq[b >> 1] << 16));
-                const float xa = lf * invT[b];
+            for (int j = 0; j < kRowsT; ++j) {
+                if (!((gum_m >> j) & 1u)) continue;
+                const float lf = __uint_as_float((j & 1) ? (lq[j >> 1] & 0xffff0000u) : (lq[j >> 1] << 16));
+                const float xa = lf * invT[j];
                 const float xu = __fmaf_rn(fabsf(xa), 1e-5f, xa);
-                const uint32_t qb = ((b < 4 ? qq.x : qq.y) >> (8 * (b & 3))) & 0xffu;
-                m8 |= !(__fadd_rn(xu, dequantize_upper(qb)) < Lw[b]) ? (1u << b) : 0u;
+                const uint32_t qb = (qq >> (8 * j)) & 0xffu;
+                m4 |= !(__fadd_rn(xu, dequantize_upper(qb)) < Lw[j]) ? (1u << j) : 0u;
             }
-            return m8;
+            return m4;
         };
-        uint32_t cand = 0u;   // bit 8 r + b: queue slot r, row b survives
+        uint32_t cand = 0u;   // bit 4 r + j: queue slot r, row rb + j survives
         if (kRegs) {
             // straight-line over the 4 queue slots (slot r holds tile
             // wg + 2 (ntw - 1 - r)) so their tests overlap
-            auto slot = [&](int r, const uint32_t (&lq)[4], uint2 qq) {
+            auto slot = [&](int r, const uint32_t (&lq)[2], uint32_t qq) {
                 const int k = wg + 2 * (ntw - 1 - r);
                 const int v = (t0 + k) * 128 + q * 32 + lane;
-                if (r < ntw && v < V) cand |= test8(lq, qq) << (8 * r);
+                if (r < ntw && v < V) cand |= test4(lq, qq) << (4 * r);
             };
             slot(0, k0, g0);
             slot(1, k1, g1);
@@ -558,9 +569,9 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 const int k = wg + 2 * (ntw - 1 - r);
                 const int v = (t0 + k) * 128 + q * 32 + lane;
                 if (v >= V) continue;
-                uint32_t lq[4];
+                uint32_t lq[2];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 2; ++j) {
                     const uint32_t l0 = ((gum_m >> (2 * j)) & 1u)
                                             ? (uint32_t)__ldcg(cache_i + (2 * j) * a.cache_s0 + v)
                                             : 0u;
@@ -569,11 +580,12 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                                             : 0u;
                     lq[j] = l0 | (l1 << 16);
                 }
-                uint32_t m8 = test8(lq, __ldcg(gq + v));
-                while (m8 != 0u) {
-                    const int b = __ffs(m8) - 1;
-                    m8 &= m8 - 1u;
-                    survivor_key(c, i, ew, (uint32_t)v, b, (pick4(lq, b >> 1) >> (16 * (b & 1))) & 0xffffu);
+                uint32_t m4 = test4(lq, __ldcg(gq + 2 * v));
+                while (m4 != 0u) {
+                    const int j = __ffs(m4) - 1;
+                    m4 &= m4 - 1u;
+                    const uint32_t pr = j < 2 ? lq[0] : lq[1];
+                    survivor_key(c, i, ew, (uint32_t)v, rb + j, (pr >> (16 * (j & 1))) & 0xffffu);
                 }
             }
         }
@@ -595,15 +607,13 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                     const int bit = __ffs(cm) - 1;
                     cm &= cm - 1u;
                     if (sl >= base && sl < base + 32u) {
-                        const int r = bit >> 3, b = bit & 7;
+                        const int r = bit >> 2, j = bit & 3;
                         const int k = wg + 2 * (ntw - 1 - r);
                         const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
-                        uint32_t lq[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            lq[j] = r == 0 ? k0[j] : r == 1 ? k1[j] : r == 2 ? k2[j] : k3[j];
-                        const uint32_t l16 = (pick4(lq, b >> 1) >> (16 * (b & 1))) & 0xffffu;
-                        c.cbuf[ew][sl - base] = ((uint64_t)v << 32) | ((uint64_t)b << 16) | l16;
+                        const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
+                                                    : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
+                        const uint32_t l16 = (pr >> (16 * (j & 1))) & 0xffffu;
+                        c.cbuf[ew][sl - base] = ((uint64_t)v << 32) | ((uint64_t)(rb + j) << 16) | l16;
                     }
                     ++sl;
                 }
@@ -619,12 +629,12 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     }
     __syncwarp();
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        if ((gum_m >> b) & 1u) continue;
+    for (int j = 0; j < kRowsT; ++j) {
+        if ((gum_m >> j) & 1u) continue;
         const uint64_t pk =
-            bo[b] != 0u ? (((uint64_t)bo[b] << 32) | ((uint64_t)(0x3FFFFu - bv[b]) << 14)) : 0ull;
+            bo[j] != 0u ? (((uint64_t)bo[j] << 32) | ((uint64_t)(0x3FFFFu - bv[j]) << 14)) : 0ull;
         const uint64_t m = tc::warp_max_u64(pk);
-        if (lane == 0) c.wbest[ew][b] = m;
+        if (lane == 0) c.wbest[ew][rb + j] = m;
     }
 }
 
@@ -663,7 +673,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(tc::smem_u32(&c.dfull[b]), 1);
-            tc::mbar_init(tc::smem_u32(&c.dfree[b]), 4);
+            tc::mbar_init(tc::smem_u32(&c.dfree[b]), kEpiWarps / 2);
             tc::mbar_init(tc::smem_u32(&c.fin[b]), 1);
         }
         tc::mbar_init_fence();
@@ -773,19 +783,11 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         } else {
             // warps 4..11
             if (i == 0) {
-                const int t256 = tid - 128;
-                // warm L2 with this CTA's base-logit slices of every position
-                for (int b = 0; b < R && b < kChainRows; ++b) {
-                    if (!c.live[b]) continue;
-                    for (int i2 = 0; i2 < N; ++i2) {
-                        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)i2 * a.base_s1;
-                        for (int v = v_begin + t256 * 64; v < v_end; v += 256 * 64)
-                            tc::prefetch_l2(row + v);
-                    }
-                }
+                const int te = tid - 128;
+                prefetch_base(c, a, 0, v_begin, v_end, te);
                 if (a.mode == 0 && gum_any)
-                    noise_bounds(c, a, 0, gum_mask, v_begin, v_end, t256);
-                asm volatile("bar.sync 2, 256;" ::: "memory");
+                    noise_bounds(c, a, 0, gum_mask, v_begin, v_end, te);
+                asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
             }
             if (a.mode == 1)
                 epilogue<RANK, true>(c, a, tmem, i, t0, nt, timeout, dcount);
@@ -809,8 +811,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 // the polling over more L2 lines
                 uint64_t *s0 = a.tc_keys + ((int64_t)i * kChainRows + b0) * kTcReplicas * Gp;
                 uint64_t *s1 = a.tc_keys + ((int64_t)i * kChainRows + b1) * kTcReplicas * Gp;
-                const uint64_t m0 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b0] : 0ull);
-                const uint64_t m1 = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b1] : 0ull);
+                const uint64_t m0 = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b0] : 0ull);
+                const uint64_t m1 = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b1] : 0ull);
                 if (lane < kTcReplicas) {
                     tc::st_relaxed_u64(s0 + lane * Gp + cta, (m0 & ~0x3FFFull) | tag);
                     tc::st_relaxed_u64(s1 + lane * Gp + cta, (m1 & ~0x3FFFull) | tag);
@@ -847,13 +849,14 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         }
                     }
                 }
-            } else if (i + 1 < N && gum_any) {
-                noise_bounds(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
+            } else if (i + 1 < N) {
+                prefetch_base(c, a, i + 1, v_begin, v_end, tid - 128);
+                if (gum_any) noise_bounds(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
             }
         } else {
             if (warp < kChainRows) {
                 const int b = warp;
-                const uint64_t m = tc::warp_max_u64(lane < 8 ? c.wbest[lane][b] : 0ull);
+                const uint64_t m = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b] : 0ull);
                 uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * kTcReplicas * Gp;
                 if (lane < kTcReplicas) tc::st_relaxed_u64(slots + lane * Gp + cta, (m & ~0x3FFFull) | tag);
                 slots += (cta % kTcReplicas) * Gp;

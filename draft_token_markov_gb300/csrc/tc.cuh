@@ -208,6 +208,14 @@ __device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t src_desc) {
                  : "memory");
 }
 
+// This warp's 32 lanes x 4 consecutive 32-bit columns.
+__device__ __forceinline__ void ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // This warp's 32 lanes x 8 consecutive 32-bit columns.
 __device__ __forceinline__ void ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile(
