@@ -147,6 +147,21 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(value: float) -> float:
+    """The maximum of a per-rank value over the default process group (the
+    rank's own value without one): the whole-job time of a step is the
+    slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def cpu_oracle_sample(seconds_hint: float = 20.0):
     """Time the oracle on a bounded sample of the workload: one call over the
     workload's first live row (all N positions), repeated while the total
@@ -290,11 +305,7 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st} in the timed region")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     chain_ms = step_ms
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms))
 
     # end to end: host (pinned) inputs copied in, tokens copied out, per step
     h_in = {k: v.pin_memory() for k, v in inp.items()}

@@ -79,6 +79,8 @@ def _declare(L):
         "markov_gumbel_noise": (i32, [P, P, P, i32, i32, i32, P, i64, P]),
         "markov_device_math": (i32, [i32, P, P, i64, P]),
         "markov_plan_query": (i64, [P, i32]),
+        "markov_plan_inject_status": (i32, [P, i32, c.c_uint32]),
+        "markov_selftest_wait": (i32, [i32, i32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -216,3 +218,18 @@ def markov_device_math(fn: int, x, out=None, stream=None):
                                     _dev(out, torch.float32, "out"), x.numel(), _stream(stream)),
            "markov_device_math")
     return out
+
+
+def markov_plan_inject_status(plan: Plan, code: int, where: int = 0):
+    """Record a device status as a failing kernel would (test hook)."""
+    _check(lib().markov_plan_inject_status(plan.handle, int(code), int(where)),
+           "markov_plan_inject_status")
+
+
+def markov_selftest_wait(which: int, timeout_us: int, stream=None) -> int:
+    """Run one bounded wait that nothing can complete; returns the status it
+    recorded (4 = MARKOV_ETIMEOUT when it gave up as designed)."""
+    code = lib().markov_selftest_wait(int(which), int(timeout_us), _stream(stream))
+    if code not in (0, 4):
+        raise MarkovError(code, "markov_selftest_wait")
+    return int(code)

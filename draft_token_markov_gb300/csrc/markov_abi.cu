@@ -429,6 +429,19 @@ markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n
     return MARKOV_OK;
 }
 
+markov_status markov_plan_inject_status(markov_plan *p, markov_status code, uint32_t where) {
+    if (!p || code == MARKOV_OK) return MARKOV_EINVAL;
+    DeviceGuard guard(p->d.device);
+    if (!guard.ok) return MARKOV_EDEVICE;
+    const uint32_t w[2] = {(uint32_t)code, where};
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(p->ctrl + 2, w, sizeof(w), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return MARKOV_ECUDA;
+    }
+    return MARKOV_OK;
+}
+
 int64_t markov_plan_query(const markov_plan *p, int32_t key) {
     if (!p) return -1;
     switch (key) {

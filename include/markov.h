@@ -236,6 +236,27 @@ enum {
 };
 int64_t markov_plan_query(const markov_plan *plan, int32_t key);
 
+/* Failure detection without a GPU fault (the pages have no counterpart:
+ * these are test hooks).
+ *
+ * markov_plan_inject_status records (code, where) in the plan's sticky
+ * device status exactly as a kernel that gave up would (synchronous copy, no
+ * kernel runs).  Every later call's kernels see it at their first check and
+ * return without computing or writing outputs, until markov_plan_status
+ * reports and clears it.  code must be a nonzero markov_status; EINVAL for a
+ * NULL plan or a zero code.
+ *
+ * markov_selftest_wait runs one of the kernels' bounded waits on a wait that
+ * nothing can complete, in a one-CTA kernel on `stream`, with a limit of
+ * timeout_us microseconds (1 .. 1e6): which 0 is the chain's grid barrier,
+ * which 1 an mbarrier wait of the tcgen05 chain.  It synchronizes the stream
+ * and returns the status the kernel recorded: MARKOV_ETIMEOUT when the wait
+ * gave up as designed, MARKOV_OK if it (wrongly) completed.  The kernel
+ * never traps and leaves the context usable.  Its scratch is a static device
+ * array, so concurrent calls race. */
+markov_status markov_plan_inject_status(markov_plan *plan, markov_status code, uint32_t where);
+markov_status markov_selftest_wait(int32_t which, int32_t timeout_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
