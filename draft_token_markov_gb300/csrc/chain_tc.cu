@@ -63,7 +63,6 @@ struct Ctl {
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t wbest[kEpiWarps][kChainRows];   // per epilogue warp, per row: best packed key
-    uint64_t cbuf[kEpiWarps][32];    // per epilogue warp: Gumbel survivors (id, row, logit)
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
@@ -91,11 +90,12 @@ __device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &) {
     return *(volatile const uint32_t *)&c.abort != 0u;
 }
 
-// At a CTA barrier: this CTA's flag, or (thread 0 only, one L2 load) an
-// error another CTA recorded.
-__device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a) {
+// At a CTA barrier: this CTA's flag, or (thread 0 only, one L2 load, when
+// `global` is set) an error another CTA recorded.  The Gumbel positions
+// check the global status in their exchange poll instead, off the barrier.
+__device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a, bool global = true) {
     bool s = *(volatile const uint32_t *)&c.abort != 0u;
-    if (threadIdx.x == 0 && !s && ld_acquire_u32(a.status) != 0u) {
+    if (global && threadIdx.x == 0 && !s && ld_acquire_u32(a.status) != 0u) {
         c.abort = 1u;
         s = true;
     }
@@ -125,38 +125,6 @@ __device__ __forceinline__ bool poll_max(const uint64_t *slots, int G, uint32_t 
         }
         if ((spin & 15u) == 15u) {
             bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
-            if (__any_sync(0xffffffffu, bad)) return false;
-        }
-    }
-}
-
-// Two rows' maxima at once (a row that is not live is skipped).
-__device__ __forceinline__ bool poll_max2(const uint64_t *s0, const uint64_t *s1, bool l0, bool l1,
-                                          int G, uint32_t tag, uint64_t deadline,
-                                          const SampleArgs &a, uint64_t &o0, uint64_t &o1) {
-    const int lane = threadIdx.x & 31;
-    for (uint32_t spin = 0;; ++spin) {
-        bool fresh = true;
-        uint64_t m0 = 0ull, m1 = 0ull;
-        for (int c = lane; c < G; c += 32) {
-            if (l0) {
-                const uint64_t k = tc::ld_relaxed_u64(s0 + c);
-                fresh = fresh && (uint32_t)(k & 0x3FFFu) == tag;
-                m0 = k > m0 ? k : m0;
-            }
-            if (l1) {
-                const uint64_t k = tc::ld_relaxed_u64(s1 + c);
-                fresh = fresh && (uint32_t)(k & 0x3FFFu) == tag;
-                m1 = k > m1 ? k : m1;
-            }
-        }
-        if (__all_sync(0xffffffffu, fresh)) {
-            o0 = tc::warp_max_u64(m0);
-            o1 = tc::warp_max_u64(m1);
-            return true;
-        }
-        if ((spin & 15u) == 15u) {
-            const bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
             if (__any_sync(0xffffffffu, bad)) return false;
         }
     }
@@ -222,17 +190,19 @@ __device__ __forceinline__ float gumbel_upper(uint64_t h) {
 }
 
 // The noise-bound bytes of position p for this CTA's ids, 8 row bytes per
-// id, written by the kEpiThreads threads of the epilogue warps (thread te
-// takes ids v_begin + te + kEpiThreads j, two at a time so that their hash
-// and log chains overlap).  The noise depends on seeds and positions only,
-// so it is drawn while the chain waits: position 0 while the head streams
-// in, position p + 1 while position p's winners are exchanged.  The row
-// loop stays rolled: the kernel's code must fit the instruction caches.
+// id, written by a group of NT threads (thread te takes ids v_begin + te +
+// NT j, two at a time so that their hash and log chains overlap).  The
+// noise depends on seeds and positions only, so it is drawn off the chain's
+// critical path: positions 0 and 1 by the epilogue warps while the head
+// streams in, position p + 1 by warps 2 and 3 (idle after the head load)
+// during position p.  The row loop stays rolled: the kernel's code must fit
+// the instruction caches.
+template <int NT>
 __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, int p,
                                              uint32_t gum_m, int v_begin, int v_end, int te) {
     uint2 *gq = reinterpret_cast<uint2 *>(a.noise) + (int64_t)p * a.V;
 #pragma unroll 1
-    for (int v0 = v_begin + te; v0 < v_end; v0 += 2 * kEpiThreads) {
+    for (int v0 = v_begin + te; v0 < v_end; v0 += 2 * NT) {
         uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};
 #pragma unroll 1
         for (int b = 0; b < kChainRows; ++b) {
@@ -242,26 +212,27 @@ __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, 
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const uint32_t qv =
-                    quantize_upper(gumbel_upper(dm_splitmix64(hb ^ (uint64_t)(v0 + kEpiThreads * u)))) << sh;
+                    quantize_upper(gumbel_upper(dm_splitmix64(hb ^ (uint64_t)(v0 + NT * u)))) << sh;
                 lo[u] |= b < 4 ? qv : 0u;
                 hi[u] |= b < 4 ? 0u : qv;
             }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u)
-            if (v0 + kEpiThreads * u < v_end) gq[v0 + kEpiThreads * u] = make_uint2(lo[u], hi[u]);
+            if (v0 + NT * u < v_end) gq[v0 + NT * u] = make_uint2(lo[u], hi[u]);
     }
 }
 
 // Warm L2 with this CTA's base logits of position p (every live row), one
-// 128-byte line per epilogue thread.
+// 128-byte line per thread of a group of NT threads.
+template <int NT>
 __device__ __forceinline__ void prefetch_base(const Ctl &c, const SampleArgs &a, int p, int v_begin,
                                               int v_end, int te) {
 #pragma unroll 1
     for (int b = 0; b < a.rows && b < kChainRows; ++b) {
         if (!c.live[b]) continue;
         const uint16_t *row = a.base + b * a.base_s0 + (int64_t)p * a.base_s1;
-        for (int v = v_begin + te * 64; v < v_end; v += kEpiThreads * 64) tc::prefetch_l2(row + v);
+        for (int v = v_begin + te * 64; v < v_end; v += NT * 64) tc::prefetch_l2(row + v);
     }
 }
 
@@ -275,10 +246,6 @@ __device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf
         y1 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y1, tf.inv_cap)));
     }
     return bf16x2_rn(y0, y1);
-}
-
-__device__ __forceinline__ uint32_t pick4(const uint32_t (&x)[4], int j) {
-    return j == 0 ? x[0] : j == 1 ? x[1] : j == 2 ? x[2] : x[3];
 }
 
 // The 4 MMAs (K = 4 x 16) of one 64-wide K chunk j of a tile into
@@ -371,16 +338,6 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
     __syncwarp();
 }
 
-// The exact key of one Gumbel survivor (id v, row b, cached logit l16),
-// folded into warp ew's best key of row b.
-__device__ __forceinline__ void survivor_key(Ctl &c, int i, int ew, uint32_t v, int b, uint32_t l16) {
-    const float lf = __uint_as_float(l16 << 16);
-    const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
-    const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
-    atomicMax(reinterpret_cast<unsigned long long *>(&c.wbest[ew][b]),
-              ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
-}
-
 // The epilogue of one position, run by the 16 warps 4-19: warp 4 + ew
 // serves accumulator wg = ew / 8 (the even / odd tiles), TMEM lane quarter
 // q = warp % 4 (the only lanes a warp may read) and rows rb..rb+3, rb =
@@ -388,25 +345,22 @@ __device__ __forceinline__ void survivor_key(Ctl &c, int i, int ew, uint32_t v, 
 // (the MMA's N columns).  Two warps per lane quarter halve every thread's
 // dependent chains, which bound this code.
 //
-// Pass 1, as each tile's bias arrives: the cached logits (two rows per
-// packed BF16 conversion), written out and, for up to 4 tiles, kept in a
-// register queue; for rows whose key is exact here (greedy rows,
-// inverse-CDF rows) the running maximum key with the lowest id; for Gumbel
-// rows a lower bound on every id's key (logit / T plus the lower end of its
-// noise byte).
-// Pass 2, Gumbel rows: the warp's maximum lower bound L is a lower bound on
-// the warp's best key, so only ids whose key upper bound reaches L can be
-// the maximum; only they get the exact key, so the warp's maximum (and the
-// token) is exactly that of keys computed for every id.
+// Per tile, as its bias arrives: the cached logits (two rows per packed
+// BF16 conversion), written out; for rows whose key is exact here (greedy
+// rows, inverse-CDF rows) the running maximum key with the lowest id.
+// Gumbel rows: a lower bound on every id's key (logit / T plus the lower
+// end of its noise byte) raises the warp's running threshold L (the largest
+// lower bound seen so far, a lower bound on the warp's best key); ids whose
+// key upper bound reaches L get their exact key at once.  L only grows, so
+// every id that could be the warp's maximum gets its exact key and the
+// warp's maximum (and the token) is exactly that of keys computed for every
+// id; the exact keys are computed while the next tile's MMAs run.
 // Leaves each warp's per-row best packed key in c.wbest[ew] (0 for rows it
 // does not own).
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
                                          const int i, const int t0, const int nt,
                                          const uint64_t timeout, uint32_t &dcount) {
-    constexpr int cpt = RANK / 64;
-    constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
-    constexpr bool kRegs = kTilesWG <= 4;                  // tiles kept in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1, rb = kRowsT * hr;
     const int V = a.V;
@@ -423,20 +377,16 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     const uint32_t *gq = reinterpret_cast<const uint32_t *>(a.noise) + ((int64_t)i * V) * 2 + hr;
     const uint16_t *base_i = a.base + (int64_t)i * a.base_s1 + rb * a.base_s0;
     uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1 + rb * a.cache_s0;
-    if (lane < kChainRows) c.wbest[ew][lane] = 0ull;
-    __syncwarp();
 
-    uint32_t bo[kRowsT], bv[kRowsT];   // best ordered key and its id
-    float lbm[kRowsT];                  // Gumbel rows: maximum key lower bound
+    uint32_t bo[kRowsT], bv[kRowsT];   // best ordered (exact) key and its id
+    float Lr[kRowsT], invT[kRowsT];    // Gumbel rows: the warp's running threshold
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
         bo[j] = 0u;
         bv[j] = 0u;
-        lbm[j] = __uint_as_float(0xff800000u);
+        Lr[j] = __uint_as_float(0xff800000u);
+        invT[j] = c.invT[rb + j];
     }
-    // the last 4 tiles' packed logits and noise bytes, newest first
-    uint32_t k0[2] = {0u, 0u}, k1[2] = {0u, 0u}, k2[2] = {0u, 0u}, k3[2] = {0u, 0u};
-    uint32_t g0 = 0u, g1 = 0u, g2 = 0u, g3 = 0u;
     uint32_t nb[kRowsT];
     uint32_t nq;
     auto load_tile = [&](int k, uint32_t (&bb)[kRowsT], uint32_t &qq) {
@@ -448,8 +398,6 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
     load_tile(wg, nb, nq);
-    bool ok = true;
-    int ntw = 0;
 #pragma unroll 1
     for (int k = wg; k < nt; k += 2) {
         uint32_t cb[kRowsT];
@@ -457,7 +405,8 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         for (int j = 0; j < kRowsT; ++j) cb[j] = nb[j];
         const uint32_t cq = nq;
         load_tile(k + 2, nb, nq);
-        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) { ok = false; break; }
+        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) break;
+        bool ok = true;
         if (lane == 0)
             ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -493,144 +442,51 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         for (int j = 0; j < kRowsT; ++j)
             if (valid && ((live_m >> j) & 1u))
                 cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
-        if (kRegs) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                k3[j] = k2[j];
-                k2[j] = k1[j];
-                k1[j] = k0[j];
-                k0[j] = lp[j];
-            }
-            g3 = g2;
-            g2 = g1;
-            g1 = g0;
-            g0 = cq;
-        }
+        uint32_t m4 = 0u;   // Gumbel rows of this id whose upper bound reaches L
 #pragma unroll
         for (int j = 0; j < kRowsT; ++j) {
-            const int b = rb + j;
             const float lf = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
             if ((gum_m >> j) & 1u) {
-                const float xa = lf * c.invT[b];
-                const float xl = __fmaf_rn(fabsf(xa), -1e-5f, xa);
+                const float xa = lf * invT[j];
                 const uint32_t qb = (cq >> (8 * j)) & 0xffu;
-                const float kl = __fadd_rn(xl, dequantize_lower(qb));
-                lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
+                const float kl = __fadd_rn(__fmaf_rn(fabsf(xa), -1e-5f, xa), dequantize_lower(qb));
+                const uint32_t wm =
+                    __reduce_max_sync(0xffffffffu, valid ? ordered_key(kl) : 0u);
+                const float lw = key_from_ordered(wm);
+                Lr[j] = (wm != 0u && lw > Lr[j]) ? lw : Lr[j];
+                const float ku = __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
+                m4 |= (valid && !(ku < Lr[j])) ? (1u << j) : 0u;
             } else {
                 float key = lf;
-                if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[b]);
+                if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[rb + j]);
                 const uint32_t o = ordered_key(key);
                 const bool better = valid && ((live_m >> j) & 1u) && o > bo[j];
                 bo[j] = better ? o : bo[j];
                 bv[j] = better ? (uint32_t)v : bv[j];
             }
         }
-        ++ntw;
-    }
-    if (gum_m != 0u && ok) {
-        float Lw[kRowsT], invT[kRowsT];
-#pragma unroll
-        for (int j = 0; j < kRowsT; ++j) {
-            invT[j] = c.invT[rb + j];
-            Lw[j] = ((gum_m >> j) & 1u)
-                        ? key_from_ordered(__reduce_max_sync(0xffffffffu, ordered_key(lbm[j])))
-                        : 0.0f;
-        }
-        // rows of one id whose key upper bound reaches the warp's L
-        auto test4 = [&](const uint32_t (&lq)[2], uint32_t qq) -> uint32_t {
-            uint32_t m4 = 0u;
-#pragma unroll
-            for (int j = 0; j < kRowsT; ++j) {
-                if (!((gum_m >> j) & 1u)) continue;
-                const float lf = __uint_as_float((j & 1) ? (lq[j >> 1] & 0xffff0000u) : (lq[j >> 1] << 16));
-                const float xa = lf * invT[j];
-                const float xu = __fmaf_rn(fabsf(xa), 1e-5f, xa);
-                const uint32_t qb = (qq >> (8 * j)) & 0xffu;
-                m4 |= !(__fadd_rn(xu, dequantize_upper(qb)) < Lw[j]) ? (1u << j) : 0u;
-            }
-            return m4;
-        };
-        uint32_t cand = 0u;   // bit 4 r + j: queue slot r, row rb + j survives
-        if (kRegs) {
-            // straight-line over the 4 queue slots (slot r holds tile
-            // wg + 2 (ntw - 1 - r)) so their tests overlap
-            auto slot = [&](int r, const uint32_t (&lq)[2], uint32_t qq) {
-                const int k = wg + 2 * (ntw - 1 - r);
-                const int v = (t0 + k) * 128 + q * 32 + lane;
-                if (r < ntw && v < V) cand |= test4(lq, qq) << (4 * r);
-            };
-            slot(0, k0, g0);
-            slot(1, k1, g1);
-            slot(2, k2, g2);
-            slot(3, k3, g3);
-        } else {
-#pragma unroll 1
-            for (int r = 0; r < ntw; ++r) {
-                const int k = wg + 2 * (ntw - 1 - r);
-                const int v = (t0 + k) * 128 + q * 32 + lane;
-                if (v >= V) continue;
-                uint32_t lq[2];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const uint32_t l0 = ((gum_m >> (2 * j)) & 1u)
-                                            ? (uint32_t)__ldcg(cache_i + (2 * j) * a.cache_s0 + v)
-                                            : 0u;
-                    const uint32_t l1 = ((gum_m >> (2 * j + 1)) & 1u)
-                                            ? (uint32_t)__ldcg(cache_i + (2 * j + 1) * a.cache_s0 + v)
-                                            : 0u;
-                    lq[j] = l0 | (l1 << 16);
-                }
-                uint32_t m4 = test4(lq, __ldcg(gq + 2 * v));
-                while (m4 != 0u) {
-                    const int j = __ffs(m4) - 1;
-                    m4 &= m4 - 1u;
-                    const uint32_t pr = j < 2 ? lq[0] : lq[1];
-                    survivor_key(c, i, ew, (uint32_t)v, rb + j, (pr >> (16 * (j & 1))) & 0xffffu);
-                }
-            }
-        }
-        if (kRegs) {
-            // the warp's survivors, one per lane: a prefix count over the lanes
-            // gives each candidate a slot of the warp's list
-            const uint32_t cnt = __popc(cand);
-            uint32_t pre = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
-                if (lane >= o) pre += y;
-            }
-            const uint32_t total = __shfl_sync(0xffffffffu, pre, 31);
-            const uint32_t first = pre - cnt;
-            for (uint32_t base = 0; base < total; base += 32u) {
-                uint32_t cm = cand, sl = first;
-                while (cm != 0u) {
-                    const int bit = __ffs(cm) - 1;
-                    cm &= cm - 1u;
-                    if (sl >= base && sl < base + 32u) {
-                        const int r = bit >> 2, j = bit & 3;
-                        const int k = wg + 2 * (ntw - 1 - r);
-                        const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
-                        const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
-                                                    : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
-                        const uint32_t l16 = (pr >> (16 * (j & 1))) & 0xffffu;
-                        c.cbuf[ew][sl - base] = ((uint64_t)v << 32) | ((uint64_t)(rb + j) << 16) | l16;
-                    }
-                    ++sl;
-                }
-                __syncwarp();
-                if (base + (uint32_t)lane < total) {
-                    const uint64_t e = c.cbuf[ew][lane];
-                    survivor_key(c, i, ew, (uint32_t)(e >> 32), (int)((e >> 16) & 7u),
-                                 (uint32_t)(e & 0xffffu));
-                }
-                __syncwarp();
+        // exact keys of this tile's candidates (few lanes, one code site)
+        while (m4 != 0u) {
+            const int j = __ffs(m4) - 1;
+            m4 &= m4 - 1u;
+            const uint32_t pr = j < 2 ? lp[0] : lp[1];
+            const float lf = __uint_as_float((j & 1) ? (pr & 0xffff0000u) : (pr << 16));
+            const uint64_t h = dm_splitmix64(c.hri[i][rb + j] ^ (uint64_t)v);
+            const uint32_t o = ordered_key(exact_key(lf, c.T[rb + j], h));
+            // ids grow with the tiles: strictly greater keeps the lowest id
+            const bool better = o > (j == 0 ? bo[0] : j == 1 ? bo[1] : j == 2 ? bo[2] : bo[3]);
+            if (better) {
+                if (j == 0) { bo[0] = o; bv[0] = (uint32_t)v; }
+                if (j == 1) { bo[1] = o; bv[1] = (uint32_t)v; }
+                if (j == 2) { bo[2] = o; bv[2] = (uint32_t)v; }
+                if (j == 3) { bo[3] = o; bv[3] = (uint32_t)v; }
             }
         }
     }
+    if (lane < kChainRows) c.wbest[ew][lane] = 0ull;
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
-        if ((gum_m >> j) & 1u) continue;
         const uint64_t pk =
             bo[j] != 0u ? (((uint64_t)bo[j] << 32) | ((uint64_t)(0x3FFFFu - bv[j]) << 14)) : 0ull;
         const uint64_t m = tc::warp_max_u64(pk);
@@ -678,6 +534,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         }
         tc::mbar_init_fence();
         c.tmem_ready = 0u;
+
         c.abort = ld_acquire_u32(a.status) != 0u ? 1u : 0u;
         c.call = *(volatile const uint32_t *)a.call_counter;
     }
@@ -704,6 +561,13 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     if (tid < N * kChainRows) {
         const int b = tid % kChainRows, i2 = tid / kChainRows;
         c.hri[i2][b] = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
+    }
+    if (cta == 0 && tid < kMaxSteps * kChainRows) {
+        // the next call's exchange words (the other call parity; the previous
+        // call, which used them, has completed): back to zero
+        const size_t np = (size_t)((c.call + 1u) & 1u);
+        a.win_max[(np * kMaxSteps * kChainRows + tid) * kLineU64] = 0ull;
+        if (tid < kMaxSteps) a.win_cnt[(np * kMaxSteps + tid) * kLineU32] = 0u;
     }
     if (warp < kChainRows && c.live[warp]) stage_embed<RANK>(b_s, a.embed, c.prev[warp], warp, lane);
     tc::fence_proxy_async_smem();
@@ -732,6 +596,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             issue_tiles<RANK, 0>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
         } else if (warp == 1) {
             issue_tiles<RANK, 1>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
+        } else if (warp < 4 && i > 0) {
+            // warps 2 and 3 after the head load: the next position's base
+            // logits into L2, off the chain's critical path
+            if (i + 1 < N) prefetch_base<64>(c, a, i + 1, v_begin, v_end, tid - 64);
         } else if (warp == 2) {
             if (lane == 0 && i == 0) {
                 for (int j = 0; j < nch; ++j) {
@@ -781,77 +649,131 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             __syncwarp();
         } else {
-            // warps 4..11
+            // warps 4..19: at position 0 the noise bounds of position 0 and the
+            // base logits into L2 while the head streams in; then the epilogue
             if (i == 0) {
                 const int te = tid - 128;
-                prefetch_base(c, a, 0, v_begin, v_end, te);
-                if (a.mode == 0 && gum_any)
-                    noise_bounds(c, a, 0, gum_mask, v_begin, v_end, te);
-                asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+                prefetch_base<kEpiThreads>(c, a, 0, v_begin, v_end, te);
+                if (a.mode == 0 && gum_any) {
+                    noise_bounds<kEpiThreads>(c, a, 0, gum_mask, v_begin, v_end, te);
+                    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+                }
+                if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
             if (a.mode == 1)
                 epilogue<RANK, true>(c, a, tmem, i, t0, nt, timeout, dcount);
             else
                 epilogue<RANK, false>(c, a, tmem, i, t0, nt, timeout, dcount);
         }
-        stop = __syncthreads_or(stop_vote(c, a));
+        stop = __syncthreads_or(stop_vote(c, a, a.mode != 0));
         if (stop) break;
 
         // ------------------------------- phase B: agree on every row's winner
         const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
         const uint32_t tag = epoch & 0x3FFFu;
         if (a.mode == 0) {
-            // Gumbel and greedy rows: warps 0-3 exchange rows w and w + 4 and
-            // stage the winners' embeddings as the next B operand; warps 4-11
-            // draw the next position's noise meanwhile
-            if (warp < 4) {
-                const int b0 = warp, b1 = warp + 4;
-                // every CTA writes its key into all kTcReplicas copies of the
-                // slot array and polls copy cta % kTcReplicas, which spreads
-                // the polling over more L2 lines
-                uint64_t *s0 = a.tc_keys + ((int64_t)i * kChainRows + b0) * kTcReplicas * Gp;
-                uint64_t *s1 = a.tc_keys + ((int64_t)i * kChainRows + b1) * kTcReplicas * Gp;
-                const uint64_t m0 = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b0] : 0ull);
-                const uint64_t m1 = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b1] : 0ull);
-                if (lane < kTcReplicas) {
-                    tc::st_relaxed_u64(s0 + lane * Gp + cta, (m0 & ~0x3FFFull) | tag);
-                    tc::st_relaxed_u64(s1 + lane * Gp + cta, (m1 & ~0x3FFFull) | tag);
-                }
-                s0 += (cta % kTcReplicas) * Gp;
-                s1 += (cta % kTcReplicas) * Gp;
-                const bool l0 = c.live[b0] != 0, l1 = c.live[b1] != 0;
-                // this CTA's candidates' embeddings into L2 while the others report
-                if (lane < 2 && (lane == 0 ? l0 : l1)) {
-                    const uint64_t m = lane == 0 ? m0 : m1;
-                    if (m != 0ull) {
-                        const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)unpack_id(m) * RANK);
-                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
-                    }
-                }
-                if (l0 || l1) {
-                    uint64_t w0 = 0ull, w1 = 0ull;
-                    if (!poll_max2(s0, s1, l0, l1, G, tag, tc::now_ns() + timeout, a, w0, w1)) {
-                        if (lane == 0) fail(c, a, 4u, 0x7000u + i);
-                    } else {
+            // Gumbel and greedy rows: warp 0 reports this CTA's best key per
+            // row and collects the winners; warps 0-3 stage the winners'
+            // embeddings (rows w and w + 4) as the next B operand.  Every CTA
+            // folds its keys into one word per (position, row) with red.max
+            // and then adds 1 to the position's counter (release); lane 0
+            // waits until all G CTAs have counted (acquire) and reads the 8
+            // words: one polled word per CTA keeps the L2 traffic low.  The
+            // words of one call parity are zeroed by the previous call.
+            if (warp < 2) {
+                if (warp == 0) {
+                    uint64_t m = 0ull;   // lane b < 8: row b's best key over the epilogue warps
+                    if (lane < kChainRows) {
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const bool lv = h == 0 ? l0 : l1;
-                            if (!lv) continue;
-                            const int b = h == 0 ? b0 : b1;
-                            const uint64_t w = h == 0 ? w0 : w1;
-                            const uint32_t id = unpack_id(w);
-                            if (lane == 0) {
-                                c.win[b] = w;
-                                c.prev[b] = (int64_t)id;
-                                if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
-                            }
-                            if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
+                        for (int e = 0; e < kEpiWarps; ++e) {
+                            const uint64_t x = c.wbest[e][lane];
+                            m = x > m ? x : m;
                         }
                     }
+                    uint64_t m8[kChainRows];
+#pragma unroll
+                    for (int b = 0; b < kChainRows; ++b) m8[b] = __shfl_sync(0xffffffffu, m, b);
+                    const size_t par = (size_t)(c.call & 1u);
+                    uint64_t *wm = a.win_max + ((par * kMaxSteps + i) * kChainRows) * kLineU64;
+                    uint32_t *wc = a.win_cnt + (par * kMaxSteps + i) * kLineU32;
+                    if (lane == 0) {
+                        bool ok = true;
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b)
+                            if (c.live[b]) tc::red_max_u64(wm + b * kLineU64, m8[b]);
+                        tc::red_release_add_u32(wc, 1u);
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        for (uint32_t spin = 0;; ++spin) {
+                            if ((int32_t)(ld_acquire_u32(wc) - (uint32_t)G) >= 0) break;
+                            if ((spin & 15u) == 15u &&
+                                (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (ok) {
+                            // all 8 loads in flight before any result is used
+                            uint64_t w8[kChainRows];
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b)
+                                w8[b] = c.live[b] ? tc::ld_relaxed_u64(wm + b * kLineU64) : 0ull;
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b) c.win[b] = w8[b];
+                        } else {
+                            fail(c, a, 4u, 0x7000u + i);
+                        }
+                    }
+                    __syncwarp();
                 }
-            } else if (i + 1 < N) {
-                prefetch_base(c, a, i + 1, v_begin, v_end, tid - 128);
-                if (gum_any) noise_bounds(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
+            }
+            if (warp < 4) {
+                asm volatile("bar.sync 3, 128;" ::: "memory");
+                // warps 0-3 stage rows w and w + 4: both gathers in flight at once
+                const int rb2[2] = {warp, warp + 4};
+                uint32_t idr[2];
+                uint4 ev[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int b = rb2[h];
+                    uint32_t id = unpack_id(c.win[b]);
+                    if (c.live[b] && id >= (uint32_t)V) {
+                        // no CTA reported a key for a live row: an internal
+                        // error; never index embed with it
+                        if (lane == 0) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB000u + i);
+                        id = 0u;
+                    }
+                    idr[h] = c.live[b] ? id : 0u;
+                    ev[h] = make_uint4(0u, 0u, 0u, 0u);
+                    if (c.live[b] && i + 1 < N && lane < RANK / 8)
+                        ev[h] = *reinterpret_cast<const uint4 *>(a.embed + (int64_t)idr[h] * RANK + 8 * lane);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int b = rb2[h];
+                    if (!c.live[b]) continue;
+                    if (lane == 0) {
+                        c.prev[b] = (int64_t)idr[h];
+                        if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)idr[h];
+                    }
+                    if (i + 1 < N && lane < RANK / 8) {
+                        const int chunk = lane >> 3, piece = lane & 7;
+                        *reinterpret_cast<uint4 *>(b_s + chunk * kBChunkBytes + b * 128 + ((piece ^ b) << 4)) = ev[h];
+                    }
+                }
+            }
+            if (warp < 4) {
+                // the control warps alone close the position: the next MMAs
+                // need only the staged B operand
+                tc::fence_proxy_async_smem();
+                tc::fence_before_sync();
+                asm volatile("bar.sync 4, 128;" ::: "memory");
+                tc::fence_after_sync();
+            } else if (i + 1 < N && gum_any) {
+                // the epilogue warps draw the next position's noise bounds while
+                // the winners are exchanged and the next MMAs start, and go
+                // straight on to the next epilogue (no CTA barrier between)
+                noise_bounds<kEpiThreads>(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
+                asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
             }
         } else {
             if (warp < kChainRows) {
@@ -1035,17 +957,21 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
                 }
+                if (id >= (uint32_t)V) {
+                    if (lane == 0) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB100u + i);
+                    id = 0u;
+                }
                 if (lane == 0) {
                     c.prev[b] = (int64_t)id;
                     if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
                 }
                 if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
             }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            stop = __syncthreads_or(stop_vote(c, a));
+            tc::fence_after_sync();
         }
-        tc::fence_proxy_async_smem();
-        tc::fence_before_sync();
-        stop = __syncthreads_or(stop_vote(c, a));
-        tc::fence_after_sync();
     }
 
     // --------------------------------------------------------------- exit

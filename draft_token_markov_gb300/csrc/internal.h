@@ -16,6 +16,10 @@ constexpr int kBatchThreads = 256;
 constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
 constexpr int kKeyPad = 16;            // u64 slots per CTA-key block are padded to 128 B
 constexpr int kTcReplicas = 8;         // copies of each tcgen05-chain key slot array
+constexpr int kLineU64 = 16;           // one 128-byte line per exchange word
+constexpr int kLineU32 = 32;
+constexpr size_t kWinMaxN = (size_t)2 * kMaxSteps * kChainRows * kLineU64;
+constexpr size_t kWinCntN = (size_t)2 * kMaxSteps * kLineU32;
 
 // The output-logit transform (muse_spark markov page, FusedMarkovParams):
 // multiplier and cap rounded to fp32, inv_cap = fp32(1) / fp32(cap).
@@ -56,6 +60,8 @@ struct SampleArgs {
     uint64_t *tc_sums;         // [N][8][Gp] inverse-CDF sum slots of the tcgen05 chain
     uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
+    uint64_t *win_max;         // [2 call parities][N][8 rows] x kLineU64: red.max words
+    uint32_t *win_cnt;         // [2 call parities][N] x kLineU32: CTAs that reported
     uint64_t timeout_ns;
     int grid;                  // persistent grid size (chain) or vocab blocks (batch)
 };

@@ -34,6 +34,8 @@ struct markov_plan {
     uint64_t *tc_sums = nullptr;
     uint32_t *sum_tags = nullptr;
     uint64_t *tok_slots = nullptr;
+    uint64_t *win_max = nullptr;
+    uint32_t *win_cnt = nullptr;
     size_t tc_slots_n = 0;
     size_t tc_keys_n = 0;         // tc_slots_n * kTcReplicas
     CUtensorMap tmap;
@@ -78,6 +80,8 @@ void free_plan(markov_plan *p) {
     if (p->tc_sums) cudaFree(p->tc_sums);
     if (p->sum_tags) cudaFree(p->sum_tags);
     if (p->tok_slots) cudaFree(p->tok_slots);
+    if (p->win_max) cudaFree(p->win_max);
+    if (p->win_cnt) cudaFree(p->win_cnt);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_noise) cudaEventDestroy(p->ev_noise);
     if (p->side) cudaStreamDestroy(p->side);
@@ -206,6 +210,10 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMalloc(&p->tc_sums, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sum_tags, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMalloc(&p->tok_slots, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->win_max, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->win_cnt, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
@@ -343,6 +351,8 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     a.tc_sums = p->tc_sums;
     a.sum_tags = p->sum_tags;
     a.tok_slots = p->tok_slots;
+    a.win_max = p->win_max;
+    a.win_cnt = p->win_cnt;
     a.timeout_ns = (uint64_t)p->d.timeout_ms * 1000000ull;
 
     if (use_tc && p->tmap_head != head) {
@@ -405,7 +415,9 @@ markov_status markov_plan_status(markov_plan *p) {
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess)
+        cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess)
         return MARKOV_ECUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MARKOV_ECUDA;
     return (markov_status)ctrl[2];

@@ -238,8 +238,23 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t *p) {
     return v;
 }
 
+__device__ __forceinline__ void ld_relaxed_v2_u64(const uint64_t *p, uint64_t &x, uint64_t &y) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
 __device__ __forceinline__ void st_relaxed_u64(uint64_t *p, uint64_t v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Fire-and-forget maximum into a global word (performed at L2).
+__device__ __forceinline__ void red_max_u64(uint64_t *p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Fire-and-forget add with release semantics: every earlier write of this
+// thread is visible to a thread that acquires the new value.
+__device__ __forceinline__ void red_release_add_u32(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_u32g(const uint32_t *p) {
