@@ -33,6 +33,7 @@
 // call's position epoch, in its own slot of a per-position array; every CTA
 // polls all slots until every tag is current (bounded) and takes the maximum.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "tc.cuh"
@@ -55,6 +56,7 @@ constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
 constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
 constexpr uint32_t kSmemB = 4 * kBChunkBytes;
 constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
+constexpr int kCList = 64;                // Gumbel survivors computed by the list warps
 
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
@@ -62,7 +64,14 @@ struct Ctl {
     uint64_t dfull[2];               // accumulator b holds a finished tile
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
-    uint64_t wbest[kEpiWarps][kChainRows];   // per epilogue warp, per row: best packed key
+    // Per position parity (a position's values are read while the next
+    // one's are written): per row, the CTA's best packed key and, for Gumbel
+    // rows, the CTA's threshold (ordered key of the largest key lower
+    // bound); the Gumbel survivor list and its length.
+    unsigned long long cbest[2][kChainRows];
+    uint32_t lcta[2][kChainRows];
+    uint32_t ncl[2];
+    uint64_t clist[kCList];          // survivor (id << 32 | row << 16 | logit bits)
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
@@ -83,6 +92,15 @@ struct Ctl {
 __device__ __forceinline__ void fail(Ctl &c, const SampleArgs &a, uint32_t code, uint32_t where) {
     set_status(a.status, code, where);
     c.abort = 1u;
+}
+
+// The per-position CTA maxima of one parity back to zero.
+__device__ __forceinline__ void clear_position(Ctl &c, int par) {
+    for (int b = 0; b < kChainRows; ++b) {
+        c.cbest[par][b] = 0ull;
+        c.lcta[par][b] = 0u;
+    }
+    c.ncl[par] = 0u;
 }
 
 // This CTA's abort flag (shared memory: cheap enough for hot loops).
@@ -338,6 +356,27 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
     __syncwarp();
 }
 
+// The exact key of Gumbel survivor (id v, row b, cached logit l16) folded
+// into the CTA's best key of that row (shared-memory atomic maximum).
+__device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, uint32_t l16) {
+    const float lf = __uint_as_float(l16 << 16);
+    const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
+    const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
+    atomicMax(&c.cbest[i & 1][b], ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
+}
+
+// An upper bound on the Gumbel key of an id from its logit and noise byte.
+__device__ __forceinline__ float key_upper(float lf, float invT, uint32_t qb) {
+    const float xa = lf * invT;
+    return __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
+}
+
+// Two upper bounds as FP16 pair, rounded toward +inf (still upper bounds;
+// NaN stays NaN, beyond the FP16 range becomes +inf).
+__device__ __forceinline__ __half2 half2_up(float lo, float hi) {
+    return __halves2half2(__float2half_ru(lo), __float2half_ru(hi));
+}
+
 // The epilogue of one position, run by the 16 warps 4-19: warp 4 + ew
 // serves accumulator wg = ew / 8 (the even / odd tiles), TMEM lane quarter
 // q = warp % 4 (the only lanes a warp may read) and rows rb..rb+3, rb =
@@ -345,25 +384,32 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
 // (the MMA's N columns).  Two warps per lane quarter halve every thread's
 // dependent chains, which bound this code.
 //
-// Per tile, as its bias arrives: the cached logits (two rows per packed
-// BF16 conversion), written out; for rows whose key is exact here (greedy
-// rows, inverse-CDF rows) the running maximum key with the lowest id.
-// Gumbel rows: a lower bound on every id's key (logit / T plus the lower
-// end of its noise byte) raises the warp's running threshold L (the largest
-// lower bound seen so far, a lower bound on the warp's best key); ids whose
-// key upper bound reaches L get their exact key at once.  L only grows, so
-// every id that could be the warp's maximum gets its exact key and the
-// warp's maximum (and the token) is exactly that of keys computed for every
-// id; the exact keys are computed while the next tile's MMAs run.
-// Leaves each warp's per-row best packed key in c.wbest[ew] (0 for rows it
-// does not own).
+// Pass 1, per tile as its bias arrives: the cached logits (two rows per
+// packed BF16 conversion), written out; for rows whose key is exact here
+// (greedy rows, inverse-CDF rows) the running maximum key with the lowest
+// id; for Gumbel rows a lower and an upper bound on every id's key (logit
+// / T plus the ends of the id's noise byte), keeping the largest lower
+// bound and, per queued tile, the upper bounds as FP16 rounded up.  Pass 2,
+// after the last tile (so that no exact key delays the next tile's
+// accumulator hand-back): the CTA's threshold L, the largest lower bound
+// over all its warps, is a lower bound on the CTA's best key, so only ids
+// whose upper bound reaches L can be that best.  They go to one list whose
+// exact keys two warps compute; the CTA's maximum (and the token) is exactly
+// that of keys computed for every id.  Leaves the CTA's per-row best packed
+// key in c.cbest[i & 1] (zeroed, with c.lcta and c.ncl, before the position).
+// `gum_any` (some row is a Gumbel row) is CTA-uniform: it decides whether the
+// epilogue warps meet at the two pass-2 barriers.
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
-                                         const int i, const int t0, const int nt,
+                                         const int i, const int t0, const int nt, const bool gum_any,
                                          const uint64_t timeout, uint32_t &dcount) {
+    constexpr int cpt = RANK / 64;
+    constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
+    constexpr bool kRegs = kTilesWG <= 4;                  // pass-2 tiles kept in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1, rb = kRowsT * hr;
     const int V = a.V;
+    const int par = i & 1;
     uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;   // this thread's 4 rows, bit j = row rb + j
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
@@ -379,14 +425,20 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1 + rb * a.cache_s0;
 
     uint32_t bo[kRowsT], bv[kRowsT];   // best ordered (exact) key and its id
-    float Lr[kRowsT], invT[kRowsT];    // Gumbel rows: the warp's running threshold
+    float lbm[kRowsT], invT[kRowsT];   // Gumbel rows: largest key lower bound
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
         bo[j] = 0u;
         bv[j] = 0u;
-        Lr[j] = __uint_as_float(0xff800000u);
+        lbm[j] = __uint_as_float(0xff800000u);
         invT[j] = c.invT[rb + j];
     }
+    // the last 4 tiles' packed logits and FP16 key upper bounds (rows j, j+1)
+    // newest first
+    uint32_t k0[2] = {0u, 0u}, k1[2] = {0u, 0u}, k2[2] = {0u, 0u}, k3[2] = {0u, 0u};
+    __half2 u0[2], u1[2], u2[2], u3[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) u0[j] = u1[j] = u2[j] = u3[j] = __float2half2_rn(0.0f);
     uint32_t nb[kRowsT];
     uint32_t nq;
     auto load_tile = [&](int k, uint32_t (&bb)[kRowsT], uint32_t &qq) {
@@ -398,6 +450,8 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
     load_tile(wg, nb, nq);
+    bool ok = true;
+    int ntw = 0;   // tiles this warp processed
 #pragma unroll 1
     for (int k = wg; k < nt; k += 2) {
         uint32_t cb[kRowsT];
@@ -405,8 +459,10 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         for (int j = 0; j < kRowsT; ++j) cb[j] = nb[j];
         const uint32_t cq = nq;
         load_tile(k + 2, nb, nq);
-        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) break;
-        bool ok = true;
+        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) {
+            ok = false;
+            break;
+        }
         if (lane == 0)
             ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -442,20 +498,17 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         for (int j = 0; j < kRowsT; ++j)
             if (valid && ((live_m >> j) & 1u))
                 cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
-        uint32_t m4 = 0u;   // Gumbel rows of this id whose upper bound reaches L
+        float ku[kRowsT];
 #pragma unroll
         for (int j = 0; j < kRowsT; ++j) {
             const float lf = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
+            ku[j] = 0.0f;
             if ((gum_m >> j) & 1u) {
                 const float xa = lf * invT[j];
                 const uint32_t qb = (cq >> (8 * j)) & 0xffu;
                 const float kl = __fadd_rn(__fmaf_rn(fabsf(xa), -1e-5f, xa), dequantize_lower(qb));
-                const uint32_t wm =
-                    __reduce_max_sync(0xffffffffu, valid ? ordered_key(kl) : 0u);
-                const float lw = key_from_ordered(wm);
-                Lr[j] = (wm != 0u && lw > Lr[j]) ? lw : Lr[j];
-                const float ku = __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
-                m4 |= (valid && !(ku < Lr[j])) ? (1u << j) : 0u;
+                lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
+                ku[j] = __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
             } else {
                 float key = lf;
                 if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[rb + j]);
@@ -465,32 +518,120 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 bv[j] = better ? (uint32_t)v : bv[j];
             }
         }
-        // exact keys of this tile's candidates (few lanes, one code site)
-        while (m4 != 0u) {
-            const int j = __ffs(m4) - 1;
-            m4 &= m4 - 1u;
-            const uint32_t pr = j < 2 ? lp[0] : lp[1];
-            const float lf = __uint_as_float((j & 1) ? (pr & 0xffff0000u) : (pr << 16));
-            const uint64_t h = dm_splitmix64(c.hri[i][rb + j] ^ (uint64_t)v);
-            const uint32_t o = ordered_key(exact_key(lf, c.T[rb + j], h));
-            // ids grow with the tiles: strictly greater keeps the lowest id
-            const bool better = o > (j == 0 ? bo[0] : j == 1 ? bo[1] : j == 2 ? bo[2] : bo[3]);
-            if (better) {
-                if (j == 0) { bo[0] = o; bv[0] = (uint32_t)v; }
-                if (j == 1) { bo[1] = o; bv[1] = (uint32_t)v; }
-                if (j == 2) { bo[2] = o; bv[2] = (uint32_t)v; }
-                if (j == 3) { bo[3] = o; bv[3] = (uint32_t)v; }
+        if (kRegs && gum_m != 0u) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                k3[j] = k2[j];
+                k2[j] = k1[j];
+                k1[j] = k0[j];
+                k0[j] = lp[j];
+                u3[j] = u2[j];
+                u2[j] = u1[j];
+                u1[j] = u0[j];
+                u0[j] = half2_up(ku[2 * j], ku[2 * j + 1]);
             }
         }
+        ++ntw;
     }
-    if (lane < kChainRows) c.wbest[ew][lane] = 0ull;
-    __syncwarp();
+    // rows with exact keys: the warp's best into the CTA's
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
+        if ((gum_m >> j) & 1u) continue;
         const uint64_t pk =
             bo[j] != 0u ? (((uint64_t)bo[j] << 32) | ((uint64_t)(0x3FFFFu - bv[j]) << 14)) : 0ull;
         const uint64_t m = tc::warp_max_u64(pk);
-        if (lane == 0) c.wbest[ew][rb + j] = m;
+        if (lane == 0 && m != 0ull) atomicMax(&c.cbest[par][rb + j], (unsigned long long)m);
+    }
+    if (!gum_any) return;
+
+    // ---- pass 2 (Gumbel rows): the CTA threshold, then the survivors
+    uint32_t lw = 0u;   // lane j < 4: ordered warp threshold of row rb + j
+#pragma unroll
+    for (int j = 0; j < kRowsT; ++j) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, ((gum_m >> j) & 1u) ? ordered_key(lbm[j]) : 0u);
+        lw = lane == j ? m : lw;
+    }
+    if (ok && ntw > 0 && lane < kRowsT && lw != 0u) atomicMax(&c.lcta[par][rb + lane], lw);
+    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+    uint32_t cand = 0u;   // bit 4 r + j: queued tile r (newest first), row rb + j survives
+    float Lc[kRowsT];
+#pragma unroll
+    for (int j = 0; j < kRowsT; ++j) {
+        const uint32_t o = *(volatile uint32_t *)&c.lcta[par][rb + j];
+        // no bound recorded (no valid id): nothing can survive
+        Lc[j] = o != 0u ? key_from_ordered(o) : __uint_as_float(0x7f800000u);
+    }
+    if (kRegs) {
+        const __half2 L01 = __halves2half2(__float2half_rd(Lc[0]), __float2half_rd(Lc[1]));
+        const __half2 L23 = __halves2half2(__float2half_rd(Lc[2]), __float2half_rd(Lc[3]));
+        auto slot = [&](int r, const __half2 (&uu)[2]) {
+            const int k = wg + 2 * (ntw - 1 - r);
+            const int v = (t0 + k) * 128 + q * 32 + lane;
+            if (r < ntw && v < V) {
+                const uint32_t m01 = __hgeu2_mask(uu[0], L01), m23 = __hgeu2_mask(uu[1], L23);
+                const uint32_t b4 = (m01 & 1u) | ((m01 >> 15) & 2u) | ((m23 & 1u) << 2) | ((m23 >> 13) & 8u);
+                cand |= (b4 & gum_m) << (4 * r);
+            }
+        };
+        slot(0, u0);
+        slot(1, u1);
+        slot(2, u2);
+        slot(3, u3);
+    }
+    // append this warp's survivors to the CTA list (a prefix count over the
+    // lanes, one shared-memory atomic per warp); survivors beyond the list
+    // get their key from their own lane at once
+    const uint32_t cnt = __popc(cand);
+    uint32_t pre = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += y;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, pre, 31);
+    uint32_t at = 0u;
+    if (lane == 31 && total != 0u) at = atomicAdd(&c.ncl[par], total);
+    at = __shfl_sync(0xffffffffu, at, 31) + pre - cnt;
+    while (cand != 0u) {
+        const int bit = __ffs(cand) - 1;
+        cand &= cand - 1u;
+        const int r = bit >> 2, j = bit & 3;
+        const int k = wg + 2 * (ntw - 1 - r);
+        const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
+        const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
+                                    : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
+        const uint32_t l16 = (pr >> (16 * (j & 1))) & 0xffffu;
+        if (at < (uint32_t)kCList)
+            c.clist[at] = ((uint64_t)v << 32) | ((uint64_t)(rb + j) << 16) | l16;
+        else
+            survivor_key(c, i, v, rb + j, l16);
+        ++at;
+    }
+    if (!kRegs && ok) {
+        // more tiles than registers hold (small ranks): the cached logits and
+        // noise bytes are read back (L2) tile by tile, exact bounds
+#pragma unroll 1
+        for (int r = 0; r < ntw; ++r) {
+            const int k = wg + 2 * r;
+            const int v = (t0 + k) * 128 + q * 32 + lane;
+            if (v >= V) continue;
+            const uint32_t qq = __ldcg(gq + 2 * v);
+#pragma unroll
+            for (int j = 0; j < kRowsT; ++j) {
+                if (!((gum_m >> j) & 1u)) continue;
+                const uint32_t l16 = (uint32_t)__ldcg(cache_i + j * a.cache_s0 + v);
+                if (!(key_upper(__uint_as_float(l16 << 16), invT[j], (qq >> (8 * j)) & 0xffu) < Lc[j]))
+                    survivor_key(c, i, (uint32_t)v, rb + j, l16);
+            }
+        }
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
+    // the list's exact keys: entry e by lane e % 32 of epilogue warp e / 32
+    const uint32_t n = *(volatile uint32_t *)&c.ncl[par];
+    const uint32_t e = (uint32_t)ew * 32u + (uint32_t)lane;
+    if (e < n && e < (uint32_t)kCList) {
+        const uint64_t en = c.clist[e];
+        survivor_key(c, i, (uint32_t)(en >> 32), (int)((en >> 16) & 7u), (uint32_t)(en & 0xffffu));
     }
 }
 
@@ -534,6 +675,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         }
         tc::mbar_init_fence();
         c.tmem_ready = 0u;
+        clear_position(c, 0);
 
         c.abort = ld_acquire_u32(a.status) != 0u ? 1u : 0u;
         c.call = *(volatile const uint32_t *)a.call_counter;
@@ -661,9 +803,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
             if (a.mode == 1)
-                epilogue<RANK, true>(c, a, tmem, i, t0, nt, timeout, dcount);
+                epilogue<RANK, true>(c, a, tmem, i, t0, nt, false, timeout, dcount);
             else
-                epilogue<RANK, false>(c, a, tmem, i, t0, nt, timeout, dcount);
+                epilogue<RANK, false>(c, a, tmem, i, t0, nt, gum_any, timeout, dcount);
         }
         stop = __syncthreads_or(stop_vote(c, a, a.mode != 0));
         if (stop) break;
@@ -680,16 +822,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             // waits until all G CTAs have counted (acquire) and reads the 8
             // words: one polled word per CTA keeps the L2 traffic low.  The
             // words of one call parity are zeroed by the previous call.
-            if (warp < 2) {
+            if (warp == 0 || warp == 2) {
                 if (warp == 0) {
-                    uint64_t m = 0ull;   // lane b < 8: row b's best key over the epilogue warps
-                    if (lane < kChainRows) {
-#pragma unroll
-                        for (int e = 0; e < kEpiWarps; ++e) {
-                            const uint64_t x = c.wbest[e][lane];
-                            m = x > m ? x : m;
-                        }
-                    }
+                    // lane b < 8: row b's best key in this CTA
+                    const uint64_t m = lane < kChainRows ? (uint64_t)c.cbest[i & 1][lane] : 0ull;
                     uint64_t m8[kChainRows];
 #pragma unroll
                     for (int b = 0; b < kChainRows; ++b) m8[b] = __shfl_sync(0xffffffffu, m, b);
@@ -724,6 +860,17 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         }
                     }
                     __syncwarp();
+                } else if (lane < kChainRows && c.live[lane]) {
+                    // warp 2: this CTA's candidate of row b = lane into L2
+                    // while the winners are agreed (the winning CTA's
+                    // prefetch serves every CTA's staging gather)
+                    const uint64_t m = c.cbest[i & 1][lane];
+                    const uint32_t id = unpack_id(m);
+                    if (m != 0ull && id < (uint32_t)V && i + 1 < N) {
+                        const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)id * RANK);
+#pragma unroll
+                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
+                    }
                 }
             }
             if (warp < 4) {
@@ -768,17 +915,21 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 tc::fence_before_sync();
                 asm volatile("bar.sync 4, 128;" ::: "memory");
                 tc::fence_after_sync();
-            } else if (i + 1 < N && gum_any) {
-                // the epilogue warps draw the next position's noise bounds while
-                // the winners are exchanged and the next MMAs start, and go
-                // straight on to the next epilogue (no CTA barrier between)
-                noise_bounds<kEpiThreads>(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
+            } else if (i + 1 < N) {
+                // the epilogue warps clear the next position's CTA maxima (their
+                // last reader finished before this position's phase-A barrier),
+                // draw its noise bounds while the winners are exchanged and the
+                // next MMAs start, and go straight on to the next epilogue (no
+                // CTA barrier between; their own barrier orders the clearing
+                // before the next position's atomics)
+                if (tid == 128) clear_position(c, (i + 1) & 1);
+                if (gum_any) noise_bounds<kEpiThreads>(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
                 asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
             }
         } else {
             if (warp < kChainRows) {
                 const int b = warp;
-                const uint64_t m = tc::warp_max_u64(lane < kEpiWarps ? c.wbest[lane][b] : 0ull);
+                const uint64_t m = c.cbest[i & 1][b];
                 uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * kTcReplicas * Gp;
                 if (lane < kTcReplicas) tc::st_relaxed_u64(slots + lane * Gp + cta, (m & ~0x3FFFull) | tag);
                 slots += (cta % kTcReplicas) * Gp;
@@ -967,6 +1118,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 }
                 if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
             }
+            // the next position's CTA maxima (last read before this
+            // position's phase-A barrier)
+            if (tid == 128 && i + 1 < N) clear_position(c, (i + 1) & 1);
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             stop = __syncthreads_or(stop_vote(c, a));
