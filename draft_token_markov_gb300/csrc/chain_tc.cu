@@ -266,43 +266,24 @@ __device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf
     return bf16x2_rn(y0, y1);
 }
 
-// The 4 MMAs (K = 4 x 16) of one 64-wide K chunk j of a tile into
-// accumulator d, with A in TMEM (j < kTmemChunks) or in shared memory.
-// Straight-line code with constant offsets: the operands stay in uniform
-// registers and one MMA issues every ~40 cycles per issuing thread (a
-// rolled loop here measured twice as slow).
-__device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t tmem, uint64_t adesc0, uint64_t bd,
-                                          int j, bool first) {
-    if (j < kTmemChunks) {
-        const uint32_t at = tmem + 32u * j;
-        tc::mma_tmemA_elect(d, at, bd, kIdesc, first ? 0u : 1u);
-        tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
-        tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
-        tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
-    } else {
-        const uint64_t ad = adesc0 + (uint64_t)(((j - kTmemChunks) * kChunkBytes) >> 4);
-        tc::mma_smemA_elect(d, ad, bd, kIdesc, first ? 0u : 1u);
-        tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
-        tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
-        tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
-    }
-}
-
-// The MMAs of accumulator W (warp W): tiles W, W + 2, ...; per tile, K
-// chunk by K chunk, 4 MMAs of K = 16 each.  The whole warp runs the loop and
-// one elected lane issues.  W is a template parameter so that the tile and
-// chunk indices, and with them the MMA operands, are warp-uniform values.
-// Position 0 awaits each chunk as the head streams in; later positions run
-// a loop with no waits inside (its code shape sets the issue rate).
-template <int RANK, int W>
-__device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const uint32_t tmem,
+// The MMAs of accumulator W (issued by warp W): tiles W, W + 2, ...; per
+// tile, K chunk by K chunk, 4 MMAs of K = 16 each, with A in TMEM (chunk j
+// < kTmemChunks) or in shared memory.  The whole warp runs the loop and one
+// elected lane issues.  Both warps run one copy of this code, kept small:
+// the kernel's code is far larger than the SM's instruction caches, and an
+// unrolled issue loop (16 KB per copy) measured several times slower inside
+// the kernel than alone, its fetches competing with the epilogue's.
+// Position 0 awaits each chunk as the head streams in.
+template <int RANK>
+__device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const uint32_t tmem, const int W,
                                             const int i, const int nt, const int ntm,
                                             const uint32_t b_sa, const uint32_t head_sa,
                                             const uint64_t timeout, uint32_t &uses) {
     constexpr int cpt = RANK / 64;
     const int lane = threadIdx.x & 31;
-    const uint32_t d = tmem + kDCol + 16u * W;
+    const uint32_t d = tmem + kDCol + 16u * (uint32_t)W;
     const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
+#pragma unroll 1
     for (int k = W; k < nt; k += 2) {
         if (__any_sync(0xffffffffu, aborted(c, a))) break;
         bool freed = true;
@@ -313,11 +294,11 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
             break;
         }
         tc::fence_after_sync();
-        if (i == 0) {
-            bool ok = true;
+        bool ok = true;
 #pragma unroll 1
-            for (int kc = 0; kc < cpt; ++kc) {
-                const int j = k * cpt + kc;
+        for (int kc = 0; kc < cpt; ++kc) {
+            const int j = k * cpt + kc;
+            if (i == 0) {
                 const uint64_t dl = tc::now_ns() + timeout;
                 if (j < kTmemChunks) {
                     while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
@@ -340,16 +321,25 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
                     if (lane == 0) fail(c, a, 4u, 0x2000u + j);
                     break;
                 }
-                // descriptors advance by (bytes >> 4) in their address field
-                mma_chunk(d, tmem, adesc0, bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4), j, kc == 0);
             }
-            if (!ok) break;
-        } else {
-#pragma unroll
-            for (int kc = 0; kc < cpt; ++kc)
-                mma_chunk(d, tmem, adesc0, bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4), k * cpt + kc,
-                          kc == 0);
+            // descriptors advance by (bytes >> 4) in their address field
+            const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
+            const uint32_t acc0 = kc == 0 ? 0u : 1u;
+            if (j < kTmemChunks) {
+                const uint32_t at = tmem + 32u * (uint32_t)j;
+                tc::mma_tmemA_elect(d, at, bd, kIdesc, acc0);
+                tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
+                tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
+                tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
+            } else {
+                const uint64_t ad = adesc0 + (uint64_t)(((uint32_t)(j - kTmemChunks) * kChunkBytes) >> 4);
+                tc::mma_smemA_elect(d, ad, bd, kIdesc, acc0);
+                tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
+                tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
+                tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
+            }
         }
+        if (!ok) break;
         tc::commit_elect(tc::smem_u32(&c.dfull[W]));
         ++uses;
     }
@@ -734,10 +724,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     bool stop = __syncthreads_or(c.abort != 0u);
     for (int i = 0; i < N && !stop; ++i) {
         // ------------------------------------- phase A: MMA and epilogue
-        if (warp == 0) {
-            issue_tiles<RANK, 0>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
-        } else if (warp == 1) {
-            issue_tiles<RANK, 1>(c, a, tmem, i, nt, ntm, b_sa, head_sa, timeout, uses);
+        if (warp < 2) {
+            issue_tiles<RANK>(c, a, tmem, warp, i, nt, ntm, b_sa, head_sa, timeout, uses);
         } else if (warp < 4 && i > 0) {
             // warps 2 and 3 after the head load: the next position's base
             // logits into L2, off the chain's critical path
