@@ -94,6 +94,27 @@ __device__ __forceinline__ void fail(Ctl &c, const SampleArgs &a, uint32_t code,
     c.abort = 1u;
 }
 
+// The staging slot of head chunk j and the load's phase in that slot.
+// TMEM chunks j < kSmemChunks take slot j (phase 0); the e = ntm -
+// kSmemChunks later TMEM chunks reuse the last e slots (phase 1), whose
+// first chunks land first; the shared-memory chunks j >= ntm (only when ntm
+// = kTmemChunks) stay in slot j - kTmemChunks, after that slot's TMEM
+// chunks.  So the loads of shared-memory chunks for the first slots wait
+// on early copies and are not queued behind the second TMEM round.
+__device__ __forceinline__ void chunk_slot(int j, int ntm, int &slot, uint32_t &phase) {
+    const int e = ntm > kSmemChunks ? ntm - kSmemChunks : 0;
+    if (j < kSmemChunks && j < ntm) {
+        slot = j;
+        phase = 0u;
+    } else if (j < ntm) {
+        slot = j - e;
+        phase = 1u;
+    } else {
+        slot = j - kTmemChunks;
+        phase = 1u + (slot >= kSmemChunks - e ? 1u : 0u);
+    }
+}
+
 // The per-position CTA maxima of one parity back to zero.
 __device__ __forceinline__ void clear_position(Ctl &c, int par) {
     for (int b = 0; b < kChainRows; ++b) {
@@ -312,8 +333,9 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
                     while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
                         if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
                     }
-                    const int s = j - kTmemChunks;
-                    const uint32_t u = 1u + (s + kSmemChunks < ntm ? 1u : 0u);
+                    int s;
+                    uint32_t u;
+                    chunk_slot(j, ntm, s, u);
                     if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
                 }
                 ok = __all_sync(0xffffffffu, ok);
@@ -627,7 +649,9 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
 
 }  // namespace
 
-template <int RANK>
+// MODE 0: Gumbel and greedy rows; MODE 1: inverse-CDF and greedy rows (one
+// kernel per mode keeps each kernel's code smaller).
+template <int RANK, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, int noise_ready) {
     constexpr int cpt = RANK / 64;                 // K-chunks per 128-id tile
@@ -711,7 +735,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     uint32_t gum_mask = 0u;   // Gumbel rows (sampling rows of the Gumbel mode)
 #pragma unroll
     for (int b = 0; b < kChainRows; ++b) gum_mask |= c.sampling[b] ? (1u << b) : 0u;
-    if (a.mode != 0) gum_mask = 0u;
+    if (MODE != 0) gum_mask = 0u;
     const bool gum_any = gum_mask != 0u;
 
     // per-role persistent state
@@ -735,16 +759,13 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 for (int j = 0; j < nch; ++j) {
                     if (aborted(c, a)) break;
                     int s;
+                    uint32_t ph;
+                    chunk_slot(j, ntm, s, ph);
                     bool ok = true;
                     const uint64_t dl = tc::now_ns() + timeout;
-                    if (j < ntm) {
-                        s = j % kSmemChunks;
-                        if (j >= kSmemChunks) ok = tc::mbar_wait(tc::smem_u32(&c.cpdone[s]), 0u, dl);
-                    } else {
-                        s = j - kTmemChunks;
-                        ok = tc::mbar_wait(tc::smem_u32(&c.cpdone[s]),
-                                           (s + kSmemChunks < ntm) ? 1u : 0u, dl);
-                    }
+                    // the slot's previous (TMEM) chunk has been copied out:
+                    // copy number ph - 1 of this slot
+                    if (ph > 0u) ok = tc::mbar_wait(tc::smem_u32(&c.cpdone[s]), (ph - 1u) & 1u, dl);
                     if (!ok) { fail(c, a, 4u, 0x3000u + j); break; }
                     const uint32_t bar = tc::smem_u32(&c.full[s]);
                     tc::mbar_expect_tx(bar, kChunkBytes);
@@ -756,25 +777,50 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             __syncwarp();
         } else if (warp == 3) {
             if (lane == 0 && i == 0) {
-                for (int j = 0; j < ntm; ++j) {
+                // chunk j's copy is issued as soon as its load lands; its
+                // completion is awaited only after the next copy is issued,
+                // so the copies' latency overlaps the loads' (unless both
+                // chunks share a slot: a parity wait sees one phase at a time)
+                bool early = false;
+                for (int j = 0; j <= ntm; ++j) {
                     if (aborted(c, a)) break;
-                    const int s = j % kSmemChunks;
-                    const uint32_t par = (uint32_t)(j / kSmemChunks) & 1u;
-                    if (!tc::mbar_wait(tc::smem_u32(&c.full[s]), par, tc::now_ns() + timeout)) {
-                        fail(c, a, 4u, 0x4000u + j);
-                        break;
-                    }
+                    int sp = 0;
+                    uint32_t pp = 0u;
+                    if (j > 0) chunk_slot(j - 1, ntm, sp, pp);
+                    if (j < ntm) {
+                        int s;
+                        uint32_t ph;
+                        chunk_slot(j, ntm, s, ph);
+                        if (!tc::mbar_wait(tc::smem_u32(&c.full[s]), ph & 1u, tc::now_ns() + timeout)) {
+                            fail(c, a, 4u, 0x4000u + j);
+                            break;
+                        }
+                        if (j > 0 && sp == s) {
+                            // (already complete: this load waited for it)
+                            if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[sp]), pp & 1u, tc::now_ns() + timeout)) {
+                                fail(c, a, 4u, 0x5000u + j - 1);
+                                break;
+                            }
+                            tc::fence_before_sync();
+                            *(volatile uint32_t *)&c.tmem_ready = (uint32_t)j;
+                            early = true;
+                        }
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::cp_128x256b(tmem + 32u * j + 8u * ks,
-                                        tc::sw128_desc(head_sa + s * kChunkBytes + 32 * ks));
-                    tc::commit(tc::smem_u32(&c.cpdone[s]));
-                    if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[s]), par, tc::now_ns() + timeout)) {
-                        fail(c, a, 4u, 0x5000u + j);
-                        break;
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc::cp_128x256b(tmem + 32u * j + 8u * ks,
+                                            tc::sw128_desc(head_sa + s * kChunkBytes + 32 * ks));
+                        tc::commit(tc::smem_u32(&c.cpdone[s]));
                     }
-                    tc::fence_before_sync();
-                    *(volatile uint32_t *)&c.tmem_ready = (uint32_t)(j + 1);
+                    if (j > 0 && !early) {
+                        // chunk j - 1, in another slot than chunk j's
+                        if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[sp]), pp & 1u, tc::now_ns() + timeout)) {
+                            fail(c, a, 4u, 0x5000u + j - 1);
+                            break;
+                        }
+                        tc::fence_before_sync();
+                        *(volatile uint32_t *)&c.tmem_ready = (uint32_t)j;
+                    }
+                    early = false;
                 }
             }
             __syncwarp();
@@ -784,24 +830,24 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (i == 0) {
                 const int te = tid - 128;
                 prefetch_base<kEpiThreads>(c, a, 0, v_begin, v_end, te);
-                if (a.mode == 0 && gum_any) {
+                if (MODE == 0 && gum_any) {
                     noise_bounds<kEpiThreads>(c, a, 0, gum_mask, v_begin, v_end, te);
                     asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
                 }
                 if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
-            if (a.mode == 1)
+            if (MODE == 1)
                 epilogue<RANK, true>(c, a, tmem, i, t0, nt, false, timeout, dcount);
             else
                 epilogue<RANK, false>(c, a, tmem, i, t0, nt, gum_any, timeout, dcount);
         }
-        stop = __syncthreads_or(stop_vote(c, a, a.mode != 0));
+        stop = __syncthreads_or(stop_vote(c, a, MODE != 0));
         if (stop) break;
 
         // ------------------------------- phase B: agree on every row's winner
         const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
         const uint32_t tag = epoch & 0x3FFFu;
-        if (a.mode == 0) {
+        if (MODE == 0) {
             // Gumbel and greedy rows: warp 0 reports this CTA's best key per
             // row and collects the winners; warps 0-3 stage the winners'
             // embeddings (rows w and w + 4) as the next B operand.  Every CTA
@@ -941,7 +987,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             // weight sums floor(exp(x - M) 2^40), then the CTA whose prefix range
             // holds mulhi64(H, S) scans its ids for the token
             bool cdf_any = false;
-            if (a.mode == 1) {
+            if (MODE == 1) {
                 for (int b = 0; b < R && b < kChainRows; ++b) {
                     if (!c.sampling[b]) continue;
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
@@ -1092,7 +1138,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (warp < kChainRows && c.live[warp]) {
                 const int b = warp;
                 uint32_t id = unpack_id(c.win[b]);
-                if (a.mode == 1 && c.sampling[b]) {
+                if (MODE == 1 && c.sampling[b]) {
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
                 }
@@ -1144,8 +1190,10 @@ int chain_tc_max_chunks() { return kMaxChunks; }
 
 cudaError_t chain_tc_prepare() {
     cudaError_t e = cudaSuccess;
-    for (const void *fn : {(const void *)chain_tc_kernel<64>, (const void *)chain_tc_kernel<128>,
-                           (const void *)chain_tc_kernel<256>}) {
+    for (const void *fn :
+         {(const void *)chain_tc_kernel<64, 0>, (const void *)chain_tc_kernel<128, 0>,
+          (const void *)chain_tc_kernel<256, 0>, (const void *)chain_tc_kernel<64, 1>,
+          (const void *)chain_tc_kernel<128, 1>, (const void *)chain_tc_kernel<256, 1>}) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
         if (e != cudaSuccess) return e;
     }
@@ -1153,7 +1201,7 @@ cudaError_t chain_tc_prepare() {
 }
 
 cudaError_t chain_tc_occupancy(int *blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, chain_tc_kernel<256>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, chain_tc_kernel<256, 0>,
                                                          kThreads, kDynSmem);
 }
 
@@ -1161,10 +1209,11 @@ cudaError_t launch_chain_tc(const SampleArgs &a, const CUtensorMap &tmap, int no
                             cudaStream_t stream) {
     void *args[] = {(void *)&a, (void *)&tmap, (void *)&noise_ready};
     const void *fn = nullptr;
+    const bool cdf = a.mode == 1;
     switch (a.r) {
-        case 64: fn = (const void *)chain_tc_kernel<64>; break;
-        case 128: fn = (const void *)chain_tc_kernel<128>; break;
-        case 256: fn = (const void *)chain_tc_kernel<256>; break;
+        case 64: fn = cdf ? (const void *)chain_tc_kernel<64, 1> : (const void *)chain_tc_kernel<64, 0>; break;
+        case 128: fn = cdf ? (const void *)chain_tc_kernel<128, 1> : (const void *)chain_tc_kernel<128, 0>; break;
+        case 256: fn = cdf ? (const void *)chain_tc_kernel<256, 1> : (const void *)chain_tc_kernel<256, 0>; break;
         default: return cudaErrorInvalidValue;
     }
     return cudaLaunchCooperativeKernel(fn, dim3(a.grid), dim3(kThreads), args, kDynSmem, stream);
