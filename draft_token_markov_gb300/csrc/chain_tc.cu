@@ -56,7 +56,6 @@ constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
 constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
 constexpr uint32_t kSmemB = 4 * kBChunkBytes;
 constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
-constexpr int kCList = 64;                // Gumbel survivors computed by the list warps
 
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
@@ -70,8 +69,6 @@ struct Ctl {
     // bound); the Gumbel survivor list and its length.
     unsigned long long cbest[2][kChainRows];
     uint32_t lcta[2][kChainRows];
-    uint32_t ncl[2];
-    uint64_t clist[kCList];          // survivor (id << 32 | row << 16 | logit bits)
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
     uint64_t scan[kThreads / 32];
@@ -121,7 +118,6 @@ __device__ __forceinline__ void clear_position(Ctl &c, int par) {
         c.cbest[par][b] = 0ull;
         c.lcta[par][b] = 0u;
     }
-    c.ncl[par] = 0u;
 }
 
 // This CTA's abort flag (shared memory: cheap enough for hot loops).
@@ -556,7 +552,13 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     }
     if (!gum_any) return;
 
-    // ---- pass 2 (Gumbel rows): the CTA threshold, then the survivors
+    // ---- pass 2 (Gumbel rows), with no CTA barrier: the warp's threshold
+    // (its largest lower bound) goes into the CTA's (shared-memory maximum),
+    // and the CTA's threshold as it stands then (every value in it is a
+    // lower bound on the CTA's best key, and it already holds this warp's)
+    // selects the ids whose upper bound reaches it; their lanes compute
+    // their exact keys.  A group that finishes its tiles early does this
+    // while the other still works on its last tile.
     uint32_t lw = 0u;   // lane j < 4: ordered warp threshold of row rb + j
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
@@ -564,8 +566,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         lw = lane == j ? m : lw;
     }
     if (ok && ntw > 0 && lane < kRowsT && lw != 0u) atomicMax(&c.lcta[par][rb + lane], lw);
-    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
-    uint32_t cand = 0u;   // bit 4 r + j: queued tile r (newest first), row rb + j survives
+    __syncwarp();
     float Lc[kRowsT];
 #pragma unroll
     for (int j = 0; j < kRowsT; ++j) {
@@ -573,7 +574,8 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         // no bound recorded (no valid id): nothing can survive
         Lc[j] = o != 0u ? key_from_ordered(o) : __uint_as_float(0x7f800000u);
     }
-    if (kRegs) {
+    if (kRegs && ok) {
+        uint32_t cand = 0u;   // bit 4 r + j: queued tile r (newest first), row rb + j survives
         const __half2 L01 = __halves2half2(__float2half_rd(Lc[0]), __float2half_rd(Lc[1]));
         const __half2 L23 = __halves2half2(__float2half_rd(Lc[2]), __float2half_rd(Lc[3]));
         auto slot = [&](int r, const __half2 (&uu)[2]) {
@@ -589,35 +591,16 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         slot(1, u1);
         slot(2, u2);
         slot(3, u3);
-    }
-    // append this warp's survivors to the CTA list (a prefix count over the
-    // lanes, one shared-memory atomic per warp); survivors beyond the list
-    // get their key from their own lane at once
-    const uint32_t cnt = __popc(cand);
-    uint32_t pre = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, pre, o);
-        if (lane >= o) pre += y;
-    }
-    const uint32_t total = __shfl_sync(0xffffffffu, pre, 31);
-    uint32_t at = 0u;
-    if (lane == 31 && total != 0u) at = atomicAdd(&c.ncl[par], total);
-    at = __shfl_sync(0xffffffffu, at, 31) + pre - cnt;
-    while (cand != 0u) {
-        const int bit = __ffs(cand) - 1;
-        cand &= cand - 1u;
-        const int r = bit >> 2, j = bit & 3;
-        const int k = wg + 2 * (ntw - 1 - r);
-        const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
-        const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
-                                    : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
-        const uint32_t l16 = (pr >> (16 * (j & 1))) & 0xffffu;
-        if (at < (uint32_t)kCList)
-            c.clist[at] = ((uint64_t)v << 32) | ((uint64_t)(rb + j) << 16) | l16;
-        else
-            survivor_key(c, i, v, rb + j, l16);
-        ++at;
+        while (cand != 0u) {
+            const int bit = __ffs(cand) - 1;
+            cand &= cand - 1u;
+            const int r = bit >> 2, j = bit & 3;
+            const int k = wg + 2 * (ntw - 1 - r);
+            const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
+            const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
+                                        : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
+            survivor_key(c, i, v, rb + j, (pr >> (16 * (j & 1))) & 0xffffu);
+        }
     }
     if (!kRegs && ok) {
         // more tiles than registers hold (small ranks): the cached logits and
@@ -636,14 +619,6 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                     survivor_key(c, i, (uint32_t)v, rb + j, l16);
             }
         }
-    }
-    asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
-    // the list's exact keys: entry e by lane e % 32 of epilogue warp e / 32
-    const uint32_t n = *(volatile uint32_t *)&c.ncl[par];
-    const uint32_t e = (uint32_t)ew * 32u + (uint32_t)lane;
-    if (e < n && e < (uint32_t)kCList) {
-        const uint64_t en = c.clist[e];
-        survivor_key(c, i, (uint32_t)(en >> 32), (int)((en >> 16) & 7u), (uint32_t)(en & 0xffffu));
     }
 }
 
