@@ -18,20 +18,28 @@
 // shared memory (bandwidth), and all MMA paths share one tensor pipe, so TMEM
 // holds as much of the head as fits.
 //
-// Warp roles (16 warps):
-//   0, 1   lane 0 issues the MMAs of the even / odd tiles into accumulator
-//          0 / 1 (one issuing thread per accumulator)
-//   2      lane 0: TMA producer of the head chunks (position 0 only)
+// Warp roles (20 warps, 640 threads):
+//   0, 1   the MMAs of the even / odd tiles into accumulator 0 / 1 (one
+//          elected lane each, one shared copy of the issue loop)
+//   2      lane 0: TMA producer of the head chunks (position 0 only); later
+//          positions: the next position's base logits into L2, and during
+//          each exchange this CTA's candidate embedding rows into L2
 //   3      lane 0: copies the TMEM-resident chunks from their shared-memory
-//          staging slot into TMEM (position 0 only)
-//   4-7    epilogue of accumulator 0; 8-11 epilogue of accumulator 1
-//   4-15   at position 0, before the epilogue: Gumbel noise of this CTA's ids
-//          for every position (ALU work hidden behind the head's HBM load)
-//   0-7    after each position: warp b exchanges row b's key with every CTA
-//          and stages markov_embed[token] as the next position's B operand
-// Cross-CTA exchange: each CTA stores its per-row best key, tagged with the
-// call's position epoch, in its own slot of a per-position array; every CTA
-// polls all slots until every tag is current (bounded) and takes the maximum.
+//          staging slot into TMEM (position 0 only); later: base prefetch
+//   4-19   the epilogue (warps 4-11 accumulator 0, 12-19 accumulator 1); at
+//          position 0, before it, the noise bounds of position 0 while the
+//          head streams in; after every position, the next position's
+//          noise bounds while the winners are exchanged
+//   0-3    after each position: warp 0 exchanges every row's key with the
+//          other CTAs, and warps 0-3 stage markov_embed[token] of rows w and
+//          w + 4 as the next position's B operand
+// Cross-CTA exchange (Gumbel and greedy rows): each CTA folds its per-row
+// best key into one word per (position, row) with red.max and then adds 1
+// to the position's counter (release); one thread per CTA polls the
+// counter (acquire, bounded) until all CTAs have counted and reads the
+// winners.  Inverse-CDF rows keep per-CTA slots tagged with the position
+// epoch (maximum, then sums and the owner's scan).
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -228,10 +236,10 @@ __device__ __forceinline__ float gumbel_upper(uint64_t h) {
 // id, written by a group of NT threads (thread te takes ids v_begin + te +
 // NT j, two at a time so that their hash and log chains overlap).  The
 // noise depends on seeds and positions only, so it is drawn off the chain's
-// critical path: positions 0 and 1 by the epilogue warps while the head
-// streams in, position p + 1 by warps 2 and 3 (idle after the head load)
-// during position p.  The row loop stays rolled: the kernel's code must fit
-// the instruction caches.
+// critical path: position 0 by the epilogue warps while the head streams
+// in, position p + 1 by the same warps while position p's winners are
+// exchanged.  The row loop stays rolled: the kernel's code must fit the
+// instruction caches.
 template <int NT>
 __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, int p,
                                              uint32_t gum_m, int v_begin, int v_end, int te) {
@@ -398,15 +406,14 @@ __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
 // id; for Gumbel rows a lower and an upper bound on every id's key (logit
 // / T plus the ends of the id's noise byte), keeping the largest lower
 // bound and, per queued tile, the upper bounds as FP16 rounded up.  Pass 2,
-// after the last tile (so that no exact key delays the next tile's
-// accumulator hand-back): the CTA's threshold L, the largest lower bound
-// over all its warps, is a lower bound on the CTA's best key, so only ids
-// whose upper bound reaches L can be that best.  They go to one list whose
-// exact keys two warps compute; the CTA's maximum (and the token) is exactly
-// that of keys computed for every id.  Leaves the CTA's per-row best packed
-// key in c.cbest[i & 1] (zeroed, with c.lcta and c.ncl, before the position).
-// `gum_any` (some row is a Gumbel row) is CTA-uniform: it decides whether the
-// epilogue warps meet at the two pass-2 barriers.
+// after the warp's last tile (so that no exact key delays an accumulator's
+// hand-back): every value of the CTA's threshold (the largest lower bound
+// contributed so far) is a lower bound on the CTA's best key, so only ids
+// whose upper bound reaches it can be that best; their lanes compute their
+// exact keys.  The CTA's maximum (and the token) is exactly that of keys
+// computed for every id.  Leaves the CTA's per-row best packed key in
+// c.cbest[i & 1] (zeroed, with c.lcta, before the position).  `gum_any`
+// (some row is a Gumbel row) is CTA-uniform.
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
                                          const int i, const int t0, const int nt, const bool gum_any,
