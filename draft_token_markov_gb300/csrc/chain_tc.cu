@@ -71,10 +71,13 @@ struct Ctl {
     uint64_t dfull[2];               // accumulator b holds a finished tile
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
+    uint64_t bstaged;                // the next position's B operand is staged
+    uint64_t sdone;                  // the shared-memory tile's bias is in sbias
     // Per position parity (a position's values are read while the next
     // one's are written): per row, the CTA's best packed key and, for Gumbel
     // rows, the CTA's threshold (ordered key of the largest key lower
     // bound); the Gumbel survivor list and its length.
+    float sbias[128][kChainRows];    // the last tile's bias sums (mma.sync path)
     unsigned long long cbest[2][kChainRows];
     uint32_t lcta[2][kChainRows];
     uint64_t win[kChainRows];
@@ -372,6 +375,52 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
     __syncwarp();
 }
 
+// The bias sums of tile `kt` (its 4 K chunks in shared memory, 128-byte
+// swizzled K-major as the TMA wrote them) for ids 16 m .. 16 m + 15 and the
+// 8 rows, by one warp: 16 mma.sync m16n8k16 (BF16 in, fp32 sums) with
+// fragments from ldmatrix, into c.sbias.  The sums' order differs from the
+// tcgen05 tiles' only in the last bit of a few fp32 sums.
+template <int RANK>
+__device__ __forceinline__ void simt_tile(Ctl &c, int kt, int ntm, int m, uint32_t b_sa,
+                                          uint32_t head_sa) {
+    constexpr int cpt = RANK / 64;
+    const int lane = threadIdx.x & 31;
+    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;
+    const int mi = lane >> 3;                       // ldmatrix.x4: matrix of this lane's address
+    const int ra = 16 * m + (mi & 1) * 8 + (lane & 7);   // A row (id within the tile)
+    const int nb = lane & 7, hb = (lane >> 3) & 1;       // ldmatrix.x2: B row, K half
+#pragma unroll 1
+    for (int kc = 0; kc < cpt; ++kc) {
+        int slot;
+        uint32_t ph;
+        chunk_slot(kt * cpt + kc, ntm, slot, ph);
+        const uint32_t sa = head_sa + (uint32_t)slot * kChunkBytes + (uint32_t)ra * 128u;
+        const uint32_t sb = b_sa + (uint32_t)kc * kBChunkBytes + (uint32_t)nb * 128u;
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+            const uint32_t ua = (uint32_t)(2 * sub + (mi >> 1)) ^ (uint32_t)(ra & 7);
+            const uint32_t ub = (uint32_t)(2 * sub + hb) ^ (uint32_t)nb;
+            uint32_t a0, a1, a2, a3, b0, b1;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(sa + (ua << 4)));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                         : "=r"(b0), "=r"(b1)
+                         : "r"(sb + (ub << 4)));
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    }
+    const int id = 16 * m + (lane >> 2), col = (lane & 3) * 2;
+    c.sbias[id][col] = d0;
+    c.sbias[id][col + 1] = d1;
+    c.sbias[id + 8][col] = d2;
+    c.sbias[id + 8][col + 1] = d3;
+}
+
 // The exact key of Gumbel survivor (id v, row b, cached logit l16) folded
 // into the CTA's best key of that row (shared-memory atomic maximum).
 __device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, uint32_t l16) {
@@ -416,8 +465,9 @@ __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
 // (some row is a Gumbel row) is CTA-uniform.
 template <int RANK, bool kCdf>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
-                                         const int i, const int t0, const int nt, const bool gum_any,
-                                         const uint64_t timeout, uint32_t &dcount) {
+                                         const int i, const int t0, const int nt, const int nts,
+                                         const int ntm, const uint32_t b_sa, const uint32_t head_sa,
+                                         const bool gum_any, const uint64_t timeout, uint32_t &dcount) {
     constexpr int cpt = RANK / 64;
     constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
     constexpr bool kRegs = kTilesWG <= 4;                  // pass-2 tiles kept in registers
@@ -466,6 +516,22 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     };
     load_tile(wg, nb, nq);
     bool ok = true;
+    if (nts >= 0 && wg == 1) {
+        // group 1, before its first tile: the bias of tile nts, 16 ids per
+        // warp, with mma.sync (m16n8k16, fp32 sums) from the tile's shared-
+        // memory A chunks and the staged B rows, into sbias
+        bool st = true;
+        if (lane == 0)
+            st = tc::mbar_wait(tc::smem_u32(&c.bstaged), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (!st) {
+            if (lane == 0) fail(c, a, 4u, 0xC000u + i);
+        } else {
+            simt_tile<RANK>(c, nts, ntm, ew - 8, b_sa, head_sa);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.sdone));
+    }
     int ntw = 0;   // tiles this warp processed
 #pragma unroll 1
     for (int k = wg; k < nt; k += 2) {
@@ -478,21 +544,42 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             ok = false;
             break;
         }
-        if (lane == 0)
-            ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-            if (lane == 0) fail(c, a, 4u, 0x6000u + i);
-            break;
-        }
-        ++dcount;
-        tc::fence_after_sync();
         uint32_t r[4];
-        tc::ld_32x32b_x4(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg + (uint32_t)rb, r);
-        tc::wait_ld();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
+        if (k == nts) {
+            // the mma.sync tile (group 0's last): its bias from sbias
+            if (lane == 0)
+                ok = tc::mbar_wait(tc::smem_u32(&c.sdone), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(c, a, 4u, 0xD000u + i);
+                break;
+            }
+            const float4 sb = *reinterpret_cast<const float4 *>(&c.sbias[q * 32 + lane][rb]);
+            r[0] = __float_as_uint(sb.x);
+            r[1] = __float_as_uint(sb.y);
+            r[2] = __float_as_uint(sb.z);
+            r[3] = __float_as_uint(sb.w);
+        } else {
+            if (lane == 0)
+                ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(c, a, 4u, 0x6000u + i);
+                break;
+            }
+            ++dcount;
+            tc::fence_after_sync();
+            tc::ld_32x32b_x4(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg + (uint32_t)rb, r);
+            tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
+        }
+        // nothing that waits on this tile's base loads may be scheduled
+        // before the accumulator is handed back
+#pragma unroll
+        for (int j = 0; j < kRowsT; ++j) asm volatile("" : "+r"(cb[j]));
+        asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
         const int v = (t0 + k) * 128 + q * 32 + lane;
         const bool valid = v < V;
         // bias = bf16(sum); logit = bf16(f32(base) + f32(bias)), two rows a time
@@ -669,6 +756,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             tc::mbar_init(tc::smem_u32(&c.dfree[b]), kEpiWarps / 2);
             tc::mbar_init(tc::smem_u32(&c.fin[b]), 1);
         }
+        tc::mbar_init(tc::smem_u32(&c.bstaged), 1);
+        tc::mbar_init(tc::smem_u32(&c.sdone), kEpiWarps / 2);
         tc::mbar_init_fence();
         c.tmem_ready = 0u;
         clear_position(c, 0);
@@ -729,9 +818,14 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
 
     bool stop = __syncthreads_or(c.abort != 0u);
     for (int i = 0; i < N && !stop; ++i) {
+        // A CTA with the full 7 tiles of rank 256 takes its last tile's bias
+        // through mma.sync in the epilogue warps after position 0: the
+        // tcgen05 tiles then pair up in 3 rounds of the two accumulators
+        // instead of 4.  (Its A chunks are in shared memory.)
+        const int nts = (MODE == 0 && RANK == 256 && nt == kMaxChunks / cpt && i > 0) ? nt - 1 : -1;
         // ------------------------------------- phase A: MMA and epilogue
         if (warp < 2) {
-            issue_tiles<RANK>(c, a, tmem, warp, i, nt, ntm, b_sa, head_sa, timeout, uses);
+            issue_tiles<RANK>(c, a, tmem, warp, i, nts >= 0 ? nts : nt, ntm, b_sa, head_sa, timeout, uses);
         } else if (warp < 4 && i > 0) {
             // warps 2 and 3 after the head load: the next position's base
             // logits into L2, off the chain's critical path
@@ -819,9 +913,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
             if (MODE == 1)
-                epilogue<RANK, true>(c, a, tmem, i, t0, nt, false, timeout, dcount);
+                epilogue<RANK, true>(c, a, tmem, i, t0, nt, -1, ntm, b_sa, head_sa, false, timeout, dcount);
             else
-                epilogue<RANK, false>(c, a, tmem, i, t0, nt, gum_any, timeout, dcount);
+                epilogue<RANK, false>(c, a, tmem, i, t0, nt, nts, ntm, b_sa, head_sa, gum_any, timeout, dcount);
         }
         stop = __syncthreads_or(stop_vote(c, a, MODE != 0));
         if (stop) break;
@@ -931,6 +1025,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 tc::fence_before_sync();
                 asm volatile("bar.sync 4, 128;" ::: "memory");
                 tc::fence_after_sync();
+                // the epilogue warps' mma.sync tile reads the staged rows too
+                if (tid == 0 && i + 1 < N) tc::mbar_arrive(tc::smem_u32(&c.bstaged));
             } else if (i + 1 < N) {
                 // the epilogue warps clear the next position's CTA maxima (their
                 // last reader finished before this position's phase-A barrier),
