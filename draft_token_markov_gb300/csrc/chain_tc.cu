@@ -935,18 +935,17 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (warp == 0 || warp == 2) {
                 if (warp == 0) {
                     // lane b < 8: row b's best key in this CTA
-                    const uint64_t m = lane < kChainRows ? (uint64_t)c.cbest[i & 1][lane] : 0ull;
-                    uint64_t m8[kChainRows];
-#pragma unroll
-                    for (int b = 0; b < kChainRows; ++b) m8[b] = __shfl_sync(0xffffffffu, m, b);
                     const size_t par = (size_t)(c.call & 1u);
                     uint64_t *wm = a.win_max + ((par * kMaxSteps + i) * kChainRows) * kLineU64;
                     uint32_t *wc = a.win_cnt + (par * kMaxSteps + i) * kLineU32;
+                    // lane b < 8 folds row b's best key in (one instruction for
+                    // all rows); the warp barrier orders the reds before lane
+                    // 0's release
+                    if (lane < kChainRows && c.live[lane])
+                        tc::red_max_u64(wm + lane * kLineU64, (uint64_t)c.cbest[i & 1][lane]);
+                    __syncwarp();
                     if (lane == 0) {
                         bool ok = true;
-#pragma unroll
-                        for (int b = 0; b < kChainRows; ++b)
-                            if (c.live[b]) tc::red_max_u64(wm + b * kLineU64, m8[b]);
                         tc::red_release_add_u32(wc, 1u);
                         const uint64_t dl = tc::now_ns() + timeout;
                         for (uint32_t spin = 0;; ++spin) {
