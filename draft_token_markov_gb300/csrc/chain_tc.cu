@@ -611,11 +611,11 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 const float kl = __fadd_rn(__fmaf_rn(fabsf(xa), -1e-5f, xa), dequantize_lower(qb));
                 lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
                 ku[j] = __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
-            } else {
+            } else if ((live_m >> j) & 1u) {
                 float key = lf;
                 if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[rb + j]);
                 const uint32_t o = ordered_key(key);
-                const bool better = valid && ((live_m >> j) & 1u) && o > bo[j];
+                const bool better = valid && o > bo[j];
                 bo[j] = better ? o : bo[j];
                 bv[j] = better ? (uint32_t)v : bv[j];
             }
