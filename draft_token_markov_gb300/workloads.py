@@ -88,9 +88,9 @@ def make_weights(w: Workload):
     return head, embed
 
 
-def make_call(w: Workload, call: int = 0):
+def make_call(w: Workload, call: int = 0, base_f32: bool = False):
     """The per-call inputs of call number ``call``: base logits [rows, N, V]
-    BF16, anchor tokens int32, temperature fp32, seeds int64 and
+    BF16 (fp32 with ``base_f32``), anchor tokens int32, temperature fp32, seeds int64 and
     row_state_idx int64 (-1 on padding rows), all on the CPU.
 
     Call 0 of every workload draws the base logits; later calls of the same
@@ -108,7 +108,8 @@ def make_call(w: Workload, call: int = 0):
                 base32[b, i, _distinct_ids(3, V, g)] = 64.0
             if b == w.nan_row:
                 base32[b, i, _distinct_ids(4, V, g)] = float("nan")
-    base = base32.to(torch.bfloat16)
+    # an fp32 base keeps the drawn values (not rounded to BF16)
+    base = base32.contiguous() if base_f32 else base32.to(torch.bfloat16)
     gc = torch.Generator("cpu").manual_seed(w.gen_seed * 1_000_003 + call)
     anchor = torch.randint(0, V, (R,), generator=gc, dtype=torch.int64).to(torch.int32)
     temps = torch.tensor(w.temperatures, dtype=torch.float32)

@@ -95,6 +95,14 @@ def _declare(L: ctypes.CDLL) -> None:
                                 P, P, P, P, P, P, c.c_int, c.c_int, c.c_float, c.c_int,
                                 c.c_float, P, c.c_int64, P, c.c_int64, c.c_int64, P, P,
                                 c.c_int]),
+        "orc_logit_typed": (c.c_float, [c.c_float, c.c_uint16, c.c_int, c.c_int, c.c_float,
+                                        c.c_int, c.c_float, c.c_float]),
+        "orc_select_f": (c.c_int64, [P, c.c_int, c.c_float, c.c_int, c.c_uint64, c.c_uint32,
+                                     c.c_uint32, P, P]),
+        "orc_chain_typed": (c.c_int, [c.c_int, c.c_int, c.c_int, c.c_int, P, c.c_int,
+                                      c.c_int64, c.c_int64, P, P, P, P, P, P, c.c_int, c.c_int,
+                                      c.c_float, c.c_int, c.c_float, P, c.c_int64, P, c.c_int,
+                                      c.c_int64, c.c_int64, P, P, c.c_int]),
         "orc_bf16_rne_n": (None, [P, P, c.c_int64]),
         "orc_log_n": (None, [P, P, c.c_int64]),
         "orc_exp_n": (None, [P, P, c.c_int64]),
@@ -270,6 +278,73 @@ def chain(base_bits: np.ndarray, head_bits: np.ndarray, embed_bits: np.ndarray,
                          _ptr(tokens), N, _ptr(cache), N * V, V,
                          _ptr(ss) if ss is not None else None,
                          _ptr(sp) if sp is not None else None, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle chain: anchor or previous token out of range")
+    return tokens, cache
+
+
+# ------------------------------------------------ fp32 base / cache variants
+
+def logit_typed(base: float, bias_bits: int, cache_f32: bool, mult: float = 1.0,
+                cap: float | None = None) -> float:
+    """The cached logit as an fp32 value for a BF16 (cache_f32 False) or fp32
+    cache; base is the base logit's fp32 value."""
+    has_t, m, has_cap, c, inv = transform_params(mult, cap)
+    return lib().orc_logit_typed(float(np.float32(base)), int(bias_bits), int(bool(cache_f32)),
+                                 has_t, m, has_cap, c, inv)
+
+
+def select_f(l: np.ndarray, T: float, mode: int, seed: int, row: int, step: int):
+    """select() on fp32 logit values."""
+    l = np.ascontiguousarray(l, dtype=np.float32)
+    k1 = ctypes.c_float()
+    k2 = ctypes.c_float()
+    tok = lib().orc_select_f(_ptr(l), l.size, float(np.float32(T)), int(mode), _u64(seed), row,
+                             step, ctypes.addressof(k1), ctypes.addressof(k2))
+    return int(tok), k1.value, k2.value
+
+
+def chain_typed(base: np.ndarray, head_bits: np.ndarray, embed_bits: np.ndarray,
+                anchor: np.ndarray, temperature: np.ndarray, seeds: np.ndarray,
+                row_state_idx: np.ndarray, mode: int, mult: float = 1.0,
+                cap: float | None = None, cache_f32: bool = False,
+                tokens: np.ndarray | None = None, cache: np.ndarray | None = None,
+                start_step: np.ndarray | None = None, start_prev: np.ndarray | None = None,
+                nthreads: int = 0):
+    """chain() with the base logits as BF16 bits (uint16) or fp32 values
+    (float32) and a BF16 (uint16 bits) or fp32 cache.  Returns (tokens,
+    cache); padding rows keep the passed-in values (defaults -1 and
+    0xFFFF / NaN)."""
+    rows, N, V = base.shape
+    Vh, r = head_bits.shape
+    assert Vh >= V and embed_bits.shape[1] == r
+    base_f32 = base.dtype == np.float32
+    base = np.ascontiguousarray(base, dtype=np.float32 if base_f32 else np.uint16)
+    head_bits = np.ascontiguousarray(head_bits, dtype=np.uint16)
+    embed_bits = np.ascontiguousarray(embed_bits, dtype=np.uint16)
+    anchor = np.ascontiguousarray(anchor, dtype=np.int32)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32)
+    seeds = np.ascontiguousarray(seeds, dtype=np.int64)
+    row_state_idx = np.ascontiguousarray(row_state_idx, dtype=np.int64)
+    if tokens is None:
+        tokens = np.full((rows, N), -1, dtype=np.int64)
+    if cache is None:
+        cache = (np.full((rows, N, V), np.nan, dtype=np.float32) if cache_f32
+                 else np.full((rows, N, V), 0xFFFF, dtype=np.uint16))
+    assert tokens.dtype == np.int64 and tokens.flags["C_CONTIGUOUS"]
+    assert cache.dtype == (np.float32 if cache_f32 else np.uint16) and cache.flags["C_CONTIGUOUS"]
+    ss = sp = None
+    if start_step is not None:
+        ss = np.ascontiguousarray(start_step, dtype=np.int32)
+        sp = np.ascontiguousarray(start_prev, dtype=np.int64)
+    has_t, m, has_cap, c, _ = transform_params(mult, cap)
+    rc = lib().orc_chain_typed(V, r, N, rows, _ptr(base), int(base_f32), N * V, V,
+                               _ptr(head_bits), _ptr(embed_bits), _ptr(anchor),
+                               _ptr(temperature), _ptr(seeds), _ptr(row_state_idx), int(mode),
+                               has_t, m, has_cap, c, _ptr(tokens), N, _ptr(cache),
+                               int(bool(cache_f32)), N * V, V,
+                               _ptr(ss) if ss is not None else None,
+                               _ptr(sp) if sp is not None else None, int(nthreads))
     if rc != 0:
         raise ValueError("oracle chain: anchor or previous token out of range")
     return tokens, cache

@@ -43,6 +43,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -233,6 +234,27 @@ uint16_t orc_logit(uint16_t base, uint16_t bias, int has_transform, float mult,
     return orc_bf16_rne(y);
 }
 
+/* The cached logit for either cache dtype, as an fp32 value.  The sharded
+ * page's chain takes BF16 or fp32 base logits and caches ([sharded]
+ * DSparkShardedMarkovSampler set-up, _kernel: base and cache dtypes) and
+ * rounds to the cache's dtype ("cache_round" in the module docstring):
+ *   s = f32(base) + f32(bias)            fp32 sum
+ *   BF16 cache: s = bf16(s), then the transform and bf16 as orc_logit;
+ *   fp32 cache: no BF16 rounding; the transform (a reading: the same fp32
+ *               steps, as the pages give the transform only for BF16
+ *               caches) and l = its fp32 result.
+ * With a BF16 base and a BF16 cache this is orc_logit's value. */
+float orc_logit_typed(float base, uint16_t bias, int cache_f32, int has_transform, float mult,
+                      int has_cap, float cap, float inv_cap)
+{
+    float s = base + orc_bf16_to_f32(bias);
+    if (!cache_f32) s = orc_bf16_to_f32(orc_bf16_rne(s));
+    if (!has_transform) return s;
+    float y = s * mult;
+    if (has_cap) y = cap * orc_tanh(y * inv_cap);
+    return cache_f32 ? y : orc_bf16_to_f32(orc_bf16_rne(y));
+}
+
 /* Gumbel key of one cached logit: fp32(l / T) + gumbel (T > 0). */
 float orc_gumbel_key(uint16_t l, float T, uint64_t seed, uint32_t row, uint32_t step,
                      uint32_t v)
@@ -246,15 +268,16 @@ static int greedy_temperature(float T) { return !(T > 0.0f); }
 
 /* The key of id v at one position: l at T = 0 (greedy), fp32(l / T) in
  * inverse-CDF mode, fp32(l / T) + gumbel in Gumbel mode. */
-static float position_key(const uint16_t *l, int v, float T, int mode, uint64_t seed,
+static float position_key(const float *l, int v, float T, int mode, uint64_t seed,
                           uint32_t row, uint32_t step)
 {
-    if (greedy_temperature(T)) return orc_bf16_to_f32(l[v]);
-    if (mode == ORC_INVCDF) return orc_bf16_to_f32(l[v]) / T;
-    return orc_gumbel_key(l[v], T, seed, row, step, (uint32_t)v);
+    if (greedy_temperature(T)) return l[v];
+    if (mode == ORC_INVCDF) return l[v] / T;
+    return l[v] / T + orc_gumbel(seed, row, step, (uint32_t)v);
 }
 
-/* Select the token of one position from its cached logits l[0..V-1].
+/* Select the token of one position from its cached logits l[0..V-1] (fp32
+ * values; a BF16 cache's values are exact in fp32).
  *   NaN rule: the lowest id whose key (the noised logit) is NaN ([muse]
  *   docstring); applied in every mode, a reading.
  *   T = 0: the lowest id of max l (the torch.argmax order).
@@ -265,8 +288,8 @@ static float position_key(const uint16_t *l, int v, float T, int mode, uint64_t 
  *   token is the smallest j whose prefix sum exceeds mulhi64(H, S).
  * Returns the token; *k1 / *k2 receive the winning and runner-up keys (NaN
  * when the NaN rule decided). */
-int64_t orc_select(const uint16_t *l, int V, float T, int mode, uint64_t seed,
-                   uint32_t row, uint32_t step, float *k1, float *k2)
+int64_t orc_select_f(const float *l, int V, float T, int mode, uint64_t seed, uint32_t row,
+                     uint32_t step, float *k1, float *k2)
 {
     float best = -INFINITY, second = -INFINITY;
     int64_t arg = -1;
@@ -294,31 +317,91 @@ int64_t orc_select(const uint16_t *l, int V, float T, int mode, uint64_t seed,
     if (M == -INFINITY) return 0;              /* every weight is zero */
     uint64_t S = 0;
     for (int v = 0; v < V; ++v) {
-        float w = orc_exp(orc_bf16_to_f32(l[v]) / T - M);
+        float w = orc_exp(l[v] / T - M);
         S += (uint64_t)(w * 0x1p40f);          /* exact scale, then truncation */
     }
     uint64_t H = orc_cdf_hash(seed, row, step);
     uint64_t t = (uint64_t)(((unsigned __int128)H * (unsigned __int128)S) >> 64);
     uint64_t prefix = 0;
     for (int v = 0; v < V; ++v) {
-        float w = orc_exp(orc_bf16_to_f32(l[v]) / T - M);
+        float w = orc_exp(l[v] / T - M);
         prefix += (uint64_t)(w * 0x1p40f);
         if (prefix > t) return v;
     }
     return V - 1;                              /* unreachable: prefix(V-1) = S > t */
 }
 
+/* orc_select_f on a BF16 cache row (raw bits). */
+int64_t orc_select(const uint16_t *l, int V, float T, int mode, uint64_t seed,
+                   uint32_t row, uint32_t step, float *k1, float *k2)
+{
+    float *lf = (float *)malloc((size_t)(V > 0 ? V : 1) * sizeof(float));
+    if (!lf) return -1;
+    for (int v = 0; v < V; ++v) lf[v] = orc_bf16_to_f32(l[v]);
+    int64_t tok = orc_select_f(lf, V, T, mode, seed, row, step, k1, k2);
+    free(lf);
+    return tok;
+}
+
 /* -------------------------------------------------------------- the chain */
 
-/* Run the chain for `rows` request rows.  Arrays hold BF16 as raw uint16
- * bits.  base[b, i, v] is at base[b*base_s0 + i*base_s1 + v]; the cache
- * likewise with cache_s0 / cache_s1; tokens at tokens[b*tok_s0 + i].
- * start_step / start_prev (both NULL, or both [rows]) restart row b at
- * position start_step[b] with previous token start_prev[b], leaving
- * earlier positions untouched: the acceptance check uses this to continue a
- * row from a token the GPU drew.  has_cap == 0 means no soft cap;
- * has_transform == 0 means l = s.  Returns 0, or -1 on a bad argument
- * (an anchor or previous token out of range). */
+/* Run the chain for `rows` request rows.  base[b, i, v] is at
+ * base[b*base_s0 + i*base_s1 + v], BF16 bits (base_f32 == 0) or fp32; the
+ * cache likewise with cache_s0 / cache_s1 and cache_f32; head and embed are
+ * BF16 bits; tokens at tokens[b*tok_s0 + i].  start_step / start_prev (both
+ * NULL, or both [rows]) restart row b at position start_step[b] with
+ * previous token start_prev[b], leaving earlier positions untouched: the
+ * acceptance check uses this to continue a row from a token the GPU drew.
+ * has_cap == 0 means no soft cap; has_transform == 0 means l = s.  Returns
+ * 0, or -1 on a bad argument (an anchor or previous token out of range). */
+int orc_chain_typed(int V, int r, int N, int rows, const void *base, int base_f32,
+                    int64_t base_s0, int64_t base_s1, const uint16_t *head, const uint16_t *embed,
+                    const int32_t *anchor, const float *temperature, const int64_t *seeds,
+                    const int64_t *row_state_idx, int mode, int has_transform, float mult,
+                    int has_cap, float cap, int64_t *tokens, int64_t tok_s0, void *cache,
+                    int cache_f32, int64_t cache_s0, int64_t cache_s1, const int32_t *start_step,
+                    const int64_t *start_prev, int nthreads)
+{
+    float inv_cap = has_cap ? 1.0f / cap : 1.0f;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    float *lrow = (float *)malloc((size_t)(V > 0 ? V : 1) * sizeof(float));
+    if (!lrow) return -1;
+    for (int b = 0; b < rows; ++b) {
+        if (row_state_idx[b] < 0) continue;           /* padding rows are inert */
+        int i0 = start_step ? start_step[b] : 0;
+        int64_t p = start_prev ? start_prev[b] : (int64_t)anchor[b];
+        if (p < 0 || p >= V) { free(lrow); return -1; }
+        for (int i = i0; i < N; ++i) {
+            const uint16_t *e = embed + (size_t)p * (size_t)r;
+            const int64_t bo = b * base_s0 + i * base_s1, co = b * cache_s0 + i * cache_s1;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+            for (int v = 0; v < V; ++v) {
+                uint16_t bv = orc_bias(head + (size_t)v * (size_t)r, e, r);
+                float bf = base_f32 ? ((const float *)base)[bo + v]
+                                    : orc_bf16_to_f32(((const uint16_t *)base)[bo + v]);
+                float l = orc_logit_typed(bf, bv, cache_f32, has_transform, mult, has_cap, cap,
+                                          inv_cap);
+                lrow[v] = l;
+                if (cache_f32) ((float *)cache)[co + v] = l;
+                else ((uint16_t *)cache)[co + v] = orc_bf16_rne(l);
+            }
+            int64_t tok = orc_select_f(lrow, V, temperature[b], mode, (uint64_t)seeds[b],
+                                       (uint32_t)b, (uint32_t)i, NULL, NULL);
+            tokens[b * tok_s0 + i] = tok;
+            p = tok;
+        }
+    }
+    free(lrow);
+    return 0;
+}
+
+/* orc_chain_typed with a BF16 base and a BF16 cache (raw bits). */
 int orc_chain(int V, int r, int N, int rows, const uint16_t *base, int64_t base_s0,
               int64_t base_s1, const uint16_t *head, const uint16_t *embed,
               const int32_t *anchor, const float *temperature, const int64_t *seeds,
@@ -327,35 +410,10 @@ int orc_chain(int V, int r, int N, int rows, const uint16_t *base, int64_t base_
               int64_t cache_s0, int64_t cache_s1, const int32_t *start_step,
               const int64_t *start_prev, int nthreads)
 {
-    float inv_cap = has_cap ? 1.0f / cap : 1.0f;
-#ifdef _OPENMP
-    if (nthreads > 0) omp_set_num_threads(nthreads);
-#else
-    (void)nthreads;
-#endif
-    for (int b = 0; b < rows; ++b) {
-        if (row_state_idx[b] < 0) continue;           /* padding rows are inert */
-        int i0 = start_step ? start_step[b] : 0;
-        int64_t p = start_prev ? start_prev[b] : (int64_t)anchor[b];
-        if (p < 0 || p >= V) return -1;
-        for (int i = i0; i < N; ++i) {
-            const uint16_t *e = embed + (size_t)p * (size_t)r;
-            const uint16_t *bi = base + b * base_s0 + i * base_s1;
-            uint16_t *ci = cache + b * cache_s0 + i * cache_s1;
-#ifdef _OPENMP
-#pragma omp parallel for schedule(static)
-#endif
-            for (int v = 0; v < V; ++v) {
-                uint16_t bv = orc_bias(head + (size_t)v * (size_t)r, e, r);
-                ci[v] = orc_logit(bi[v], bv, has_transform, mult, has_cap, cap, inv_cap);
-            }
-            int64_t tok = orc_select(ci, V, temperature[b], mode, (uint64_t)seeds[b],
-                                     (uint32_t)b, (uint32_t)i, NULL, NULL);
-            tokens[b * tok_s0 + i] = tok;
-            p = tok;
-        }
-    }
-    return 0;
+    return orc_chain_typed(V, r, N, rows, base, 0, base_s0, base_s1, head, embed, anchor,
+                           temperature, seeds, row_state_idx, mode, has_transform, mult, has_cap,
+                           cap, tokens, tok_s0, cache, 0, cache_s0, cache_s1, start_step,
+                           start_prev, nthreads);
 }
 
 /* ------------------------------------------------------- array helpers */
