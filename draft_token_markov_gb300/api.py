@@ -74,6 +74,8 @@ def _declare(L):
         "markov_noise_join": (i32, [P, P]),
         "markov_chain_sample": (i32, [P, P, i64, i64, P, P, P, P, P, P, i32, i32, f32, f32,
                                       P, i64, P, i64, i64, P]),
+        "markov_chain_sample_typed": (i32, [P, P, i32, i64, i64, P, P, P, P, P, P, i32, i32, f32,
+                                            f32, P, i64, P, i32, i64, i64, P]),
         "markov_plan_status": (i32, [P]),
         "markov_status_string": (c.c_char_p, [i32]),
         "markov_gumbel_noise": (i32, [P, P, P, i32, i32, i32, P, i64, P]),
@@ -105,6 +107,10 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+MARKOV_BF16 = 0
+MARKOV_F32 = 1
 
 
 class Plan:
@@ -165,13 +171,18 @@ def markov_chain_sample(plan: Plan, base_logits, head, embed, anchor_tokens, tem
                         stream=None):
     """Sample the draft tokens; returns (draft_tokens, logit_cache).  Output
     tensors are allocated when not given (padding rows are then left
-    uninitialised, as the library never writes them)."""
+    uninitialised, as the library never writes them).  base_logits and
+    logit_cache may each be bfloat16 or float32 (markov_chain_sample_typed;
+    the cache defaults to bfloat16)."""
     rows, N, V = base_logits.shape
     dev = base_logits.device
     if draft_tokens is None:
         draft_tokens = torch.empty((rows, N), dtype=torch.int64, device=dev)
     if logit_cache is None:
         logit_cache = torch.empty((rows, N, V), dtype=torch.bfloat16, device=dev)
+    dtypes = {torch.bfloat16: MARKOV_BF16, torch.float32: MARKOV_F32}
+    if base_logits.dtype not in dtypes or logit_cache.dtype not in dtypes:
+        raise TypeError("base_logits and logit_cache must be bfloat16 or float32")
     if base_logits.stride(2) != 1 or logit_cache.stride(2) != 1 or draft_tokens.stride(1) != 1:
         raise ValueError("the last dimension of base_logits, logit_cache and draft_tokens must "
                          "be contiguous")
@@ -179,15 +190,16 @@ def markov_chain_sample(plan: Plan, base_logits, head, embed, anchor_tokens, tem
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
     cap = -1.0 if soft_cap is None else float(soft_cap)
-    code = lib().markov_chain_sample(
-        plan.handle, _dev(base_logits, torch.bfloat16, "base_logits"), base_logits.stride(0),
-        base_logits.stride(1), _dev(head, torch.bfloat16, "head"),
+    code = lib().markov_chain_sample_typed(
+        plan.handle, _dev(base_logits, base_logits.dtype, "base_logits"),
+        dtypes[base_logits.dtype], base_logits.stride(0), base_logits.stride(1),
+        _dev(head, torch.bfloat16, "head"),
         _dev(embed, torch.bfloat16, "embed"), _dev(anchor_tokens, torch.int32, "anchor_tokens"),
         _dev(temperature, torch.float32, "temperature"), _dev(seeds, torch.int64, "seeds"),
         _dev(row_state_idx, torch.int64, "row_state_idx"), rows, int(mode),
         float(output_multiplier), cap, _dev(draft_tokens, torch.int64, "draft_tokens"),
-        draft_tokens.stride(0), _dev(logit_cache, torch.bfloat16, "logit_cache"),
-        logit_cache.stride(0), logit_cache.stride(1), _stream(stream))
+        draft_tokens.stride(0), _dev(logit_cache, logit_cache.dtype, "logit_cache"),
+        dtypes[logit_cache.dtype], logit_cache.stride(0), logit_cache.stride(1), _stream(stream))
     _check(code, "markov_chain_sample")
     return draft_tokens, logit_cache
 

@@ -109,11 +109,11 @@ batch_logits_kernel(const SampleArgs a, int i) {
                 const int row = row0 + nt * 8 + 2 * t + (e & 1);
                 if (!row_live(a, row)) continue;
                 const int v = v0 + g + ((e & 2) ? 8 : 0);
-                const uint32_t bb = a.base[row * a.base_s0 + (int64_t)i * a.base_s1 + v];
-                const uint32_t l = logit_bits(bb, acc[nt][e], a.tf);
-                a.cache[row * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
+                const float l = logit_value(base_value(a, row, i, v), acc[nt][e], a.tf,
+                                            a.cache_f != nullptr);
+                cache_put(a, row, i, v, l);
                 const float T = a.temperature[row];
-                float key = dm_bf16_f32(l);
+                float key = l;
                 if (samples(T)) {
                     key = __fdiv_rn(key, T);
                     if (a.mode == 0)
@@ -187,10 +187,9 @@ batch_cdfsum_kernel(const SampleArgs a, int i, int nblk) {
     block_range(a.V, nblk, blk, v0, v1);
     if (threadIdx.x == 0) s_sum = 0ull;
     __syncthreads();
-    const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
     uint64_t part = 0ull;
     for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-        float x = __fdiv_rn(dm_bf16_f32(crow[v]), T);
+        float x = __fdiv_rn(cache_value(a, b, i, v), T);
         part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
     }
 #pragma unroll
@@ -241,13 +240,12 @@ batch_pick_kernel(const SampleArgs a, int i, int nblk) {
             const uint64_t target = s_red[0];
             int v0, v1;
             block_range(a.V, nblk, s_blk, v0, v1);
-            const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
             const int len = v1 - v0;
             const int chunk = (len + kBatchThreads - 1) / kBatchThreads;
             const int c0 = v0 + tid * chunk, c1 = min(c0 + chunk, v1);
             uint64_t mine = 0ull;
             for (int v = c0; v < c1; ++v) {
-                float x = __fdiv_rn(dm_bf16_f32(crow[v]), T);
+                float x = __fdiv_rn(cache_value(a, b, i, v), T);
                 mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
             }
             uint64_t incl = mine;
@@ -263,7 +261,7 @@ batch_pick_kernel(const SampleArgs a, int i, int nblk) {
             uint64_t run = s_blkpre + wpre + incl - mine;
             if (run <= target && target < run + mine) {
                 for (int v = c0; v < c1; ++v) {
-                    float x = __fdiv_rn(dm_bf16_f32(crow[v]), T);
+                    float x = __fdiv_rn(cache_value(a, b, i, v), T);
                     run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                     if (run > target) {
                         s_tok = v;

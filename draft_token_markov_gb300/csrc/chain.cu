@@ -160,10 +160,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                 const bool live = (e & 1) ? l1 : l0;
                 if (!live) continue;
                 const int v = v0 + g + ((e & 2) ? 8 : 0);
-                const uint32_t bb = a.base[row * a.base_s0 + (int64_t)i * a.base_s1 + v];
-                const uint32_t l = logit_bits(bb, acc[e], a.tf);
-                a.cache[row * a.cache_s0 + (int64_t)i * a.cache_s1 + v] = (uint16_t)l;
-                const float lf = dm_bf16_f32(l);
+                const float lf = logit_value(base_value(a, row, i, v), acc[e], a.tf, a.cache_f != nullptr);
+                cache_put(a, row, i, v, lf);
                 const bool smp = (e & 1) ? s1 : s0;
                 float key = lf;
                 if (smp) {
@@ -229,10 +227,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                 if (o == 0xffffffffu || M == __uint_as_float(0x7f800000u) ||
                     M == __uint_as_float(0xff800000u))
                     continue;
-                const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
                 uint64_t part = 0ull;
                 for (int v = v_begin + tid; v < v_end; v += kChainThreads) {
-                    float x = __fdiv_rn(dm_bf16_f32(crow[v]), rs.T[b]);
+                    float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
                     float w = dm_exp(__fsub_rn(x, M));
                     part += (uint64_t)__float2ull_rz(__fmul_rn(w, 0x1p40f));
                 }
@@ -279,14 +276,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                 if (P <= target && target < P + Sc) {
                     // this CTA holds the token: each thread takes a contiguous
                     // chunk of the slice, chunk sums are scanned across the CTA
-                    const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
                     const int len = v_end - v_begin;
                     const int chunk = (len + kChainThreads - 1) / kChainThreads;
                     const int c0 = v_begin + tid * chunk;
                     const int c1 = min(c0 + chunk, v_end);
                     uint64_t mine = 0ull;
                     for (int v = c0; v < c1; ++v) {
-                        float x = __fdiv_rn(dm_bf16_f32(crow[v]), rs.T[b]);
+                        float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
                         mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                     }
                     // exclusive scan of `mine` over the CTA, in thread order
@@ -303,7 +299,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                     uint64_t run = P + wpre + incl - mine;
                     if (run <= target && target < run + mine) {
                         for (int v = c0; v < c1; ++v) {
-                            float x = __fdiv_rn(dm_bf16_f32(crow[v]), rs.T[b]);
+                            float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
                             run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                             if (run > target) {
                                 tok_slot[b] = (uint64_t)v;

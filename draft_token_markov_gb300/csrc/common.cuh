@@ -64,20 +64,46 @@ __device__ __forceinline__ uint32_t packed_ordered(uint64_t p) { return (uint32_
 
 // ---------------------------------------------------------- epilogue
 
-// The cached logit (BF16 bits) of one element from its base logit and its
-// fp32 bias sum: bias = bf16(sum); s = bf16(f32(base) + f32(bias)); with a
-// transform l = bf16(cap * tanh((s * mult) * inv_cap)) or bf16(s * mult).
-// (sharded_markov page, "Per call" diagram: cache_round(base + bf16(head .
-// embed)); muse_spark markov page, fused_markov_params: the output-logit
-// transform in the epilogue, multiplier and cap rounded to fp32.)
-__device__ __forceinline__ uint32_t logit_bits(uint32_t base_bits, float bias_sum,
-                                               const Transform &tf) {
-    uint32_t bias = dm_bf16_bits(bias_sum);
-    uint32_t s = dm_bf16_bits(__fadd_rn(dm_bf16_f32(base_bits), dm_bf16_f32(bias)));
+// The cached logit of one element, as an fp32 value, from its base logit
+// and its fp32 bias sum: bias = bf16(sum); s = f32(base) + f32(bias) in
+// fp32, rounded to BF16 for a BF16 cache; with a transform y = s * mult,
+// then cap * tanh(y * inv_cap) when capped, rounded to BF16 for a BF16
+// cache.  (sharded_markov page, "Per call" diagram: cache_round(base +
+// bf16(head . embed)), its chain compiled for BF16 or fp32 base logits and
+// caches; muse_spark markov page, fused_markov_params: the output-logit
+// transform in the epilogue, multiplier and cap rounded to fp32.  For an
+// fp32 cache the transform's fp32 steps are a reading: the pages give the
+// transform for BF16 caches only.)
+__device__ __forceinline__ float logit_value(float base, float bias_sum, const Transform &tf,
+                                             bool cache_f32) {
+    float s = __fadd_rn(base, dm_bf16_f32(dm_bf16_bits(bias_sum)));
+    if (!cache_f32) s = dm_bf16_f32(dm_bf16_bits(s));
     if (!tf.has_transform) return s;
-    float y = __fmul_rn(dm_bf16_f32(s), tf.mult);
+    float y = __fmul_rn(s, tf.mult);
     if (tf.has_cap) y = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y, tf.inv_cap)));
-    return dm_bf16_bits(y);
+    return cache_f32 ? y : dm_bf16_f32(dm_bf16_bits(y));
+}
+
+// Base logit (row, position i, id v) as fp32, from a BF16 or an fp32 base.
+__device__ __forceinline__ float base_value(const SampleArgs &a, int row, int i, int v) {
+    const int64_t o = row * a.base_s0 + (int64_t)i * a.base_s1 + v;
+    return a.base_f ? a.base_f[o] : dm_bf16_f32(a.base[o]);
+}
+
+// Cache element (row, i, v) as fp32 (a BF16 cache's values are exact in fp32).
+__device__ __forceinline__ float cache_value(const SampleArgs &a, int row, int i, int v) {
+    const int64_t o = row * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
+    return a.cache_f ? a.cache_f[o] : dm_bf16_f32(a.cache[o]);
+}
+
+// Store a logit from logit_value into the cache (for a BF16 cache the value
+// is a BF16 value: its top 16 bits).
+__device__ __forceinline__ void cache_put(const SampleArgs &a, int row, int i, int v, float l) {
+    const int64_t o = row * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
+    if (a.cache_f)
+        a.cache_f[o] = l;
+    else
+        a.cache[o] = (uint16_t)(__float_as_uint(l) >> 16);
 }
 
 // Two fp32 values rounded to BF16 (nearest, ties to even) in one

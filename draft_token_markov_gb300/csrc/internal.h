@@ -47,6 +47,11 @@ struct SampleArgs {
     int64_t tok_s0;
     uint16_t *cache;
     int64_t cache_s0, cache_s1;
+    // fp32 variants (the simple chain and the batch path): when set, the
+    // base logits / the cache are fp32 at these pointers (same strides, in
+    // elements) and base / cache are unused
+    const float *base_f;
+    float *cache_f;
     float *noise;              // [rows * N, V] fp32 Gumbel noise (Gumbel mode)
     int64_t noise_s0;          // row stride of the noise, in floats
     // plan scratch

@@ -290,7 +290,28 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
                                   float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
                                   uint16_t *logit_cache, int64_t cache_s0, int64_t cache_s1,
                                   void *stream) {
+    return markov_chain_sample_typed(p, base_logits, MARKOV_BF16, base_s0, base_s1, head, embed,
+                                     anchor_tokens, temperature, seeds, row_state_idx, rows, mode,
+                                     output_multiplier, soft_cap, draft_tokens, tok_s0,
+                                     logit_cache, MARKOV_BF16, cache_s0, cache_s1, stream);
+}
+
+markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
+                                        markov_dtype base_dtype, int64_t base_s0,
+                                        int64_t base_s1, const uint16_t *head,
+                                        const uint16_t *embed, const int32_t *anchor_tokens,
+                                        const float *temperature, const int64_t *seeds,
+                                        const int64_t *row_state_idx, int32_t rows,
+                                        markov_mode mode, float output_multiplier,
+                                        float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
+                                        void *logit_cache, markov_dtype cache_dtype,
+                                        int64_t cache_s0, int64_t cache_s1, void *stream) {
     if (!p) return MARKOV_EINVAL;
+    if ((base_dtype != MARKOV_BF16 && base_dtype != MARKOV_F32) ||
+        (cache_dtype != MARKOV_BF16 && cache_dtype != MARKOV_F32))
+        return MARKOV_EINVAL;
+    const bool base_f32 = base_dtype == MARKOV_F32, cache_f32 = cache_dtype == MARKOV_F32;
+    const int64_t cache_es = cache_f32 ? 4 : 2;   // cache element bytes
     const int V = p->d.vocab, r = p->d.rank, N = p->d.num_steps;
     if (!base_logits || !head || !embed || !anchor_tokens || !temperature || !seeds ||
         !row_state_idx || !draft_tokens || !logit_cache)
@@ -302,7 +323,8 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     if (tok_s0 < N) return MARKOV_EINVAL;
     // the cache asserts of the sharded_markov page's sample(): 16-byte
     // aligned pointer and row strides
-    if (!aligned16(logit_cache) || (cache_s0 * 2) % 16 != 0 || (cache_s1 * 2) % 16 != 0)
+    if (!aligned16(logit_cache) || (cache_s0 * cache_es) % 16 != 0 ||
+        (cache_s1 * cache_es) % 16 != 0)
         return MARKOV_EINVAL;
     if (!aligned16(head) || !aligned16(embed)) return MARKOV_EINVAL;
     if (!std::isfinite(output_multiplier) || std::isnan(soft_cap)) return MARKOV_EINVAL;
@@ -312,14 +334,18 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     if ((p->path == MARKOV_PATH_CHAIN || p->path == MARKOV_PATH_CHAIN_SIMPLE) && !chain)
         return MARKOV_EUNSUPPORTED;
     if (p->path == MARKOV_PATH_BATCH) chain = false;
-    const bool use_tc = chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE;
+    // the tcgen05 chain takes BF16 base logits and cache only
+    if ((base_f32 || cache_f32) && p->path == MARKOV_PATH_CHAIN) return MARKOV_EUNSUPPORTED;
+    const bool use_tc =
+        chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE && !base_f32 && !cache_f32;
 
     DeviceGuard guard(p->d.device);
     if (!guard.ok) return MARKOV_EDEVICE;
     cudaStream_t s = (cudaStream_t)stream;
 
     SampleArgs a{};
-    a.base = base_logits;
+    a.base = base_f32 ? nullptr : static_cast<const uint16_t *>(base_logits);
+    a.base_f = base_f32 ? static_cast<const float *>(base_logits) : nullptr;
     a.base_s0 = base_s0;
     a.base_s1 = base_s1;
     a.head = head;
@@ -336,7 +362,8 @@ markov_status markov_chain_sample(markov_plan *p, const uint16_t *base_logits, i
     a.tf = make_transform(output_multiplier, soft_cap);
     a.tokens = draft_tokens;
     a.tok_s0 = tok_s0;
-    a.cache = logit_cache;
+    a.cache = cache_f32 ? nullptr : static_cast<uint16_t *>(logit_cache);
+    a.cache_f = cache_f32 ? static_cast<float *>(logit_cache) : nullptr;
     a.cache_s0 = cache_s0;
     a.cache_s1 = cache_s1;
     a.noise = p->noise;

@@ -58,6 +58,13 @@ typedef enum markov_mode {
     MARKOV_INVCDF = 1           /* inverse CDF (fused_markov page) */
 } markov_mode;
 
+/* Element type of the base logits and of the logits cache (sharded_markov
+ * page: the chain kernel is compiled per base and cache dtype, BF16 or fp32). */
+typedef enum markov_dtype {
+    MARKOV_BF16 = 0,
+    MARKOV_F32 = 1
+} markov_dtype;
+
 typedef enum markov_path {
     MARKOV_PATH_AUTO = 0,       /* chain up to markov_chain_max_rows rows, else batch */
     MARKOV_PATH_CHAIN = 1,      /* the persistent single-launch chain kernel (tcgen05, head
@@ -155,6 +162,33 @@ markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits
                                   float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
                                   uint16_t *logit_cache, int64_t cache_s0,
                                   int64_t cache_s1, void *stream);
+
+/* markov_chain_sample with the base logits and the cache in either dtype
+ * (sharded_markov page: BF16 or fp32 for both; the module docstring's
+ * cache_round rounds each logit to the cache's dtype).
+ *   base_logits   device, [rows, N, V] of base_dtype, strides in elements.
+ *   logit_cache   device, [rows, N, V] of cache_dtype, strides in elements;
+ *                 pointer and row strides 16-byte aligned.
+ *   With an fp32 cache a logit is fp32(base) + fp32(bf16(head . embed)),
+ *   then the transform's fp32 steps when there is one, never rounded to
+ *   BF16; with a BF16 cache it is markov_chain_sample's logit (an fp32 base
+ *   is added in fp32 before the BF16 rounding).  Keys and tokens follow from
+ *   the cached values exactly as in markov_chain_sample.
+ * BF16 / BF16 is markov_chain_sample.  Any fp32 operand takes the simple
+ * persistent chain (rows <= 8) or the per-position kernels; a plan forced to
+ * MARKOV_PATH_CHAIN (the tcgen05 chain, BF16 only) returns EUNSUPPORTED.
+ * Other arguments and errors as markov_chain_sample; EINVAL for an unknown
+ * dtype. */
+markov_status markov_chain_sample_typed(markov_plan *plan, const void *base_logits,
+                                        markov_dtype base_dtype, int64_t base_s0,
+                                        int64_t base_s1, const uint16_t *head,
+                                        const uint16_t *embed, const int32_t *anchor_tokens,
+                                        const float *temperature, const int64_t *seeds,
+                                        const int64_t *row_state_idx, int32_t rows,
+                                        markov_mode mode, float output_multiplier,
+                                        float soft_cap, int64_t *draft_tokens, int64_t tok_s0,
+                                        void *logit_cache, markov_dtype cache_dtype,
+                                        int64_t cache_s0, int64_t cache_s1, void *stream);
 
 /* markov_chain_sample without a plan, for callers that cannot allocate
  * device memory: code running while a CUDA graph is captured on a stream

@@ -23,6 +23,7 @@ from __future__ import annotations
 from dataclasses import dataclass, field
 
 import numpy as np
+import torch
 
 import oracle
 from oracle import GUMBEL, INVCDF
@@ -158,6 +159,129 @@ def check(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mode: int
                 sp[b] = gt
                 t2, c2 = oracle.chain(base, head_bits, embed_bits, anchor, temp, seeds, idx2, mode,
                                       mult, cap, start_step=ss, start_prev=sp, nthreads=nthreads)
+                ref_tok[i + 1:] = t2[b, i + 1:]
+                ref_cache[i + 1:] = c2[b, i + 1:]
+    return rep
+
+
+# ---------------------------------------------- fp32 base / cache variants
+
+def _base_f32(base, b, i, v) -> float:
+    """Base logit (b, i, v) as an fp32 value (BF16 bits or fp32 input)."""
+    x = base[b, i, v]
+    if base.dtype == np.uint16:
+        return float(oracle.bits_to_f32(np.array([x], np.uint16))[0])
+    return float(x)
+
+
+def _typed_logit(base, b, i, v, bias_bits, cache_f32, mult, cap) -> float:
+    return float(np.float32(oracle.logit_typed(_base_f32(base, b, i, v), int(bias_bits), cache_f32,
+                                               mult, cap)))
+
+
+def check_typed(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mode: int,
+                mult: float, cap, gpu_tokens: np.ndarray, gpu_cache: np.ndarray, cache_f32: bool,
+                tok_sentinel: int, cache_sentinel_bits: int, nthreads: int = 0) -> Report:
+    """The acceptance rule of `check` for a BF16 or fp32 base and a BF16 or
+    fp32 cache.  gpu_cache holds BF16 bits (uint16) or fp32 values (float32).
+    An fp32 cache element must equal the oracle's exactly (NaN where the
+    oracle has NaN) unless a one-ulp change of its BF16 bias explains it; a
+    BF16 cache element as in `check`.  Tokens as in `check`, on fp32 keys."""
+    base_t = inputs["base"]
+    base = (base_t.numpy() if base_t.dtype == torch.float32 else oracle.bf16_bits(base_t))
+    anchor = inputs["anchor"].numpy()
+    temp = inputs["temperature"].numpy()
+    seeds = inputs["seeds"].numpy()
+    idx = inputs["row_state_idx"].numpy()
+    R, N, V = base.shape
+    o_tok, o_cache = oracle.chain_typed(base, head_bits, embed_bits, anchor, temp, seeds, idx,
+                                        mode, mult, cap, cache_f32=cache_f32, nthreads=nthreads)
+    rep = Report()
+    for b in range(R):
+        if idx[b] < 0:
+            raw = gpu_cache[b].view(np.uint32 if cache_f32 else np.uint16)
+            if not (np.all(gpu_tokens[b] == tok_sentinel) and np.all(raw == cache_sentinel_bits)):
+                rep.failures.append(("padding row written", b))
+            continue
+        ref_tok = o_tok[b].copy()
+        ref_cache = o_cache[b].copy()
+        T = float(temp[b])
+        seed = int(seeds[b])
+        for i in range(N):
+            rep.positions += 1
+            g, r_ = gpu_cache[b, i], ref_cache[i]
+            if cache_f32:
+                gf, rf = g.astype(np.float32), r_.astype(np.float32)
+                gn, rn = np.isnan(gf), np.isnan(rf)
+            else:
+                gf, rf = oracle.bits_to_f32(g), oracle.bits_to_f32(r_)
+                gn, rn = is_nan_bf16(g), is_nan_bf16(r_)
+            if np.any(gn != rn):
+                rep.failures.append(("cache NaN mismatch", b, i))
+            both = ~gn & ~rn
+            rep.cache_elems += int(both.sum())
+            if cache_f32:
+                diff = both & (gf != rf)
+                far = diff
+            else:
+                d = np.zeros(V, dtype=np.int64)
+                d[both] = np.abs(ordered_bf16(g[both]) - ordered_bf16(r_[both]))
+                diff = d >= 1
+                far = d > 1
+                rep.cache_ulp_diffs += int((d == 1).sum())
+            p_i = int(anchor[b]) if i == 0 else int(gpu_tokens[b, i - 1])
+            for v in np.flatnonzero(far):
+                bias = oracle.bias_one(head_bits, embed_bits, int(v), p_i)
+                allowed = {_typed_logit(base, b, i, int(v), nb, cache_f32, mult, cap)
+                           for nb in bf16_nudges(bias)}
+                if float(gf[v]) in allowed:
+                    rep.cache_bias_ulp += 1
+                else:
+                    rep.failures.append(("cache beyond a 1-ulp bias change", b, i, int(v)))
+            gt = int(gpu_tokens[b, i])
+            sel, _, _ = oracle.select_f(gf, T, mode, seed, b, i)
+            if sel != gt:
+                rep.failures.append(("selection on GPU cache differs", b, i, sel, gt))
+                continue
+            if gt == int(ref_tok[i]):
+                continue
+            if not np.any(diff):
+                rep.failures.append(("token differs with identical cache", b, i, gt,
+                                     int(ref_tok[i])))
+                continue
+            ot = int(ref_tok[i])
+            excuse = None
+            if mode == GUMBEL or not (T > 0):
+                def key_range(v):
+                    bias = oracle.bias_one(head_bits, embed_bits, v, p_i)
+                    ks = []
+                    for nb in bf16_nudges(bias):
+                        l = _typed_logit(base, b, i, v, nb, cache_f32, mult, cap)
+                        if not (T > 0):
+                            ks.append(l)
+                        else:
+                            x = np.float32(np.float32(l) / np.float32(T))
+                            ks.append(float(np.float32(x + np.float32(oracle.gumbel(seed, b, i, v, 1)[0]))))
+                    return min(ks), max(ks)
+                lo_w, _ = key_range(ot)
+                _, hi_g = key_range(gt)
+                if hi_g >= lo_w:
+                    excuse = ("contender", b, i, gt, ot, float(hi_g - lo_w))
+            else:
+                excuse = ("inverse-cdf on a cache 1 ulp apart", b, i, gt, ot)
+            if excuse is None:
+                rep.failures.append(("token not excusable", b, i, gt, ot))
+                continue
+            rep.excused.append(excuse)
+            if i + 1 < N:
+                idx2 = np.full(R, -1, dtype=np.int64)
+                idx2[b] = idx[b]
+                ss = np.full(R, i + 1, dtype=np.int32)
+                sp = np.zeros(R, dtype=np.int64)
+                sp[b] = gt
+                t2, c2 = oracle.chain_typed(base, head_bits, embed_bits, anchor, temp, seeds, idx2,
+                                            mode, mult, cap, cache_f32=cache_f32, start_step=ss,
+                                            start_prev=sp, nthreads=nthreads)
                 ref_tok[i + 1:] = t2[b, i + 1:]
                 ref_cache[i + 1:] = c2[b, i + 1:]
     return rep
