@@ -234,14 +234,16 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.CONFIGS[WORKLOAD_CFG]
+    base_f32, cache_f32 = args.base_dtype == "f32", args.cache_dtype == "f32"
     head, embed = W.make_weights(w)
-    inp = W.make_call(w)
+    inp = W.make_call(w, base_f32=base_f32)
     head, embed = head.to(dev), embed.to(dev)
     d = {k: v.to(dev) for k, v in inp.items()}
     plan = api.Plan(w.vocab, w.rank, w.steps, w.rows, device=local)
     R, N, V = w.rows, w.steps, w.vocab
     toks = torch.full((R, N), -1, dtype=torch.int64, device=dev)
-    cache = torch.empty((R, N, V), dtype=torch.bfloat16, device=dev)
+    cache = torch.empty((R, N, V), dtype=torch.float32 if cache_f32 else torch.bfloat16,
+                        device=dev)
     live = int((inp["row_state_idx"] >= 0).sum())
     tokens_per_step = live * N
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -327,10 +329,11 @@ def run_gpu(args):
     d2h = h_tok.numel() * h_tok.element_size()
 
     peak, peak_kind = _peaks()
-    alg_bytes = W.algorithmic_bytes(w)
+    alg_bytes = W.algorithmic_bytes(w, 4 if base_f32 else 2, 4 if cache_f32 else 2)
+    typed = base_f32 or cache_f32
     chain_avg_s = statistics.mean(chain_ms) / 1000.0
     achieved = alg_bytes / chain_avg_s / 1e9
-    traffic = _traffic()
+    traffic = None if typed else _traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores = cpu_oracle_sample(args.cpu_seconds)
@@ -341,7 +344,8 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if not typed else f"{args.base_dtype} base, {args.cache_dtype} cache",
         "data": "synthetic (seeded, shaped like the pages' DeepSeek-V4.1 Markov head; "
                 "random weights)",
         "config": {"workload": w.name, "rows": R, "live_rows": live, "vocab": V, "rank": w.rank,
@@ -354,7 +358,9 @@ def run_gpu(args):
                         "chain_kernel_median": statistics.median(chain_ms) * 1000.0},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "chain_tc_kernel", "algorithmic_bytes_per_launch": alg_bytes,
+                     "kernel": {"tcgen05 chain": "chain_tc_kernel", "simple chain": "chain_kernel",
+                                "batch": "batch kernels"}.get(path, path),
+                     "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,
         "e2e": {"value": tokens_per_step / (e2e_step / 1000.0), "unit": UNIT,
@@ -381,6 +387,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--base-dtype", default="bf16", choices=["bf16", "f32"],
+                    help="element type of the base logits (f32: the typed variant, simple chain)")
+    ap.add_argument("--cache-dtype", default="bf16", choices=["bf16", "f32"],
+                    help="element type of the logits cache")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

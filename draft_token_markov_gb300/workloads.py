@@ -138,7 +138,10 @@ def small(V: int, r: int, rows: int, steps: int, mode: int = GUMBEL, *, seed: in
 
 
 # Algorithmic bytes of one call: the head once, the live rows' base-logit
-# reads and their cache writes (BF16).  Noise bytes are not algorithmic.
-def algorithmic_bytes(w: Workload) -> int:
+# reads and their cache writes (BF16 unless the element sizes say otherwise).
+# Noise bytes are not algorithmic.
+def algorithmic_bytes(w: Workload, base_bytes: int = 2, cache_bytes: int = 2) -> int:
+    """base_bytes / cache_bytes: element sizes of the base logits and the
+    cache (2 for BF16, 4 for fp32)."""
     head = w.vocab * w.rank * 2
-    return head + 2 * (w.live_rows * w.steps * w.vocab * 2)
+    return head + w.live_rows * w.steps * w.vocab * (base_bytes + cache_bytes)
