@@ -274,11 +274,15 @@ __device__ __forceinline__ void noise_bounds(const Ctl &c, const SampleArgs &a, 
 template <int NT>
 __device__ __forceinline__ void prefetch_base(const Ctl &c, const SampleArgs &a, int p, int v_begin,
                                               int v_end, int te) {
+    const int es = a.base_f ? 4 : 2;   // BF16 or fp32 base logits
 #pragma unroll 1
     for (int b = 0; b < a.rows && b < kChainRows; ++b) {
         if (!c.live[b]) continue;
-        const uint16_t *row = a.base + b * a.base_s0 + (int64_t)p * a.base_s1;
-        for (int v = v_begin + te * 64; v < v_end; v += NT * 64) tc::prefetch_l2(row + v);
+        const int64_t off = b * a.base_s0 + (int64_t)p * a.base_s1;
+        const uint8_t *row = a.base_f ? reinterpret_cast<const uint8_t *>(a.base_f + off)
+                                      : reinterpret_cast<const uint8_t *>(a.base + off);
+        for (int64_t o = (int64_t)v_begin * es + te * 128; o < (int64_t)v_end * es; o += NT * 128)
+            tc::prefetch_l2(row + o);
     }
 }
 
@@ -292,6 +296,13 @@ __device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf
         y1 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y1, tf.inv_cap)));
     }
     return bf16x2_rn(y0, y1);
+}
+
+// The output-logit transform of one fp32 logit, kept in fp32 (fp32 caches).
+__device__ __noinline__ float transform_f32(float s, const Transform &tf) {
+    float y = __fmul_rn(s, tf.mult);
+    if (tf.has_cap) y = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y, tf.inv_cap)));
+    return y;
 }
 
 // The MMAs of accumulator W (issued by warp W): tiles W, W + 2, ...; per
@@ -421,10 +432,9 @@ __device__ __forceinline__ void simt_tile(Ctl &c, int kt, int ntm, int m, uint32
     c.sbias[id + 8][col + 1] = d3;
 }
 
-// The exact key of Gumbel survivor (id v, row b, cached logit l16) folded
+// The exact key of Gumbel survivor (id v, row b, cached logit lf) folded
 // into the CTA's best key of that row (shared-memory atomic maximum).
-__device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, uint32_t l16) {
-    const float lf = __uint_as_float(l16 << 16);
+__device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, float lf) {
     const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
     const uint32_t o = ordered_key(exact_key(lf, c.T[b], h));
     atomicMax(&c.cbest[i & 1][b], ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
@@ -463,7 +473,7 @@ __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
 // computed for every id.  Leaves the CTA's per-row best packed key in
 // c.cbest[i & 1] (zeroed, with c.lcta, before the position).  `gum_any`
 // (some row is a Gumbel row) is CTA-uniform.
-template <int RANK, bool kCdf>
+template <int RANK, bool kCdf, int DT>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
                                          const int i, const int t0, const int nt, const int nts,
                                          const int ntm, const uint32_t b_sa, const uint32_t head_sa,
@@ -486,8 +496,14 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     const uint32_t gum_m = kCdf ? 0u : (samp_m & live_m);
     div_m = kCdf ? (div_m & live_m) : 0u;
     const uint32_t *gq = reinterpret_cast<const uint32_t *>(a.noise) + ((int64_t)i * V) * 2 + hr;
-    const uint16_t *base_i = a.base + (int64_t)i * a.base_s1 + rb * a.base_s0;
-    uint16_t *cache_i = a.cache + (int64_t)i * a.cache_s1 + rb * a.cache_s0;
+    // DT bit 0: fp32 base logits, bit 1: fp32 cache (else BF16)
+    constexpr bool kBaseF32 = (DT & 1) != 0, kCacheF32 = (DT & 2) != 0;
+    const int64_t bofs = (int64_t)i * a.base_s1 + rb * a.base_s0;
+    const int64_t cofs = (int64_t)i * a.cache_s1 + rb * a.cache_s0;
+    const uint16_t *base_i = kBaseF32 ? nullptr : a.base + bofs;
+    const float *base_fi = kBaseF32 ? a.base_f + bofs : nullptr;
+    uint16_t *cache_i = kCacheF32 ? nullptr : a.cache + cofs;
+    float *cache_fi = kCacheF32 ? a.cache_f + cofs : nullptr;
 
     uint32_t bo[kRowsT], bv[kRowsT];   // best ordered (exact) key and its id
     float lbm[kRowsT], invT[kRowsT];   // Gumbel rows: largest key lower bound
@@ -511,7 +527,10 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         const bool ok2 = k < nt && v < V;
 #pragma unroll
         for (int j = 0; j < kRowsT; ++j)
-            bb[j] = (ok2 && ((live_m >> j) & 1u)) ? (uint32_t)__ldg(base_i + j * a.base_s0 + v) : 0u;
+            bb[j] = (ok2 && ((live_m >> j) & 1u))
+                        ? (kBaseF32 ? __float_as_uint(__ldg(base_fi + j * a.base_s0 + v))
+                                    : (uint32_t)__ldg(base_i + j * a.base_s0 + v))
+                        : 0u;
         qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
     load_tile(wg, nb, nq);
@@ -582,28 +601,48 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
         const int v = (t0 + k) * 128 + q * 32 + lane;
         const bool valid = v < V;
-        // bias = bf16(sum); logit = bf16(f32(base) + f32(bias)), two rows a time
+        // bias = bf16(sum); logit = cache_round(f32(base) + f32(bias)), two
+        // rows a time (BF16 caches: packed; fp32 caches: kept in fp32)
         uint32_t lp[2];
+        float lf4[kRowsT];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const uint32_t bb = bf16x2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            const float s0 = __fadd_rn(__uint_as_float(cb[2 * j] << 16), __uint_as_float(bb << 16));
-            const float s1 = __fadd_rn(__uint_as_float(cb[2 * j + 1] << 16),
-                                       __uint_as_float(bb & 0xffff0000u));
-            lp[j] = bf16x2_rn(s0, s1);
+            const float b0 = kBaseF32 ? __uint_as_float(cb[2 * j]) : __uint_as_float(cb[2 * j] << 16);
+            const float b1 = kBaseF32 ? __uint_as_float(cb[2 * j + 1]) : __uint_as_float(cb[2 * j + 1] << 16);
+            const float s0 = __fadd_rn(b0, __uint_as_float(bb << 16));
+            const float s1 = __fadd_rn(b1, __uint_as_float(bb & 0xffff0000u));
+            if (kCacheF32) {
+                lf4[2 * j] = s0;
+                lf4[2 * j + 1] = s1;
+            } else {
+                lp[j] = bf16x2_rn(s0, s1);
+            }
         }
-        if (a.tf.has_transform) {
-            lp[0] = transform_pair(lp[0], a.tf);
-            lp[1] = transform_pair(lp[1], a.tf);
-        }
+        if (kCacheF32) {
+            if (a.tf.has_transform) {
 #pragma unroll
-        for (int j = 0; j < kRowsT; ++j)
-            if (valid && ((live_m >> j) & 1u))
-                cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
+                for (int j = 0; j < kRowsT; ++j) lf4[j] = transform_f32(lf4[j], a.tf);
+            }
+#pragma unroll
+            for (int j = 0; j < kRowsT; ++j)
+                if (valid && ((live_m >> j) & 1u)) cache_fi[j * a.cache_s0 + v] = lf4[j];
+        } else {
+            if (a.tf.has_transform) {
+                lp[0] = transform_pair(lp[0], a.tf);
+                lp[1] = transform_pair(lp[1], a.tf);
+            }
+#pragma unroll
+            for (int j = 0; j < kRowsT; ++j) {
+                lf4[j] = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
+                if (valid && ((live_m >> j) & 1u))
+                    cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
+            }
+        }
         float ku[kRowsT];
 #pragma unroll
         for (int j = 0; j < kRowsT; ++j) {
-            const float lf = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
+            const float lf = lf4[j];
             ku[j] = 0.0f;
             if ((gum_m >> j) & 1u) {
                 const float xa = lf * invT[j];
@@ -623,10 +662,12 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         if (kRegs && gum_m != 0u) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                k3[j] = k2[j];
-                k2[j] = k1[j];
-                k1[j] = k0[j];
-                k0[j] = lp[j];
+                if (!kCacheF32) {
+                    k3[j] = k2[j];
+                    k2[j] = k1[j];
+                    k1[j] = k0[j];
+                    k0[j] = lp[j];
+                }
                 u3[j] = u2[j];
                 u2[j] = u1[j];
                 u1[j] = u0[j];
@@ -691,9 +732,16 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             const int r = bit >> 2, j = bit & 3;
             const int k = wg + 2 * (ntw - 1 - r);
             const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
-            const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
-                                        : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
-            survivor_key(c, i, v, rb + j, (pr >> (16 * (j & 1))) & 0xffffu);
+            float lf;
+            if (kCacheF32) {
+                // an fp32 cache's logit, read back (this thread wrote it)
+                lf = cache_fi[j * a.cache_s0 + v];
+            } else {
+                const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
+                                            : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
+                lf = __uint_as_float(((pr >> (16 * (j & 1))) & 0xffffu) << 16);
+            }
+            survivor_key(c, i, v, rb + j, lf);
         }
     }
     if (!kRegs && ok) {
@@ -708,9 +756,10 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
 #pragma unroll
             for (int j = 0; j < kRowsT; ++j) {
                 if (!((gum_m >> j) & 1u)) continue;
-                const uint32_t l16 = (uint32_t)__ldcg(cache_i + j * a.cache_s0 + v);
-                if (!(key_upper(__uint_as_float(l16 << 16), invT[j], (qq >> (8 * j)) & 0xffu) < Lc[j]))
-                    survivor_key(c, i, (uint32_t)v, rb + j, l16);
+                const float lf = kCacheF32 ? __ldcg(cache_fi + j * a.cache_s0 + v)
+                                           : __uint_as_float((uint32_t)__ldcg(cache_i + j * a.cache_s0 + v) << 16);
+                if (!(key_upper(lf, invT[j], (qq >> (8 * j)) & 0xffu) < Lc[j]))
+                    survivor_key(c, i, (uint32_t)v, rb + j, lf);
             }
         }
     }
@@ -720,7 +769,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
 
 // MODE 0: Gumbel and greedy rows; MODE 1: inverse-CDF and greedy rows (one
 // kernel per mode keeps each kernel's code smaller).
-template <int RANK, int MODE>
+template <int RANK, int MODE, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
 chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, int noise_ready) {
     constexpr int cpt = RANK / 64;                 // K-chunks per 128-id tile
@@ -913,9 +962,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
             if (MODE == 1)
-                epilogue<RANK, true>(c, a, tmem, i, t0, nt, -1, ntm, b_sa, head_sa, false, timeout, dcount);
+                epilogue<RANK, true, DT>(c, a, tmem, i, t0, nt, -1, ntm, b_sa, head_sa, false, timeout, dcount);
             else
-                epilogue<RANK, false>(c, a, tmem, i, t0, nt, nts, ntm, b_sa, head_sa, gum_any, timeout, dcount);
+                epilogue<RANK, false, DT>(c, a, tmem, i, t0, nt, nts, ntm, b_sa, head_sa, gum_any, timeout, dcount);
         }
         stop = __syncthreads_or(stop_vote(c, a, MODE != 0));
         if (stop) break;
@@ -1081,10 +1130,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     const float M = key_from_ordered(o);
                     if (o == 0xffffffffu || isinf(M)) continue;
-                    const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                    const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
                     uint64_t part = 0ull;
                     for (int v = v_begin + tid; v < v_end; v += kThreads) {
-                        const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                        const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
                         part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                     }
     #pragma unroll
@@ -1147,14 +1196,14 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     const uint64_t H = dm_cdf_hash(c.hri[i][b]);
                     const uint64_t target = __umul64hi(H, S);
                     if (P <= target && target < P + Sc) {
-                        const uint16_t *crow = a.cache + b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                        const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
                         const int len = v_end - v_begin;
                         const int chunk = (len + kThreads - 1) / kThreads;
                         const int c0 = v_begin + tid * chunk;
                         const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
                         uint64_t mine = 0ull;
                         for (int v = c0; v < c1; ++v) {
-                            const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                            const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
                             mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                         }
                         uint64_t incl = mine;
@@ -1170,7 +1219,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         uint64_t run = P + wpre + incl - mine;
                         if (run <= target && target < run + mine) {
                             for (int v = c0; v < c1; ++v) {
-                                const float x = __fdiv_rn(dm_bf16_f32(crow[v]), c.T[b]);
+                                const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
                                 run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                                 if (run > target) {
                                     tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
@@ -1265,34 +1314,53 @@ size_t chain_tc_smem() { return kDynSmem; }
 
 int chain_tc_max_chunks() { return kMaxChunks; }
 
+// One kernel per (rank, mode, base / cache dtypes).
+template <int RANK>
+static const void *tc_kernel_for(int mode, int dt) {
+    switch (mode * 4 + dt) {
+        case 0: return (const void *)chain_tc_kernel<RANK, 0, 0>;
+        case 1: return (const void *)chain_tc_kernel<RANK, 0, 1>;
+        case 2: return (const void *)chain_tc_kernel<RANK, 0, 2>;
+        case 3: return (const void *)chain_tc_kernel<RANK, 0, 3>;
+        case 4: return (const void *)chain_tc_kernel<RANK, 1, 0>;
+        case 5: return (const void *)chain_tc_kernel<RANK, 1, 1>;
+        case 6: return (const void *)chain_tc_kernel<RANK, 1, 2>;
+        default: return (const void *)chain_tc_kernel<RANK, 1, 3>;
+    }
+}
+
+static const void *tc_kernel(int r, int mode, int dt) {
+    switch (r) {
+        case 64: return tc_kernel_for<64>(mode, dt);
+        case 128: return tc_kernel_for<128>(mode, dt);
+        case 256: return tc_kernel_for<256>(mode, dt);
+        default: return nullptr;
+    }
+}
+
 cudaError_t chain_tc_prepare() {
     cudaError_t e = cudaSuccess;
-    for (const void *fn :
-         {(const void *)chain_tc_kernel<64, 0>, (const void *)chain_tc_kernel<128, 0>,
-          (const void *)chain_tc_kernel<256, 0>, (const void *)chain_tc_kernel<64, 1>,
-          (const void *)chain_tc_kernel<128, 1>, (const void *)chain_tc_kernel<256, 1>}) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
-        if (e != cudaSuccess) return e;
-    }
+    for (int r : {64, 128, 256})
+        for (int mode = 0; mode < 2; ++mode)
+            for (int dt = 0; dt < 4; ++dt) {
+                e = cudaFuncSetAttribute(tc_kernel(r, mode, dt),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDynSmem);
+                if (e != cudaSuccess) return e;
+            }
     return e;
 }
 
 cudaError_t chain_tc_occupancy(int *blocks_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, chain_tc_kernel<256, 0>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, chain_tc_kernel<256, 0, 0>,
                                                          kThreads, kDynSmem);
 }
 
 cudaError_t launch_chain_tc(const SampleArgs &a, const CUtensorMap &tmap, int noise_ready,
                             cudaStream_t stream) {
     void *args[] = {(void *)&a, (void *)&tmap, (void *)&noise_ready};
-    const void *fn = nullptr;
-    const bool cdf = a.mode == 1;
-    switch (a.r) {
-        case 64: fn = cdf ? (const void *)chain_tc_kernel<64, 1> : (const void *)chain_tc_kernel<64, 0>; break;
-        case 128: fn = cdf ? (const void *)chain_tc_kernel<128, 1> : (const void *)chain_tc_kernel<128, 0>; break;
-        case 256: fn = cdf ? (const void *)chain_tc_kernel<256, 1> : (const void *)chain_tc_kernel<256, 0>; break;
-        default: return cudaErrorInvalidValue;
-    }
+    const int dt = (a.base_f ? 1 : 0) | (a.cache_f ? 2 : 0);
+    const void *fn = tc_kernel(a.r, a.mode == 1 ? 1 : 0, dt);
+    if (!fn) return cudaErrorInvalidValue;
     return cudaLaunchCooperativeKernel(fn, dim3(a.grid), dim3(kThreads), args, kDynSmem, stream);
 }
 

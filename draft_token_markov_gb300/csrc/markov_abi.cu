@@ -334,10 +334,7 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
     if ((p->path == MARKOV_PATH_CHAIN || p->path == MARKOV_PATH_CHAIN_SIMPLE) && !chain)
         return MARKOV_EUNSUPPORTED;
     if (p->path == MARKOV_PATH_BATCH) chain = false;
-    // the tcgen05 chain takes BF16 base logits and cache only
-    if ((base_f32 || cache_f32) && p->path == MARKOV_PATH_CHAIN) return MARKOV_EUNSUPPORTED;
-    const bool use_tc =
-        chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE && !base_f32 && !cache_f32;
+    const bool use_tc = chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE;
 
     DeviceGuard guard(p->d.device);
     if (!guard.ok) return MARKOV_EDEVICE;

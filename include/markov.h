@@ -174,11 +174,9 @@ markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits
  *   BF16; with a BF16 cache it is markov_chain_sample's logit (an fp32 base
  *   is added in fp32 before the BF16 rounding).  Keys and tokens follow from
  *   the cached values exactly as in markov_chain_sample.
- * BF16 / BF16 is markov_chain_sample.  Any fp32 operand takes the simple
- * persistent chain (rows <= 8) or the per-position kernels; a plan forced to
- * MARKOV_PATH_CHAIN (the tcgen05 chain, BF16 only) returns EUNSUPPORTED.
- * Other arguments and errors as markov_chain_sample; EINVAL for an unknown
- * dtype. */
+ * BF16 / BF16 is markov_chain_sample.  Every path takes every dtype pair
+ * (each kernel is compiled per base and cache dtype).  Other arguments and
+ * errors as markov_chain_sample; EINVAL for an unknown dtype. */
 markov_status markov_chain_sample_typed(markov_plan *plan, const void *base_logits,
                                         markov_dtype base_dtype, int64_t base_s0,
                                         int64_t base_s1, const uint16_t *head,

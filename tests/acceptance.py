@@ -179,14 +179,37 @@ def _typed_logit(base, b, i, v, bias_bits, cache_f32, mult, cap) -> float:
                                                mult, cap)))
 
 
+def _bias_candidates(head_bits, embed_bits, v: int, p: int) -> set:
+    """BF16 biases a correct fp32 reduction of head[v] . embed[p] can round
+    to, in any summation order: the oracle's bias one ulp either way, and
+    every BF16 value within the fp32 summation error bound 2 r u sum|h e|
+    (u = 2^-24) of the exact (fp64) dot product, rounded outward.  Under
+    cancellation that bound spans more than one BF16 ulp of the small sum,
+    which an fp32 cache keeps (a BF16 cache's rounding of base + bias hides
+    it)."""
+    cands = set(bf16_nudges(oracle.bias_one(head_bits, embed_bits, v, p)))
+    h = oracle.bits_to_f32(np.ascontiguousarray(head_bits[v])).astype(np.float64)
+    e = oracle.bits_to_f32(np.ascontiguousarray(embed_bits[p])).astype(np.float64)
+    dot = float(np.dot(h, e))
+    err = 2.0 * h.size * 2.0 ** -24 * float(np.sum(np.abs(h * e)))
+    lo = oracle.bf16_rne(np.array([dot - err], dtype=np.float32))[0]
+    hi = oracle.bf16_rne(np.array([dot + err], dtype=np.float32))[0]
+    a, b = int(ordered_bf16(np.array([lo], np.uint16))[0]), int(ordered_bf16(np.array([hi], np.uint16))[0])
+    for o in range(min(a, b) - 1, max(a, b) + 2):
+        cands.add((o if o >= 0 else (0x8000 | (-o))) & 0xFFFF)
+    return cands
+
+
 def check_typed(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mode: int,
                 mult: float, cap, gpu_tokens: np.ndarray, gpu_cache: np.ndarray, cache_f32: bool,
                 tok_sentinel: int, cache_sentinel_bits: int, nthreads: int = 0) -> Report:
     """The acceptance rule of `check` for a BF16 or fp32 base and a BF16 or
     fp32 cache.  gpu_cache holds BF16 bits (uint16) or fp32 values (float32).
     An fp32 cache element must equal the oracle's exactly (NaN where the
-    oracle has NaN) unless a one-ulp change of its BF16 bias explains it; a
-    BF16 cache element as in `check`.  Tokens as in `check`, on fp32 keys."""
+    oracle has NaN) unless another BF16 bias of the same dot product that a
+    correct fp32 reduction can give (_bias_candidates) explains it; a BF16
+    cache element as in `check`, with the same bias set.  Tokens as in
+    `check`, on fp32 keys."""
     base_t = inputs["base"]
     base = (base_t.numpy() if base_t.dtype == torch.float32 else oracle.bf16_bits(base_t))
     anchor = inputs["anchor"].numpy()
@@ -231,9 +254,8 @@ def check_typed(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mod
                 rep.cache_ulp_diffs += int((d == 1).sum())
             p_i = int(anchor[b]) if i == 0 else int(gpu_tokens[b, i - 1])
             for v in np.flatnonzero(far):
-                bias = oracle.bias_one(head_bits, embed_bits, int(v), p_i)
                 allowed = {_typed_logit(base, b, i, int(v), nb, cache_f32, mult, cap)
-                           for nb in bf16_nudges(bias)}
+                           for nb in _bias_candidates(head_bits, embed_bits, int(v), p_i)}
                 if float(gf[v]) in allowed:
                     rep.cache_bias_ulp += 1
                 else:
@@ -253,9 +275,8 @@ def check_typed(inputs: dict, head_bits: np.ndarray, embed_bits: np.ndarray, mod
             excuse = None
             if mode == GUMBEL or not (T > 0):
                 def key_range(v):
-                    bias = oracle.bias_one(head_bits, embed_bits, v, p_i)
                     ks = []
-                    for nb in bf16_nudges(bias):
+                    for nb in _bias_candidates(head_bits, embed_bits, v, p_i):
                         l = _typed_logit(base, b, i, v, nb, cache_f32, mult, cap)
                         if not (T > 0):
                             ks.append(l)

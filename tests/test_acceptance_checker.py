@@ -88,3 +88,42 @@ def test_checker_bias_ulp_rule():
     v = (int(toks[0, 0]) + 1) % 256
     c3[0, 0, v] = int(c3[0, 0, v]) + (3 if c3[0, 0, v] < 0x7000 else -3)
     assert not _chk(w, inp, hb, eb, toks, c3).ok()
+
+
+def test_typed_checker_accepts_oracle_and_rejects_mistakes():
+    from tests.acceptance import check_typed
+    sent_bits = 0x7FABCDEF
+    for base_f32, cache_f32 in ((True, True), (False, True), (True, False)):
+        w = W.small(512, 32, 3, 3, W.GUMBEL, seed=22, padding_rows=(1,),
+                    temperatures=(0.0, 1.0))
+        head, embed = W.make_weights(w)
+        inp = W.make_call(w, base_f32=base_f32)
+        hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
+        base = inp["base"].numpy() if base_f32 else oracle.bf16_bits(inp["base"])
+        toks = np.full((w.rows, w.steps), SENT_T, dtype=np.int64)
+        if cache_f32:
+            cache = np.full((w.rows, w.steps, w.vocab), sent_bits, dtype=np.uint32).view(np.float32)
+        else:
+            cache = np.full((w.rows, w.steps, w.vocab), SENT_C, dtype=np.uint16)
+        toks, cache = oracle.chain_typed(base, hb, eb, inp["anchor"].numpy(),
+                                         inp["temperature"].numpy(), inp["seeds"].numpy(),
+                                         inp["row_state_idx"].numpy(), w.mode,
+                                         cache_f32=cache_f32, tokens=toks, cache=cache)
+        sent = sent_bits if cache_f32 else SENT_C
+
+        def chk(t, c):
+            return check_typed(inp, hb, eb, w.mode, 1.0, None, t, c, cache_f32, SENT_T, sent)
+
+        assert chk(toks, cache).ok()
+        t2 = toks.copy()
+        t2[0, 1] = (t2[0, 1] + 1) % 512
+        assert not chk(t2, cache).ok()
+        c2 = cache.copy()
+        if cache_f32:
+            c2[2, 0, 5] = c2[2, 0, 5] + np.float32(0.25)       # far beyond any bias change
+        else:
+            c2[2, 0, 5] = int(c2[2, 0, 5]) + 2
+        assert not chk(toks, c2).ok()
+        c3 = cache.copy()
+        c3[1, 0, 0] = c3[2, 0, 0]                               # a padding row written
+        assert not chk(toks, c3).ok()

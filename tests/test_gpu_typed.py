@@ -1,8 +1,8 @@
 """Parity of the fp32 base-logit and fp32 cache variants (the
 sharded_markov page's chain compiled per base and cache dtype, BF16 or
 fp32; cache_round rounds each logit to the cache's dtype) against the
-oracle's typed chain, through the C ABI, on the simple persistent chain
-(up to 8 rows) and the per-position kernels (more rows), both modes,
+oracle's typed chain, through the C ABI, on the tcgen05 chain, the simple
+persistent chain (up to 8 rows) and the per-position kernels (more rows), both modes,
 ragged vocabulary tails (V a multiple of 16, not of 128), padding rows and, for the batch path, a soft cap."""
 import numpy as np
 import pytest
@@ -46,6 +46,10 @@ def _run_typed(api, w, inp, path, cache_f32):
 
 CASES = [
     # (name, workload, path)
+    ("tcgen05 chain", lambda mode: W.small(12000, 256, 8, 4, mode, seed=70, padding_rows=(2, 5),
+                                           spikes=4, temperatures=(0.0, 0.6, 1.0)), CHAIN),
+    ("tcgen05 chain, rank 128, capped", lambda mode: W.small(6000, 128, 4, 3, mode, seed=76,
+                                                             spikes=2, mult=0.5, cap=30.0), CHAIN),
     ("chain", lambda mode: W.small(5008, 128, 6, 4, mode, seed=71, padding_rows=(1,), spikes=3,
                                    temperatures=(0.0, 0.7, 1.0)), SIMPLE),
     ("auto", lambda mode: W.small(4096, 64, 3, 3, mode, seed=72, spikes=2), AUTO),
@@ -77,22 +81,3 @@ def test_bf16_through_the_typed_entry_equals_the_bf16_call(gpu_lib):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_forced_tcgen05_chain_rejects_fp32(gpu_lib):
-    api = gpu_lib
-    w = W.small(4096, 64, 2, 2, W.GUMBEL, seed=75)
-    inp = U.to_dev(W.make_call(w, base_f32=True))
-    h, e, _, _ = U.weights(w)
-    plan = api.Plan(w.vocab, w.rank, w.steps, w.rows)
-    try:
-        plan.set_path(CHAIN)
-        toks = torch.full((w.rows, w.steps), U.SENT_T, dtype=torch.int64, device="cuda")
-        cache = torch.zeros((w.rows, w.steps, w.vocab), dtype=torch.float32, device="cuda")
-        with pytest.raises(api.MarkovError) as ex:
-            api.markov_chain_sample(plan, inp["base"], h.cuda(), e.cuda(), inp["anchor"],
-                                    inp["temperature"], inp["seeds"], inp["row_state_idx"],
-                                    w.mode, 1.0, None, toks, cache)
-        assert ex.value.code == 2                       # MARKOV_EUNSUPPORTED
-        torch.cuda.synchronize()
-        assert np.all(toks.cpu().numpy() == U.SENT_T)
-    finally:
-        plan.close()
