@@ -34,6 +34,9 @@ sys.path.insert(0, ROOT)
 METRIC = "draft tokens/s and µs per N-step Markov call; % of GB300 HBM roofline"
 UNIT = "draft tokens/s"
 WORKLOAD_CFG = 2
+# --workload names: the default is the DeepSeek-V4.1 chain the headline is
+# quoted on; the others measure the remaining workloads' paths
+WORKLOADS = {"deepseek": 2, "latency": 3, "softcap": 4, "batch": 5, "tiny": 1}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_deepseek_traffic.json")
 
 
@@ -162,14 +165,14 @@ def max_over_ranks(value: float) -> float:
     return float(t.item())
 
 
-def cpu_oracle_sample(seconds_hint: float = 20.0):
+def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG):
     """Time the oracle on a bounded sample of the workload: one call over the
     workload's first live row (all N positions), repeated while the total
     stays near seconds_hint.  Returns (tokens/s, sample description, cores)."""
     import numpy as np
     import oracle
     from draft_token_markov_gb300 import workloads as W
-    w = W.CONFIGS[WORKLOAD_CFG]
+    w = W.CONFIGS[cfg]
     head, embed = W.make_weights(w)
     inp = W.make_call(w)
     hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
@@ -180,7 +183,7 @@ def cpu_oracle_sample(seconds_hint: float = 20.0):
     cores = os.cpu_count() or 1
     base = oracle.bf16_bits(inp["base"])
     args = (base, hb, eb, inp["anchor"].numpy(), inp["temperature"].numpy(),
-            inp["seeds"].numpy(), idx, w.mode)
+            inp["seeds"].numpy(), idx, w.mode, w.mult, w.cap)
     t0 = time.perf_counter()
     calls = 0
     while True:
@@ -200,14 +203,15 @@ def run_reference(args):
         return
     vals = []
     desc = cores = None
+    cfg = WORKLOADS[args.workload]
     for _ in range(args.warmup):
-        cpu_oracle_sample(2.0)
+        cpu_oracle_sample(2.0, cfg)
     for _ in range(args.steps):
-        v, desc, cores = cpu_oracle_sample(8.0)
+        v, desc, cores = cpu_oracle_sample(8.0, cfg)
         vals.append(v)
     value = statistics.mean(vals)
     from draft_token_markov_gb300 import workloads as W
-    w = W.CONFIGS[WORKLOAD_CFG]
+    w = W.CONFIGS[cfg]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.steps / value,
@@ -233,7 +237,8 @@ def run_gpu(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.CONFIGS[WORKLOAD_CFG]
+    cfg = WORKLOADS[args.workload]
+    w = W.CONFIGS[cfg]
     base_f32, cache_f32 = args.base_dtype == "f32", args.cache_dtype == "f32"
     head, embed = W.make_weights(w)
     inp = W.make_call(w, base_f32=base_f32)
@@ -336,7 +341,7 @@ def run_gpu(args):
     traffic = None if typed else _traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, cores = cpu_oracle_sample(args.cpu_seconds)
+        v, desc, cores = cpu_oracle_sample(args.cpu_seconds, cfg)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
     ms_per_step = total_ms / args.steps
     value = tokens_per_step * world * args.steps / (total_ms / 1000.0)
@@ -349,7 +354,8 @@ def run_gpu(args):
         "data": "synthetic (seeded, shaped like the pages' DeepSeek-V4.1 Markov head; "
                 "random weights)",
         "config": {"workload": w.name, "rows": R, "live_rows": live, "vocab": V, "rank": w.rank,
-                   "steps_per_call": N, "mode": "gumbel", "l2": "flushed before every step (256 MB write, then a 256 MB read of another buffer)",
+                   "steps_per_call": N,
+                   "mode": "gumbel" if w.mode == W.GUMBEL else "inverse cdf", "l2": "flushed before every step (256 MB write, then a 256 MB read of another buffer)",
                    "parallelism": f"replicas x{world}", "path": path,
                    "resident_head_bytes": plan.query(api.Q_RESIDENT_HEAD_BYTES)},
         "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
@@ -388,9 +394,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--base-dtype", default="bf16", choices=["bf16", "f32"],
-                    help="element type of the base logits (f32: the typed variant, simple chain)")
+                    help="element type of the base logits")
     ap.add_argument("--cache-dtype", default="bf16", choices=["bf16", "f32"],
                     help="element type of the logits cache")
+    ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOADS),
+                    help="deepseek (default, the headline): V=129280 r=256 8 rows N=8; "
+                         "latency: 1 row; softcap: V=262144 r=128 inverse CDF; batch: 64 rows "
+                         "(the per-position path); tiny: V=4096 r=64")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -1,19 +1,37 @@
 // batch.cu -- the per-position path for batches above the chain limit
 // (fused_markov page, FusedMarkovSampler: per draft position a bias
 // contraction plus a logits kernel over (row, vocab block) and a per-row
-// select kernel; sharded_markov page, module docstring: batches above
-// max_rows take this loop).
+// select step; sharded_markov page, module docstring: batches above
+// max_rows take this loop; muse_spark markov page, MarkovSampler: the
+// per-step kernels are launched with programmatic dependent launch).
 //
 // Per position i, in launch order on one stream:
 //   logits  grid (blocks, row groups of 64): bias tiles [16 ids x 64 rows] by
 //           mma.m16n8k16 with the previous tokens' embeddings staged in
 //           shared memory, the epilogue (BF16 rounding, base add, transform,
-//           cache store) and each block's best (key, id) per row;
-//   cdfsum  (inverse CDF only) grid (blocks, rows): the block's integer
-//           weight sum floor(exp(x - M) 2^40) once M is reduced;
-//   pick    grid (rows): reduce the blocks' partials; in inverse-CDF mode find
-//           the block whose prefix holds mulhi64(H, S) and scan it.
-// The next position's logits kernel reads token i from draft_tokens.
+//           cache store) and each block's best (key, id) per row, merged
+//           into the row's winner word by one u64 atomicMax per block.  The
+//           last block of a row group to finish (a done counter) writes the
+//           token of every row the winner decides: all rows in Gumbel mode,
+//           greedy rows and rows with a NaN, +inf or all -inf maximum in
+//           inverse-CDF mode;
+//   cdf     (inverse CDF only) grid (vocab blocks of 4096 ids, rows): the
+//           block's integer weight sum floor(exp(x - M) 2^40); the last
+//           block of a row scans the row's block sums for mulhi64(H, S),
+//           then the target block's weights, and writes the token.
+// The next position's logits kernel reads token i from draft_tokens.  Every
+// block that takes the last-block step resets the counter and the winner
+// word it consumed, so each call leaves them zero for the next.
+//
+// Every launch after the first of a call is a programmatic dependent launch:
+// it may start while the kernel before it still runs, does only input-side
+// work (block ranges, L2 prefetch of its base-logit rows) until
+// griddepcontrol.wait, and every block of every kernel passes that wait
+// before it reads or writes anything the path writes, and before it exits.
+// A grid therefore completes only after the grid before it has, and a
+// kernel's wait covers the whole chain of launches before it.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace dtm {
@@ -21,8 +39,8 @@ namespace dtm {
 namespace {
 
 constexpr int kBW = kBatchThreads / 32;    // warps per block
-constexpr int kGroupRows = 64;             // rows per row group (8 MMA n-tiles)
-constexpr int kNT = kGroupRows / 8;
+constexpr int kGroupRows = kBatchGroupRows;  // rows per row group
+constexpr int kMT = kGroupRows / 16;         // MMA M-tiles (16 rows) per row group
 constexpr int kBPad = 32;
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -32,6 +50,56 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Programmatic dependent launch: pdl_wait() returns once the kernel before
+// this one on the stream has completed and its writes are visible (at once
+// for an ordinary launch); pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// L2 eviction policies: the head is read at every position and should stay
+// in L2 across them; base logits are read once and cache entries written
+// once per call.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_nc_v4(const void *ptr, uint64_t pol) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *ptr, uint64_t pol) {
+    uint32_t v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ float2 ld_nc_f2(const void *ptr, uint64_t pol) {
+    float2 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "l"(ptr), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_u32(void *ptr, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(ptr), "r"(v), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_f2(void *ptr, float2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(ptr), "f"(v.x),
+                 "f"(v.y), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ int64_t prev_token(const SampleArgs &a, int b, int i) {
@@ -49,118 +117,29 @@ __device__ __forceinline__ void block_range(int V, int nblk, int blk, int &v0, i
     v1 = (int)((int64_t)(blk + 1) * nt / nblk) * kTile;
 }
 
-}  // namespace
-
-template <int RANK>
-__global__ void __launch_bounds__(kBatchThreads)
-batch_logits_kernel(const SampleArgs a, int i) {
-    extern __shared__ __align__(16) uint16_t e_smem[];      // [64][RANK + kBPad]
-    __shared__ unsigned long long s_best[kGroupRows];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int blk = blockIdx.x, nblk = gridDim.x;
-    const int row0 = blockIdx.y * kGroupRows;
-    const int V = a.V;
-    int v_begin, v_end;
-    block_range(V, nblk, blk, v_begin, v_end);
-
-    for (int idx = tid; idx < kGroupRows * (RANK / 8); idx += kBatchThreads) {
-        int b = idx / (RANK / 8), c = idx % (RANK / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row_live(a, row0 + b)) {
-            int64_t p = prev_token(a, row0 + b, i);
-            if (p >= 0 && p < V) v = *reinterpret_cast<const uint4 *>(a.embed + p * RANK + 8 * c);
-        }
-        *reinterpret_cast<uint4 *>(e_smem + b * (RANK + kBPad) + 8 * c) = v;
-    }
-    if (tid < kGroupRows) s_best[tid] = 0ull;
-    __syncthreads();
-
-    // rows handled by this thread: row0 + 8 nt + 2t + {0, 1}
-    uint64_t best[kNT][2];
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) best[nt][0] = best[nt][1] = 0ull;
-    const int ngroups = min(kNT, (a.rows - row0 + 7) / 8);
-
-    for (int v0 = v_begin + warp * kTile; v0 < v_end; v0 += kBW * kTile) {
-        float acc[kNT][4];
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-        const uint16_t *ha = a.head + (int64_t)(v0 + g) * RANK + 8 * t;
-        const uint16_t *hb = ha + 8 * RANK;
-#pragma unroll 2
-        for (int j = 0; j < RANK / 32; ++j) {
-            uint4 x = *reinterpret_cast<const uint4 *>(ha + 32 * j);
-            uint4 y = *reinterpret_cast<const uint4 *>(hb + 32 * j);
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-                if (nt >= ngroups) break;
-                uint4 e = *reinterpret_cast<const uint4 *>(e_smem + (nt * 8 + g) * (RANK + kBPad) +
-                                                           8 * t + 32 * j);
-                mma16816(acc[nt], x.x, y.x, x.y, y.y, e.x, e.y);
-                mma16816(acc[nt], x.z, y.z, x.w, y.w, e.z, e.w);
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) {
-            if (nt >= ngroups) break;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = row0 + nt * 8 + 2 * t + (e & 1);
-                if (!row_live(a, row)) continue;
-                const int v = v0 + g + ((e & 2) ? 8 : 0);
-                const float l = logit_value(base_value(a, row, i, v), acc[nt][e], a.tf,
-                                            a.cache_f != nullptr);
-                cache_put(a, row, i, v, l);
-                const float T = a.temperature[row];
-                float key = l;
-                if (samples(T)) {
-                    key = __fdiv_rn(key, T);
-                    if (a.mode == 0)
-                        key = __fadd_rn(key, a.noise[(int64_t)(row * a.N + i) * a.noise_s0 + v]);
-                }
-                const uint64_t pk = pack_key(key, (uint32_t)v);
-                best[nt][e & 1] = pk > best[nt][e & 1] ? pk : best[nt][e & 1];
-            }
-        }
-    }
-#pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint64_t v = best[nt][h];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
-                v = w > v ? w : v;
-            }
-            if (g == 0 && v) atomicMax(&s_best[nt * 8 + 2 * t + h], (unsigned long long)v);
-        }
-    }
-    __syncthreads();
-    if (tid < kGroupRows && row0 + tid < a.rows)
-        a.keys[(int64_t)(row0 + tid) * nblk + blk] = s_best[tid];
+__device__ __forceinline__ unsigned long long *win_slot(const SampleArgs &a, int i, int b) {
+    return reinterpret_cast<unsigned long long *>(a.bwin + (size_t)i * kMaxRows + b);
+}
+__device__ __forceinline__ uint32_t *group_counter(const SampleArgs &a, int i, int grp) {
+    return a.bcnt + (size_t)i * kBatchCntPerStep + grp;
+}
+__device__ __forceinline__ uint32_t *row_counter(const SampleArgs &a, int i, int b) {
+    return a.bcnt + (size_t)i * kBatchCntPerStep + kMaxRows / kGroupRows + b;
 }
 
-// Reduce the blocks' partial maxima of one row (the packed key).
-__device__ uint64_t reduce_partials(const SampleArgs &a, int b, int nblk, uint64_t *s_red) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint64_t m = 0ull;
-    for (int c = tid; c < nblk; c += blockDim.x) {
-        uint64_t k = a.keys[(int64_t)b * nblk + c];
-        m = k > m ? k : m;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        uint64_t w = __shfl_xor_sync(0xffffffffu, m, o);
-        m = w > m ? w : m;
-    }
-    if (lane == 0) s_red[warp] = m;
+// Whether this block is the last of `total` blocks to pass `counter`.  Every
+// block calls it once, after its results are written; the fences order each
+// block's writes before its increment and the last block's reads after it.
+__device__ bool last_block(uint32_t *counter, uint32_t total, int *s_flag) {
     __syncthreads();
-    uint64_t r = 0ull;
-    for (int w = 0; w < (int)(blockDim.x / 32); ++w) r = s_red[w] > r ? s_red[w] : r;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *s_flag = atomicAdd(counter, 1u) == total - 1u;
+    }
     __syncthreads();
-    return r;
+    const bool last = *s_flag != 0;
+    if (last) __threadfence();
+    return last;
 }
 
 // Whether an inverse-CDF row with this winner needs the weight sums: its
@@ -173,111 +152,425 @@ __device__ __forceinline__ bool needs_sums(uint64_t win) {
            M != __uint_as_float(0xff800000u);
 }
 
-__global__ void __launch_bounds__(kBatchThreads)
-batch_cdfsum_kernel(const SampleArgs a, int i, int nblk) {
-    __shared__ uint64_t s_red[kBatchThreads / 32];
-    __shared__ unsigned long long s_sum;
-    const int b = blockIdx.y, blk = blockIdx.x;
-    if (!row_live(a, b) || !samples(a.temperature[b])) return;
-    const uint64_t win = reduce_partials(a, b, nblk, s_red);
-    if (!needs_sums(win)) return;
-    const float M = key_from_ordered(packed_ordered(win));
-    const float T = a.temperature[b];
-    int v0, v1;
-    block_range(a.V, nblk, blk, v0, v1);
-    if (threadIdx.x == 0) s_sum = 0ull;
-    __syncthreads();
-    uint64_t part = 0ull;
-    for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-        float x = __fdiv_rn(cache_value(a, b, i, v), T);
-        part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&s_sum, (unsigned long long)part);
-    __syncthreads();
-    if (threadIdx.x == 0) a.sums[(int64_t)b * nblk + blk] = s_sum;
-}
-
-__global__ void __launch_bounds__(kBatchThreads)
-batch_pick_kernel(const SampleArgs a, int i, int nblk) {
-    __shared__ uint64_t s_red[kBatchThreads / 32];
-    __shared__ uint64_t s_scan[kBatchThreads / 32];
-    __shared__ uint64_t s_blkpre;
-    __shared__ int s_blk;
-    __shared__ int64_t s_tok;
-    const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (!row_live(a, b)) return;
-    const uint64_t win = reduce_partials(a, b, nblk, s_red);
-    const float T = a.temperature[b];
+// The token of a row that its winner decides without weight sums.
+__device__ __forceinline__ int64_t direct_token(const SampleArgs &a, uint64_t win, float T) {
     int64_t tok = (int64_t)packed_id(win);
     if (a.mode == 1 && samples(T)) {
-        uint32_t o = packed_ordered(win);
+        const uint32_t o = packed_ordered(win);
         if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) tok = 0;
-        if (needs_sums(win)) {
-            const float M = key_from_ordered(o);
-            const uint64_t *sums = a.sums + (int64_t)b * nblk;
-            // total and the block holding the target (serial over blocks: few hundred)
-            if (tid == 0) {
-                uint64_t S = 0ull;
-                for (int c = 0; c < nblk; ++c) S += sums[c];
-                const uint64_t H = dm_cdf_hash(dm_row_step_hash((uint64_t)a.seeds[b], (uint32_t)b,
-                                                                (uint32_t)i));
-                const uint64_t target = __umul64hi(H, S);
-                uint64_t pre = 0ull;
-                int c = 0;
-                for (; c < nblk; ++c) {
-                    if (target < pre + sums[c]) break;
-                    pre += sums[c];
-                }
-                s_blk = c < nblk ? c : nblk - 1;
-                s_blkpre = pre;
-                s_red[0] = target;
-                s_tok = -1;
-            }
-            __syncthreads();
-            const uint64_t target = s_red[0];
-            int v0, v1;
-            block_range(a.V, nblk, s_blk, v0, v1);
-            const int len = v1 - v0;
-            const int chunk = (len + kBatchThreads - 1) / kBatchThreads;
-            const int c0 = v0 + tid * chunk, c1 = min(c0 + chunk, v1);
-            uint64_t mine = 0ull;
-            for (int v = c0; v < c1; ++v) {
-                float x = __fdiv_rn(cache_value(a, b, i, v), T);
-                mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-            }
-            uint64_t incl = mine;
+    }
+    return tok;
+}
+
+// The output-logit transform of one fp32 cached logit, and of two packed
+// BF16 cached logits (out of line: only transformed heads take them).
+__device__ __noinline__ float transform_one_f32(float s, const Transform tf) {
+    float y = __fmul_rn(s, tf.mult);
+    if (tf.has_cap) y = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y, tf.inv_cap)));
+    return y;
+}
+
+__device__ __noinline__ uint32_t transform_two_bf16(uint32_t lp, const Transform tf) {
+    float y0 = __fmul_rn(__uint_as_float(lp << 16), tf.mult);
+    float y1 = __fmul_rn(__uint_as_float(lp & 0xffff0000u), tf.mult);
+    if (tf.has_cap) {
+        y0 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y0, tf.inv_cap)));
+        y1 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y1, tf.inv_cap)));
+    }
+    return bf16x2_rn(y0, y1);
+}
+
+// Integer inverse-CDF weight floor(exp(x / T - M) 2^40) of cached logit x.
+__device__ __forceinline__ uint64_t cdf_weight(const SampleArgs &a, int b, int i, int v, float T,
+                                               float M) {
+    const float x = __fdiv_rn(cache_value(a, b, i, v), T);
+    return (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+}
+
+}  // namespace
+
+// The logits kernel of position i.  MMA roles: M = 16 rows (the previous
+// tokens' embeddings, staged in shared memory), N = 8 vocab ids (head rows,
+// read from global), K = rank, so that each thread's accumulators hold pairs
+// of consecutive ids of one row: base logits are read and cache entries
+// written two ids at a time.  Rows of a thread: row0 + 16 m + 8 h + g for
+// M-tile m < kMT and half h < 2 (bit 2 m + h of `live`).
+template <int RANK, bool kBaseF32>
+__global__ void __launch_bounds__(kBatchThreads, 2)
+batch_logits_kernel(const SampleArgs a, int i) {
+    extern __shared__ __align__(16) uint16_t e_smem[];      // [64][RANK + kBPad]
+    __shared__ unsigned long long s_best[kGroupRows];
+    __shared__ float s_T[kGroupRows];
+    __shared__ int s_resc[kGroupRows];
+    __shared__ unsigned int s_vmin;
+    __shared__ int s_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int blk = blockIdx.x, nblk = gridDim.x;
+    const int row0 = blockIdx.y * kGroupRows;
+    const int V = a.V;
+    int v_begin, v_end;
+    block_range(V, nblk, blk, v_begin, v_end);
+    pdl_trigger();
+    {
+        // input side only: this block's head rows (kept in L2 across
+        // positions) and its base-logit rows of position i into L2
+        const char *hp = reinterpret_cast<const char *>(a.head + (int64_t)v_begin * RANK);
+        const int hlines = (v_end - v_begin) * RANK * 2 / 128;
+        for (int l = tid; l < hlines; l += kBatchThreads)
+            asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(hp + (int64_t)l * 128));
+        constexpr int esz = kBaseF32 ? 4 : 2;
+        const char *bp = kBaseF32 ? reinterpret_cast<const char *>(a.base_f)
+                                  : reinterpret_cast<const char *>(a.base);
+        const int lines = ((v_end - v_begin) * esz + 127) / 128 + 1;
+        for (int idx = tid; idx < kGroupRows * lines; idx += kBatchThreads) {
+            const int b = idx / lines, l = idx - b * lines;
+            if (!row_live(a, row0 + b)) continue;
+            const int64_t o0 = (row0 + b) * a.base_s0 + (int64_t)i * a.base_s1 + v_begin;
+            const char *q = bp + o0 * esz + (int64_t)l * 128;
+            if (q < bp + (o0 + (v_end - v_begin)) * esz)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+        }
+    }
+    pdl_wait();
+
+    for (int idx = tid; idx < kGroupRows * (RANK / 8); idx += kBatchThreads) {
+        int b = idx / (RANK / 8), c = idx % (RANK / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row_live(a, row0 + b)) {
+            int64_t p = prev_token(a, row0 + b, i);
+            if (p >= 0 && p < V) v = *reinterpret_cast<const uint4 *>(a.embed + p * RANK + 8 * c);
+        }
+        *reinterpret_cast<uint4 *>(e_smem + b * (RANK + kBPad) + 8 * c) = v;
+    }
+    if (tid < kGroupRows) {
+        s_best[tid] = 0ull;
+        s_T[tid] = row0 + tid < a.rows ? a.temperature[row0 + tid] : 0.0f;
+    }
+    if (tid == 0) s_vmin = 0xffffffffu;
+    uint32_t live = 0u;
 #pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                if (lane >= o2) incl += y;
-            }
-            if (lane == 31) s_scan[warp] = incl;
-            __syncthreads();
-            uint64_t wpre = 0ull;
-            for (int w = 0; w < warp; ++w) wpre += s_scan[w];
-            uint64_t run = s_blkpre + wpre + incl - mine;
-            if (run <= target && target < run + mine) {
-                for (int v = c0; v < c1; ++v) {
-                    float x = __fdiv_rn(cache_value(a, b, i, v), T);
-                    run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-                    if (run > target) {
-                        s_tok = v;
-                        break;
+    for (int q = 0; q < 2 * kMT; ++q)
+        if (row_live(a, row0 + 16 * (q >> 1) + 8 * (q & 1) + g)) live |= 1u << q;
+    __syncthreads();
+
+    uint64_t best[kMT][2];
+#pragma unroll
+    for (int m = 0; m < kMT; ++m) best[m][0] = best[m][1] = 0ull;
+    const int nm = min(kMT, (a.rows - row0 + 15) / 16);
+    const uint64_t keep = policy_evict_last(), once = policy_evict_first();
+    const bool cache_f32 = a.cache_f != nullptr;
+    // paired base loads need the pair's alignment
+    const bool vec = ((reinterpret_cast<uintptr_t>(kBaseF32 ? (const void *)a.base_f
+                                                             : (const void *)a.base) &
+                       (kBaseF32 ? 7u : 3u)) == 0u) &&
+                     ((a.base_s0 | a.base_s1) & 1) == 0;
+    // the key of a row is its logit except for Gumbel rows that sample
+    // (inverse-CDF rows divide their maximum by T once, at the end)
+    uint32_t divides = 0u;
+    if (a.mode == 0) {
+#pragma unroll
+        for (int q = 0; q < 2 * kMT; ++q)
+            if (samples(s_T[16 * (q >> 1) + 8 * (q & 1) + g])) divides |= 1u << q;
+    }
+
+    for (int v0 = v_begin + warp * kTile; v0 < v_end; v0 += kBW * kTile) {
+        // this tile's base logits first: their latency overlaps the MMAs
+        using BaseT = typename std::conditional<kBaseF32, float2, uint32_t>::type;
+        BaseT bv[kMT][2][2];
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const int q = 2 * m + h;
+                    const int64_t o = (row0 + 16 * m + 8 * h + g) * a.base_s0 +
+                                      (int64_t)i * a.base_s1 + v0 + 8 * n + 2 * t;
+                    if constexpr (kBaseF32) {
+                        bv[m][h][n] = make_float2(0.0f, 0.0f);
+                        if (m < nm && ((live >> q) & 1u))
+                            bv[m][h][n] = vec ? ld_nc_f2(a.base_f + o, once)
+                                              : make_float2(__ldg(a.base_f + o),
+                                                            __ldg(a.base_f + o + 1));
+                    } else {
+                        bv[m][h][n] = 0u;
+                        if (m < nm && ((live >> q) & 1u))
+                            bv[m][h][n] = vec ? ld_nc_u32(a.base + o, once)
+                                              : ((uint32_t)__ldg(a.base + o) |
+                                                 ((uint32_t)__ldg(a.base + o + 1) << 16));
                     }
                 }
+
+        float acc[kMT][2][4];
+#pragma unroll
+        for (int m = 0; m < kMT; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.0f;
+        const uint16_t *h0 = a.head + (int64_t)(v0 + g) * RANK + 8 * t;
+        const uint16_t *h1 = h0 + 8 * RANK;
+        // head fragments two k-chunks ahead of the MMAs that use them
+        uint4 hx[2], hy[2];
+        hx[0] = ld_nc_v4(h0, keep);
+        hy[0] = ld_nc_v4(h1, keep);
+        hx[1] = ld_nc_v4(h0 + 32, keep);
+        hy[1] = ld_nc_v4(h1 + 32, keep);
+#pragma unroll
+        for (int j = 0; j < RANK / 32; ++j) {
+            const uint4 x = hx[j & 1], y = hy[j & 1];
+            if (j + 2 < RANK / 32) {
+                hx[j & 1] = ld_nc_v4(h0 + 32 * (j + 2), keep);
+                hy[j & 1] = ld_nc_v4(h1 + 32 * (j + 2), keep);
             }
-            __syncthreads();
-            tok = s_tok;
-            if (tok < 0) {
-                if (tid == 0) set_status(a.status, 6u /* MARKOV_EDEVICE */, 0x200u + i);
-                tok = 0;
+#pragma unroll
+            for (int m = 0; m < kMT; ++m) {
+                if (m >= nm) break;
+                const uint16_t *er = e_smem + (16 * m + g) * (RANK + kBPad) + 8 * t + 32 * j;
+                const uint4 ea = *reinterpret_cast<const uint4 *>(er);
+                const uint4 eb = *reinterpret_cast<const uint4 *>(er + 8 * (RANK + kBPad));
+                mma16816(acc[m][0], ea.x, eb.x, ea.y, eb.y, x.x, x.y);
+                mma16816(acc[m][1], ea.x, eb.x, ea.y, eb.y, y.x, y.y);
+                mma16816(acc[m][0], ea.z, eb.z, ea.w, eb.w, x.z, x.w);
+                mma16816(acc[m][1], ea.z, eb.z, ea.w, eb.w, y.z, y.w);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kMT; ++m) {
+            if (m >= nm) break;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = 2 * m + h;
+                if (!((live >> q) & 1u)) continue;
+                const int rr = 16 * m + 8 * h + g;
+                const int row = row0 + rr;
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const int v = v0 + 8 * n + 2 * t;
+                    // bias = bf16(sum); s = f32(base) + f32(bias)
+                    const uint32_t bb = bf16x2_rn(acc[m][n][2 * h], acc[m][n][2 * h + 1]);
+                    float b0, b1;
+                    if constexpr (kBaseF32) {
+                        b0 = bv[m][h][n].x;
+                        b1 = bv[m][h][n].y;
+                    } else {
+                        b0 = __uint_as_float(bv[m][h][n] << 16);
+                        b1 = __uint_as_float(bv[m][h][n] & 0xffff0000u);
+                    }
+                    float l0 = __fadd_rn(b0, __uint_as_float(bb << 16));
+                    float l1 = __fadd_rn(b1, __uint_as_float(bb & 0xffff0000u));
+                    const int64_t co = row * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
+                    if (cache_f32) {
+                        if (a.tf.has_transform) {
+                            l0 = transform_one_f32(l0, a.tf);
+                            l1 = transform_one_f32(l1, a.tf);
+                        }
+                        st_f2(a.cache_f + co, make_float2(l0, l1), once);
+                    } else {
+                        uint32_t lp = bf16x2_rn(l0, l1);
+                        if (a.tf.has_transform) lp = transform_two_bf16(lp, a.tf);
+                        st_u32(a.cache + co, lp, once);
+                        l0 = __uint_as_float(lp << 16);
+                        l1 = __uint_as_float(lp & 0xffff0000u);
+                    }
+                    float k0 = l0, k1 = l1;
+                    if ((divides >> q) & 1u) {
+                        const float T = s_T[rr];
+                        const float2 gn = *reinterpret_cast<const float2 *>(
+                            a.noise + (int64_t)(row * a.N + i) * a.noise_s0 + v);
+                        k0 = __fadd_rn(__fdiv_rn(l0, T), gn.x);
+                        k1 = __fadd_rn(__fdiv_rn(l1, T), gn.y);
+                    }
+                    const uint64_t p0 = pack_key(k0, (uint32_t)v);
+                    const uint64_t p1 = pack_key(k1, (uint32_t)v + 1u);
+                    const uint64_t pm = p0 > p1 ? p0 : p1;
+                    best[m][h] = pm > best[m][h] ? pm : best[m][h];
+                }
             }
         }
     }
-    if (tid == 0) a.tokens[b * a.tok_s0 + i] = tok;
+#pragma unroll
+    for (int m = 0; m < kMT; ++m) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint64_t v = best[m][h];
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+                v = w > v ? w : v;
+            }
+            if (t == 0 && v) atomicMax(&s_best[16 * m + 8 * h + g], (unsigned long long)v);
+        }
+    }
+    __syncthreads();
+    // inverse-CDF rows that sample: the block's key is fl(max l / T), which
+    // is max fl(l / T) since rounding is monotone; only the id of a +inf
+    // key needs the exact keys (their lowest id), so such rows rescan
+    bool resc = false;
+    if (tid < kGroupRows) {
+        const uint64_t bw = s_best[tid];
+        const float T = s_T[tid];
+        if (a.mode == 1 && bw != 0ull && samples(T)) {
+            const uint32_t o = packed_ordered(bw);
+            if (o != 0xffffffffu) {
+                const float k = __fdiv_rn(key_from_ordered(o), T);
+                if (k == __uint_as_float(0x7f800000u))
+                    resc = true;
+                else
+                    s_best[tid] = pack_key(k, packed_id(bw));
+            }
+        }
+        s_resc[tid] = resc;
+    }
+    if (__syncthreads_or(resc)) {
+        // rare: the lowest id of this block whose key fl(l / T) is +inf
+        for (int rr = 0; rr < kGroupRows; ++rr) {
+            if (!s_resc[rr]) continue;
+            const float T = s_T[rr];
+            for (int v = v_begin + tid; v < v_end; v += kBatchThreads) {
+                if (__fdiv_rn(cache_value(a, row0 + rr, i, v), T) == __uint_as_float(0x7f800000u)) {
+                    atomicMin(&s_vmin, (unsigned int)v);
+                    break;
+                }
+            }
+            __syncthreads();
+            if (tid == 0) {
+                s_best[rr] = pack_key(__uint_as_float(0x7f800000u), s_vmin);
+                s_vmin = 0xffffffffu;
+            }
+            __syncthreads();
+        }
+    }
+    // the block's best per row into the row's winner word
+    if (tid < kGroupRows && s_best[tid]) atomicMax(win_slot(a, i, row0 + tid), s_best[tid]);
+    if (!last_block(group_counter(a, i, blockIdx.y), (uint32_t)nblk, &s_flag)) return;
+
+    // last block of the row group: every block's maximum is in
+    if (tid == 0) *group_counter(a, i, blockIdx.y) = 0u;
+    const int b = row0 + tid;
+    if (tid < kGroupRows && row_live(a, b)) {
+        unsigned long long *ws = win_slot(a, i, b);
+        const uint64_t win = __ldcg(ws);
+        const float T = s_T[tid];
+        if (a.mode == 0 || !samples(T) || !needs_sums(win)) {
+            a.tokens[b * a.tok_s0 + i] = direct_token(a, win, T);
+            *ws = 0ull;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kBatchThreads)
+batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
+    __shared__ unsigned long long s_w[kBW];
+    __shared__ unsigned long long s_blkpre, s_target;
+    __shared__ long long s_tok;
+    __shared__ int s_blk, s_flag;
+    const int b = blockIdx.y, c = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();
+    if (!row_live(a, b)) return;
+    const float T = a.temperature[b];
+    if (!samples(T)) return;
+    unsigned long long *ws = win_slot(a, i, b);
+    const uint64_t win = __ldcg(ws);
+    if (win == 0ull) return;                  // the logits kernel decided the row
+    const float M = key_from_ordered(packed_ordered(win));
+
+    // this block's weight sum (ids strided over the threads: coalesced reads)
+    const int v0 = c * kCdfIds, v1 = min(a.V, v0 + kCdfIds);
+    uint64_t part = 0ull;
+    for (int v = v0 + tid; v < v1; v += kBatchThreads) part += cdf_weight(a, b, i, v, T, M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0) s_w[warp] = part;
+    __syncthreads();
+    if (tid == 0) {
+        uint64_t sum = 0ull;
+        for (int w = 0; w < kBW; ++w) sum += s_w[w];
+        a.sums[(int64_t)b * nb2 + c] = sum;
+    }
+    if (!last_block(row_counter(a, i, b), (uint32_t)nb2, &s_flag)) return;
+
+    // last block of the row: the block whose prefix range holds the target
+    if (tid == 0) {
+        *row_counter(a, i, b) = 0u;
+        s_tok = -1;
+    }
+    if (warp == 0) {
+        const unsigned long long *sums =
+            reinterpret_cast<const unsigned long long *>(a.sums + (int64_t)b * nb2);
+        const uint64_t x0 = 2 * lane < nb2 ? __ldcg(sums + 2 * lane) : 0ull;
+        const uint64_t x1 = 2 * lane + 1 < nb2 ? __ldcg(sums + 2 * lane + 1) : 0ull;
+        uint64_t incl = x0 + x1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint64_t S = __shfl_sync(0xffffffffu, incl, 31);
+        const uint64_t excl = incl - x0 - x1;
+        const uint64_t H =
+            dm_cdf_hash(dm_row_step_hash((uint64_t)a.seeds[b], (uint32_t)b, (uint32_t)i));
+        const uint64_t target = __umul64hi(H, S);
+        int hit = -1;
+        uint64_t hitpre = 0ull;
+        if (x0 && excl <= target && target < excl + x0) {
+            hit = 2 * lane;
+            hitpre = excl;
+        } else if (x1 && excl + x0 <= target && target < excl + x0 + x1) {
+            hit = 2 * lane + 1;
+            hitpre = excl + x0;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+        const int src = m ? __ffs(m) - 1 : 0;
+        const int cb = __shfl_sync(0xffffffffu, hit, src);
+        const uint64_t pre = __shfl_sync(0xffffffffu, hitpre, src);
+        if (lane == 0) {
+            s_blk = m ? cb : -1;
+            s_blkpre = pre;
+            s_target = target;
+        }
+    }
+    __syncthreads();
+    const int cb = s_blk;
+    if (cb >= 0) {
+        // scan the target block: 16 consecutive ids per thread, in vocab order
+        const uint64_t target = s_target;
+        const int w0 = cb * kCdfIds, w1 = min(a.V, w0 + kCdfIds);
+        const int c0 = w0 + tid * 16, c1 = min(c0 + 16, w1);
+        uint64_t mine = 0ull;
+        for (int v = c0; v < c1; ++v) mine += cdf_weight(a, b, i, v, T, M);
+        uint64_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_w[warp] = incl;
+        __syncthreads();
+        uint64_t wpre = 0ull;
+        for (int w = 0; w < warp; ++w) wpre += s_w[w];
+        uint64_t run = s_blkpre + wpre + incl - mine;
+        if (mine && run <= target && target < run + mine) {
+            for (int v = c0; v < c1; ++v) {
+                run += cdf_weight(a, b, i, v, T, M);
+                if (run > target) {
+                    s_tok = v;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int64_t tok = s_tok;
+        if (tok < 0) {
+            set_status(a.status, 6u /* MARKOV_EDEVICE */, 0x200u + i);
+            tok = 0;
+        }
+        a.tokens[b * a.tok_s0 + i] = tok;
+        *ws = 0ull;
+    }
 }
 
 int batch_blocks(int V) {
@@ -288,31 +581,57 @@ int batch_blocks(int V) {
     return nblk;
 }
 
+// One launch of the path; pdl: as a programmatic dependent of the launch
+// before it on the stream.
+template <typename... Params, typename... Args>
+static cudaError_t launch_one(void (*kernel)(Params...), dim3 grid, size_t smem,
+                              cudaStream_t stream, bool pdl, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kBatchThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches) {
-    const int nblk = a.grid;
     const int groups = (a.rows + kGroupRows - 1) / kGroupRows;
+    // one wave: the plan's vocab blocks shared out over the row groups
+    const int nblk = a.grid / groups > 0 ? a.grid / groups : 1;
+    const int nb2 = (a.V + kCdfIds - 1) / kCdfIds;
     const size_t smem = (size_t)kGroupRows * (a.r + kBPad) * sizeof(uint16_t);
+    *launches = 0;
+    if (nb2 > 64 || a.rows > kMaxRows || a.N > kMaxSteps) return cudaErrorInvalidValue;
+    void (*logits)(const SampleArgs, int);
+    const bool bf = a.base_f != nullptr;
+    switch (a.r) {
+        case 64: logits = bf ? batch_logits_kernel<64, true> : batch_logits_kernel<64, false>; break;
+        case 128:
+            logits = bf ? batch_logits_kernel<128, true> : batch_logits_kernel<128, false>;
+            break;
+        case 256:
+            logits = bf ? batch_logits_kernel<256, true> : batch_logits_kernel<256, false>;
+            break;
+        default: return cudaErrorInvalidValue;
+    }
     int n = 0;
-    for (int i = 0; i < a.N; ++i) {
-        dim3 grid(nblk, groups);
-        switch (a.r) {
-            case 64: batch_logits_kernel<64><<<grid, kBatchThreads, smem, stream>>>(a, i); break;
-            case 128: batch_logits_kernel<128><<<grid, kBatchThreads, smem, stream>>>(a, i); break;
-            case 256: batch_logits_kernel<256><<<grid, kBatchThreads, smem, stream>>>(a, i); break;
-            default: return cudaErrorInvalidValue;
-        }
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < a.N && e == cudaSuccess; ++i) {
+        // the first launch of a call waits for the stream as usual
+        e = launch_one(logits, dim3(nblk, groups), smem, stream, i > 0, a, i);
         ++n;
-        if (a.mode == 1) {
-            batch_cdfsum_kernel<<<dim3(nblk, a.rows), kBatchThreads, 0, stream>>>(a, i, nblk);
+        if (e == cudaSuccess && a.mode == 1) {
+            e = launch_one(batch_cdf_kernel, dim3(nb2, a.rows), 0, stream, true, a, i, nb2);
             ++n;
         }
-        batch_pick_kernel<<<a.rows, kBatchThreads, 0, stream>>>(a, i, nblk);
-        ++n;
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
     *launches = n;
-    return cudaSuccess;
+    return e;
 }
 
 }  // namespace dtm

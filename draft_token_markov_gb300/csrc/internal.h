@@ -20,6 +20,14 @@ constexpr int kLineU64 = 16;           // one 128-byte line per exchange word
 constexpr int kLineU32 = 32;
 constexpr size_t kWinMaxN = (size_t)2 * kMaxSteps * kChainRows * kLineU64;
 constexpr size_t kWinCntN = (size_t)2 * kMaxSteps * kLineU32;
+// per-position path: a winner word per (position, row) and, per position,
+// a done counter per 64-row group (logits kernel) and per row (inverse-CDF
+// sum kernel)
+constexpr int kBatchGroupRows = 32;
+constexpr int kBatchCntPerStep = kMaxRows / kBatchGroupRows + kMaxRows;
+constexpr size_t kBatchWinN = (size_t)kMaxSteps * kMaxRows;
+constexpr size_t kBatchCntN = (size_t)kMaxSteps * kBatchCntPerStep;
+constexpr int kCdfIds = kBatchThreads * 16;   // vocab ids per inverse-CDF sum block
 
 // The output-logit transform (muse_spark markov page, FusedMarkovParams):
 // multiplier and cap rounded to fp32, inv_cap = fp32(1) / fp32(cap).
@@ -47,9 +55,9 @@ struct SampleArgs {
     int64_t tok_s0;
     uint16_t *cache;
     int64_t cache_s0, cache_s1;
-    // fp32 variants (the simple chain and the batch path): when set, the
-    // base logits / the cache are fp32 at these pointers (same strides, in
-    // elements) and base / cache are unused
+    // fp32 variants (every path): when set, the base logits / the cache are
+    // fp32 at these pointers (same strides, in elements) and base / cache are
+    // unused
     const float *base_f;
     float *cache_f;
     float *noise;              // [rows * N, V] fp32 Gumbel noise (Gumbel mode)
@@ -66,6 +74,8 @@ struct SampleArgs {
     uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
     uint64_t *win_max;         // [2 call parities][N][8 rows] x kLineU64: red.max words
+    uint64_t *bwin;            // [kMaxSteps][kMaxRows] per-position path winners (0: none)
+    uint32_t *bcnt;            // [kMaxSteps][kBatchCntPerStep] its done counters
     uint32_t *win_cnt;         // [2 call parities][N] x kLineU32: CTAs that reported
     uint64_t timeout_ns;
     int grid;                  // persistent grid size (chain) or vocab blocks (batch)

@@ -36,6 +36,11 @@ struct markov_plan {
     uint64_t *tok_slots = nullptr;
     uint64_t *win_max = nullptr;
     uint32_t *win_cnt = nullptr;
+    // the per-position path's winner words and done counters; every call
+    // leaves them zero, except one whose launches failed part way
+    uint64_t *bwin = nullptr;
+    uint32_t *bcnt = nullptr;
+    bool batch_dirty = false;
     size_t tc_slots_n = 0;
     size_t tc_keys_n = 0;         // tc_slots_n * kTcReplicas
     CUtensorMap tmap;
@@ -78,6 +83,8 @@ void free_plan(markov_plan *p) {
     if (p->ctrl) cudaFree(p->ctrl);
     if (p->tc_keys) cudaFree(p->tc_keys);
     if (p->tc_sums) cudaFree(p->tc_sums);
+    if (p->bwin) cudaFree(p->bwin);
+    if (p->bcnt) cudaFree(p->bcnt);
     if (p->sum_tags) cudaFree(p->sum_tags);
     if (p->tok_slots) cudaFree(p->tok_slots);
     if (p->win_max) cudaFree(p->win_max);
@@ -214,6 +221,10 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMalloc(&p->win_cnt, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&p->bwin, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->bcnt, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->bwin, 0, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->bcnt, 0, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
@@ -377,6 +388,8 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
     a.tok_slots = p->tok_slots;
     a.win_max = p->win_max;
     a.win_cnt = p->win_cnt;
+    a.bwin = p->bwin;
+    a.bcnt = p->bcnt;
     a.timeout_ns = (uint64_t)p->d.timeout_ms * 1000000ull;
 
     if (use_tc && p->tmap_head != head) {
@@ -415,9 +428,16 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
         p->last_path = MARKOV_PATH_CHAIN_SIMPLE;
     } else {
         a.grid = p->batch_grid;
+        if (p->batch_dirty) {
+            // an earlier call's launches failed part way: start from cleared slots
+            if (cudaMemsetAsync(p->bwin, 0, kBatchWinN * sizeof(uint64_t), s) != cudaSuccess ||
+                cudaMemsetAsync(p->bcnt, 0, kBatchCntN * sizeof(uint32_t), s) != cudaSuccess)
+                return MARKOV_ECUDA;
+            p->batch_dirty = false;
+        }
         int n = 0;
         cudaError_t e = launch_batch(a, s, &n);
-        if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+        if (e != cudaSuccess) { cudaGetLastError(); p->batch_dirty = true; return MARKOV_ECUDA; }
         launches += n;
         p->last_path = MARKOV_PATH_BATCH;
     }
@@ -441,7 +461,9 @@ markov_status markov_plan_status(markov_plan *p) {
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess)
+        cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->bwin, 0, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->bcnt, 0, kBatchCntN * sizeof(uint32_t)) != cudaSuccess)
         return MARKOV_ECUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MARKOV_ECUDA;
     return (markov_status)ctrl[2];

@@ -54,6 +54,29 @@ def test_batch_rows_parity(gpu_lib, w):
     assert rep.ok(), rep.summary()
 
 
+def test_batch_calls_share_one_plan(gpu_lib):
+    # the per-position path keeps per-row winner words and done counters in
+    # the plan; each call must leave them cleared for the next, whatever its
+    # row count or mode
+    V, r = 4096, 128
+    plan = gpu_lib.Plan(V, r, 4, 70)
+    try:
+        for k, (rows, mode) in enumerate([(70, W.INVCDF), (20, W.GUMBEL), (70, W.GUMBEL),
+                                          (33, W.INVCDF), (70, W.INVCDF)]):
+            w = W.small(V, r, rows, 4, mode, seed=60 + k, padding_rows=(1,),
+                        temperatures=(0.0, 0.7, 1.0))
+            inp = W.make_call(w)
+            toks, cache = U.run(gpu_lib, w, inp, BATCH, plan=plan)
+            assert plan.query(gpu_lib.Q_LAST_PATH) == BATCH
+            # inverse CDF: logits + sum kernels per position; Gumbel: the noise
+            # kernel, then one logits kernel per position
+            assert plan.query(gpu_lib.Q_LAST_LAUNCHES) == (8 if mode == W.INVCDF else 1 + 4)
+            rep = U.check(w, inp, toks, cache)
+            assert rep.ok(), (k, rep.summary())
+    finally:
+        plan.close()
+
+
 def test_forced_chain_refuses_large_batch(gpu_lib):
     w = BATCHES[0]
     plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
