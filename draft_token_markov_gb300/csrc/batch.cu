@@ -152,6 +152,15 @@ __device__ __forceinline__ bool needs_sums(uint64_t win) {
            M != __uint_as_float(0xff800000u);
 }
 
+// ordered_key in fewer instructions: -0 is first made +0 (x + 0 rounds it
+// so), then negative keys flip all bits and others the sign bit; any NaN
+// maps above all.
+__device__ __forceinline__ uint32_t ordered_canonical(float k) {
+    const uint32_t b = __float_as_uint(__fadd_rn(k, 0.0f));
+    const uint32_t o = b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+    return (b & 0x7fffffffu) > 0x7f800000u ? 0xffffffffu : o;
+}
+
 // The token of a row that its winner decides without weight sums.
 __device__ __forceinline__ int64_t direct_token(const SampleArgs &a, uint64_t win, float T) {
     int64_t tok = (int64_t)packed_id(win);
@@ -181,10 +190,28 @@ __device__ __noinline__ uint32_t transform_two_bf16(uint32_t lp, const Transform
 }
 
 // Integer inverse-CDF weight floor(exp(x / T - M) 2^40) of cached logit x.
-__device__ __forceinline__ uint64_t cdf_weight(const SampleArgs &a, int b, int i, int v, float T,
-                                               float M) {
-    const float x = __fdiv_rn(cache_value(a, b, i, v), T);
-    return (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+__device__ __forceinline__ uint64_t cdf_weight_of(float x, float T, float M) {
+    return (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(__fdiv_rn(x, T), M)), 0x1p40f));
+}
+
+// Eight consecutive cached logits (row b, position i, ids v .. v + 7, v a
+// multiple of 8: the cache's 16-byte alignment holds) as fp32.
+__device__ __forceinline__ void cache8(const SampleArgs &a, int b, int i, int v, float (&x)[8]) {
+    const int64_t o = b * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
+    if (a.cache_f) {
+        const float4 p = __ldg(reinterpret_cast<const float4 *>(a.cache_f + o));
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(a.cache_f + o + 4));
+        x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
+        x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
+    } else {
+        const uint4 p = __ldg(reinterpret_cast<const uint4 *>(a.cache + o));
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
 }
 
 }  // namespace
@@ -254,9 +281,12 @@ batch_logits_kernel(const SampleArgs a, int i) {
         if (row_live(a, row0 + 16 * (q >> 1) + 8 * (q & 1) + g)) live |= 1u << q;
     __syncthreads();
 
-    uint64_t best[kMT][2];
+    // per row of this thread: the best ordered key so far and its id (ids
+    // are visited in increasing order, so a strict comparison keeps the
+    // lowest id of equal keys); ordered key 0 is below every real key
+    uint32_t bo[kMT][2], bi[kMT][2];
 #pragma unroll
-    for (int m = 0; m < kMT; ++m) best[m][0] = best[m][1] = 0ull;
+    for (int m = 0; m < kMT; ++m) bo[m][0] = bo[m][1] = bi[m][0] = bi[m][1] = 0u;
     const int nm = min(kMT, (a.rows - row0 + 15) / 16);
     const uint64_t keep = policy_evict_last(), once = policy_evict_first();
     const bool cache_f32 = a.cache_f != nullptr;
@@ -380,10 +410,15 @@ batch_logits_kernel(const SampleArgs a, int i) {
                         k0 = __fadd_rn(__fdiv_rn(l0, T), gn.x);
                         k1 = __fadd_rn(__fdiv_rn(l1, T), gn.y);
                     }
-                    const uint64_t p0 = pack_key(k0, (uint32_t)v);
-                    const uint64_t p1 = pack_key(k1, (uint32_t)v + 1u);
-                    const uint64_t pm = p0 > p1 ? p0 : p1;
-                    best[m][h] = pm > best[m][h] ? pm : best[m][h];
+                    const uint32_t o0 = ordered_canonical(k0), o1 = ordered_canonical(k1);
+                    if (o0 > bo[m][h]) {
+                        bo[m][h] = o0;
+                        bi[m][h] = (uint32_t)v;
+                    }
+                    if (o1 > bo[m][h]) {
+                        bo[m][h] = o1;
+                        bi[m][h] = (uint32_t)v + 1u;
+                    }
                 }
             }
         }
@@ -392,7 +427,8 @@ batch_logits_kernel(const SampleArgs a, int i) {
     for (int m = 0; m < kMT; ++m) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            uint64_t v = best[m][h];
+            uint64_t v = bo[m][h] ? ((uint64_t)bo[m][h] << 32) | (uint64_t)(0xffffffffu - bi[m][h])
+                                  : 0ull;
 #pragma unroll
             for (int o = 1; o < 4; o <<= 1) {
                 uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
@@ -476,10 +512,25 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
     if (win == 0ull) return;                  // the logits kernel decided the row
     const float M = key_from_ordered(packed_ordered(win));
 
-    // this block's weight sum (ids strided over the threads: coalesced reads)
+    // this block's weight sum: 8 consecutive ids per 16-byte load, both
+    // loads issued before any weight (consecutive threads, consecutive ids)
     const int v0 = c * kCdfIds, v1 = min(a.V, v0 + kCdfIds);
+    constexpr int kU = kCdfIds / (8 * kBatchThreads);
+    float x[kU][8];
+    bool ok[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int vv = v0 + (u * kBatchThreads + tid) * 8;
+        ok[u] = vv < v1;
+        if (ok[u]) cache8(a, b, i, vv, x[u]);
+    }
     uint64_t part = 0ull;
-    for (int v = v0 + tid; v < v1; v += kBatchThreads) part += cdf_weight(a, b, i, v, T, M);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        if (ok[u]) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part += cdf_weight_of(x[u][e], T, M);
+        }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
     if (lane == 0) s_w[warp] = part;
@@ -537,9 +588,21 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
         // scan the target block: 16 consecutive ids per thread, in vocab order
         const uint64_t target = s_target;
         const int w0 = cb * kCdfIds, w1 = min(a.V, w0 + kCdfIds);
-        const int c0 = w0 + tid * 16, c1 = min(c0 + 16, w1);
+        const int c0 = w0 + tid * 16;
+        float y[2][8];
+        bool oky[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            oky[u] = c0 + 8 * u < w1;
+            if (oky[u]) cache8(a, b, i, c0 + 8 * u, y[u]);
+        }
         uint64_t mine = 0ull;
-        for (int v = c0; v < c1; ++v) mine += cdf_weight(a, b, i, v, T, M);
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (oky[u]) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mine += cdf_weight_of(y[u][e], T, M);
+            }
         uint64_t incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -552,13 +615,13 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
         for (int w = 0; w < warp; ++w) wpre += s_w[w];
         uint64_t run = s_blkpre + wpre + incl - mine;
         if (mine && run <= target && target < run + mine) {
-            for (int v = c0; v < c1; ++v) {
-                run += cdf_weight(a, b, i, v, T, M);
-                if (run > target) {
-                    s_tok = v;
-                    break;
-                }
+            int hit = -1;
+            for (int k = 0; k < 16 && hit < 0; ++k) {
+                if (!oky[k >> 3]) break;
+                run += cdf_weight_of(y[k >> 3][k & 7], T, M);
+                if (run > target) hit = k;
             }
+            if (hit >= 0) s_tok = c0 + hit;
         }
     }
     __syncthreads();
