@@ -239,6 +239,11 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     cfg = WORKLOADS[args.workload]
     w = W.CONFIGS[cfg]
+    if args.rows:
+        # the workload with another row count (its padding rows below it kept)
+        w = w.with_(rows=args.rows, padding_rows=tuple(b for b in w.padding_rows
+                                                        if b < args.rows),
+                    name=f"{w.name} at rows={args.rows}")
     base_f32, cache_f32 = args.base_dtype == "f32", args.cache_dtype == "f32"
     head, embed = W.make_weights(w)
     inp = W.make_call(w, base_f32=base_f32)
@@ -397,6 +402,8 @@ def main():
                     help="element type of the base logits")
     ap.add_argument("--cache-dtype", default="bf16", choices=["bf16", "f32"],
                     help="element type of the logits cache")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="run the workload with this many rows instead of its own")
     ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOADS),
                     help="deepseek (default, the headline): V=129280 r=256 8 rows N=8; "
                          "latency: 1 row; softcap: V=262144 r=128 inverse CDF; batch: 64 rows "
