@@ -39,8 +39,6 @@ namespace dtm {
 namespace {
 
 constexpr int kBW = kBatchThreads / 32;    // warps per block
-constexpr int kGroupRows = kBatchGroupRows;  // rows per row group
-constexpr int kMT = kGroupRows / 16;         // MMA M-tiles (16 rows) per row group
 constexpr int kBPad = 32;
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -124,7 +122,7 @@ __device__ __forceinline__ uint32_t *group_counter(const SampleArgs &a, int i, i
     return a.bcnt + (size_t)i * kBatchCntPerStep + grp;
 }
 __device__ __forceinline__ uint32_t *row_counter(const SampleArgs &a, int i, int b) {
-    return a.bcnt + (size_t)i * kBatchCntPerStep + kMaxRows / kGroupRows + b;
+    return a.bcnt + (size_t)i * kBatchCntPerStep + kMaxRows / 16 + b;
 }
 
 // Whether this block is the last of `total` blocks to pass `counter`.  Every
@@ -216,15 +214,23 @@ __device__ __forceinline__ void cache8(const SampleArgs &a, int b, int i, int v,
 
 }  // namespace
 
-// The logits kernel of position i.  MMA roles: M = 16 rows (the previous
+// The logits kernel of position i, for row groups of 16 MT rows.  MMA
+// roles: M = 16 rows (the previous
 // tokens' embeddings, staged in shared memory), N = 8 vocab ids (head rows,
 // read from global), K = rank, so that each thread's accumulators hold pairs
 // of consecutive ids of one row: base logits are read and cache entries
 // written two ids at a time.  Rows of a thread: row0 + 16 m + 8 h + g for
-// M-tile m < kMT and half h < 2 (bit 2 m + h of `live`).
-template <int RANK, bool kBaseF32>
+// M-tile m < MT and half h < 2 (bit 2 m + h of `live`).  The head fragments
+// of a tile are fetched kDepth k-chunks ahead of their MMAs: the whole tile
+// at once for 16-row groups (few accumulators leave the registers for it),
+// two chunks for 32-row groups.
+template <int RANK, bool kBaseF32, int MT>
 __global__ void __launch_bounds__(kBatchThreads, 2)
 batch_logits_kernel(const SampleArgs a, int i) {
+    constexpr int kGroupRows = 16 * MT;
+    constexpr int kMT = MT;
+    constexpr int kChunks = RANK / 32;
+    constexpr int kDepth = MT == 1 ? kChunks : 2;
     extern __shared__ __align__(16) uint16_t e_smem[];      // [64][RANK + kBPad]
     __shared__ unsigned long long s_best[kGroupRows];
     __shared__ float s_T[kGroupRows];
@@ -339,18 +345,19 @@ batch_logits_kernel(const SampleArgs a, int i) {
             for (int n = 0; n < 2; ++n) acc[m][n][0] = acc[m][n][1] = acc[m][n][2] = acc[m][n][3] = 0.0f;
         const uint16_t *h0 = a.head + (int64_t)(v0 + g) * RANK + 8 * t;
         const uint16_t *h1 = h0 + 8 * RANK;
-        // head fragments two k-chunks ahead of the MMAs that use them
-        uint4 hx[2], hy[2];
-        hx[0] = ld_nc_v4(h0, keep);
-        hy[0] = ld_nc_v4(h1, keep);
-        hx[1] = ld_nc_v4(h0 + 32, keep);
-        hy[1] = ld_nc_v4(h1 + 32, keep);
+        // head fragments kDepth k-chunks ahead of the MMAs that use them
+        uint4 hx[kDepth], hy[kDepth];
 #pragma unroll
-        for (int j = 0; j < RANK / 32; ++j) {
-            const uint4 x = hx[j & 1], y = hy[j & 1];
-            if (j + 2 < RANK / 32) {
-                hx[j & 1] = ld_nc_v4(h0 + 32 * (j + 2), keep);
-                hy[j & 1] = ld_nc_v4(h1 + 32 * (j + 2), keep);
+        for (int d = 0; d < kDepth; ++d) {
+            hx[d] = ld_nc_v4(h0 + 32 * d, keep);
+            hy[d] = ld_nc_v4(h1 + 32 * d, keep);
+        }
+#pragma unroll
+        for (int j = 0; j < kChunks; ++j) {
+            const uint4 x = hx[j % kDepth], y = hy[j % kDepth];
+            if (j + kDepth < kChunks) {
+                hx[j % kDepth] = ld_nc_v4(h0 + 32 * (j + kDepth), keep);
+                hy[j % kDepth] = ld_nc_v4(h1 + 32 * (j + kDepth), keep);
             }
 #pragma unroll
             for (int m = 0; m < kMT; ++m) {
@@ -662,26 +669,33 @@ static cudaError_t launch_one(void (*kernel)(Params...), dim3 grid, size_t smem,
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+template <int MT>
+static void (*logits_kernel(int r, bool base_f32))(const SampleArgs, int) {
+    switch (r) {
+        case 64: return base_f32 ? batch_logits_kernel<64, true, MT> : batch_logits_kernel<64, false, MT>;
+        case 128:
+            return base_f32 ? batch_logits_kernel<128, true, MT> : batch_logits_kernel<128, false, MT>;
+        case 256:
+            return base_f32 ? batch_logits_kernel<256, true, MT> : batch_logits_kernel<256, false, MT>;
+        default: return nullptr;
+    }
+}
+
 cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches) {
-    const int groups = (a.rows + kGroupRows - 1) / kGroupRows;
+    // the launch variant by row count: 16-row groups (whole-tile head
+    // prefetch) up to 16 rows, 32-row groups above
+    const int mt = a.rows <= 16 ? 1 : 2;
+    const int group_rows = 16 * mt;
+    const int groups = (a.rows + group_rows - 1) / group_rows;
     // one wave: the plan's vocab blocks shared out over the row groups
     const int nblk = a.grid / groups > 0 ? a.grid / groups : 1;
     const int nb2 = (a.V + kCdfIds - 1) / kCdfIds;
-    const size_t smem = (size_t)kGroupRows * (a.r + kBPad) * sizeof(uint16_t);
+    const size_t smem = (size_t)group_rows * (a.r + kBPad) * sizeof(uint16_t);
     *launches = 0;
     if (nb2 > 64 || a.rows > kMaxRows || a.N > kMaxSteps) return cudaErrorInvalidValue;
-    void (*logits)(const SampleArgs, int);
-    const bool bf = a.base_f != nullptr;
-    switch (a.r) {
-        case 64: logits = bf ? batch_logits_kernel<64, true> : batch_logits_kernel<64, false>; break;
-        case 128:
-            logits = bf ? batch_logits_kernel<128, true> : batch_logits_kernel<128, false>;
-            break;
-        case 256:
-            logits = bf ? batch_logits_kernel<256, true> : batch_logits_kernel<256, false>;
-            break;
-        default: return cudaErrorInvalidValue;
-    }
+    void (*logits)(const SampleArgs, int) =
+        mt == 1 ? logits_kernel<1>(a.r, a.base_f != nullptr) : logits_kernel<2>(a.r, a.base_f != nullptr);
+    if (!logits) return cudaErrorInvalidValue;
     int n = 0;
     cudaError_t e = cudaSuccess;
     for (int i = 0; i < a.N && e == cudaSuccess; ++i) {

@@ -21,10 +21,9 @@ constexpr int kLineU32 = 32;
 constexpr size_t kWinMaxN = (size_t)2 * kMaxSteps * kChainRows * kLineU64;
 constexpr size_t kWinCntN = (size_t)2 * kMaxSteps * kLineU32;
 // per-position path: a winner word per (position, row) and, per position,
-// a done counter per 64-row group (logits kernel) and per row (inverse-CDF
-// sum kernel)
-constexpr int kBatchGroupRows = 32;
-constexpr int kBatchCntPerStep = kMaxRows / kBatchGroupRows + kMaxRows;
+// a done counter per row group of 16 or 32 rows (logits kernel; the first
+// kMaxRows / 16 words) and per row (inverse-CDF sum kernel)
+constexpr int kBatchCntPerStep = kMaxRows / 16 + kMaxRows;
 constexpr size_t kBatchWinN = (size_t)kMaxSteps * kMaxRows;
 constexpr size_t kBatchCntN = (size_t)kMaxSteps * kBatchCntPerStep;
 constexpr int kCdfIds = kBatchThreads * 16;   // vocab ids per inverse-CDF sum block
