@@ -250,6 +250,7 @@ def run_gpu(args):
     head, embed = head.to(dev), embed.to(dev)
     d = {k: v.to(dev) for k, v in inp.items()}
     plan = api.Plan(w.vocab, w.rank, w.steps, w.rows, device=local)
+    plan.set_path({"auto": 0, "chain": 1, "batch": 2, "simple": 3}[args.path])
     R, N, V = w.rows, w.steps, w.vocab
     toks = torch.full((R, N), -1, dtype=torch.int64, device=dev)
     cache = torch.empty((R, N, V), dtype=torch.float32 if cache_f32 else torch.bfloat16,
@@ -402,6 +403,8 @@ def main():
                     help="element type of the base logits")
     ap.add_argument("--cache-dtype", default="bf16", choices=["bf16", "f32"],
                     help="element type of the logits cache")
+    ap.add_argument("--path", default="auto", choices=["auto", "chain", "batch", "simple"],
+                    help="force a path (default: the library's automatic choice)")
     ap.add_argument("--rows", type=int, default=0,
                     help="run the workload with this many rows instead of its own")
     ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOADS),

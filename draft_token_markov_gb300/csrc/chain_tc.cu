@@ -836,7 +836,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     __syncthreads();
     if (tid < N * kChainRows) {
         const int b = tid % kChainRows, i2 = tid / kChainRows;
-        c.hri[i2][b] = dm_row_step_hash(c.seed[b], (uint32_t)b, (uint32_t)i2);
+        c.hri[i2][b] = dm_row_step_hash(c.seed[b], (uint32_t)(a.row_base + b), (uint32_t)i2);
     }
     if (cta == 0 && tid < kMaxSteps * kChainRows) {
         // the next call's exchange words (the other call parity; the previous

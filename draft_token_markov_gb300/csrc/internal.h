@@ -11,6 +11,7 @@ constexpr int kMaxSteps = 16;          // draft positions a plan may take
 constexpr int kMaxVocab = 262144;      // vocabulary bound
 constexpr int kMaxRows = 256;          // rows a plan may take
 constexpr int kChainRows = 8;          // rows of one chain launch (MMA N = 8)
+constexpr int kChainSliceRows = 24;    // automatic path, Gumbel: tcgen05 chain per 8-row slice up to here
 constexpr int kChainThreads = 512;     // threads of a chain CTA (one CTA per SM)
 constexpr int kBatchThreads = 256;
 constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
@@ -78,6 +79,8 @@ struct SampleArgs {
     uint32_t *win_cnt;         // [2 call parities][N] x kLineU32: CTAs that reported
     uint64_t timeout_ns;
     int grid;                  // persistent grid size (chain) or vocab blocks (batch)
+    int row_base;              // the call's row index of this launch's row 0 (row slices
+                               // of the chain): the noise and inverse-CDF hashes take it
 };
 
 // Kernel launchers (return the CUDA error of the launch).

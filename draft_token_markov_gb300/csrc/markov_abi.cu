@@ -345,6 +345,15 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
     if ((p->path == MARKOV_PATH_CHAIN || p->path == MARKOV_PATH_CHAIN_SIMPLE) && !chain)
         return MARKOV_EUNSUPPORTED;
     if (p->path == MARKOV_PATH_BATCH) chain = false;
+    // the automatic choice between the chain limit and kChainSliceRows rows
+    // in Gumbel mode: one tcgen05 chain launch per 8-row slice (no forked
+    // noise: each slice draws its own).  Measured on the 129280 x 256 head:
+    // 12 / 16 / 24 rows take 193 / 199 / 300 us this way against 229 / 235 /
+    // 328 us for the per-position kernels; in inverse-CDF mode the chain's
+    // two-pass selection makes slices slower (9 rows: 381 against 271 us).
+    const bool sliced = !chain && p->path == MARKOV_PATH_AUTO && mode == MARKOV_GUMBEL &&
+                        rows <= kChainSliceRows && p->tc_ok && p->noise_state == 0;
+    if (sliced) chain = true;
     const bool use_tc = chain && p->tc_ok && p->path != MARKOV_PATH_CHAIN_SIMPLE;
 
     DeviceGuard guard(p->d.device);
@@ -413,10 +422,26 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
 
     if (use_tc) {
         a.grid = p->tc_grid;
-        cudaError_t e = launch_chain_tc(a, p->tmap, noise_ready, s);
-        if (e == cudaErrorCooperativeLaunchTooLarge) { cudaGetLastError(); return MARKOV_ENOTRESIDENT; }
-        if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
-        ++launches;
+        for (int b0 = 0; b0 < rows; b0 += kChainRows) {
+            // rows [b0, b0 + 8) of the call as one chain launch
+            SampleArgs as = a;
+            const int64_t bo = (int64_t)b0;
+            if (as.base) as.base += bo * base_s0;
+            if (as.base_f) as.base_f += bo * base_s0;
+            if (as.cache) as.cache += bo * cache_s0;
+            if (as.cache_f) as.cache_f += bo * cache_s0;
+            as.anchor += b0;
+            as.temperature += b0;
+            as.seeds += b0;
+            as.row_state_idx += b0;
+            as.tokens += bo * tok_s0;
+            as.rows = rows - b0 < kChainRows ? rows - b0 : kChainRows;
+            as.row_base = b0;
+            cudaError_t e = launch_chain_tc(as, p->tmap, noise_ready, s);
+            if (e == cudaErrorCooperativeLaunchTooLarge) { cudaGetLastError(); return MARKOV_ENOTRESIDENT; }
+            if (e != cudaSuccess) { cudaGetLastError(); return MARKOV_ECUDA; }
+            ++launches;
+        }
         p->last_path = MARKOV_PATH_CHAIN;
     } else if (chain) {
         if (p->chain_occ < 1) return MARKOV_ENOTRESIDENT;

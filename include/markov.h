@@ -66,7 +66,10 @@ typedef enum markov_dtype {
 } markov_dtype;
 
 typedef enum markov_path {
-    MARKOV_PATH_AUTO = 0,       /* chain up to markov_chain_max_rows rows, else batch */
+    MARKOV_PATH_AUTO = 0,       /* up to markov_chain_max_rows rows: the chain; Gumbel mode
+                                   up to 24 rows (no forked noise pending, tcgen05 chain
+                                   available): one tcgen05 chain launch per 8-row slice;
+                                   else batch */
     MARKOV_PATH_CHAIN = 1,      /* the persistent single-launch chain kernel (tcgen05, head
                                    resident in TMEM and shared memory when it fits) */
     MARKOV_PATH_BATCH = 2,      /* per-position kernels (the larger-batch loop) */

@@ -24,12 +24,14 @@ def _eager(api, w, inp, head, embed, plan):
     return toks.cpu().numpy(), cache.view(torch.int16).cpu().numpy()
 
 
-@pytest.mark.parametrize("rows", [8, 20], ids=["chain", "per-position"])
+@pytest.mark.parametrize("rows", [8, 20, 40], ids=["chain", "chain-slices", "per-position"])
 @pytest.mark.parametrize("mode", [W.GUMBEL, W.INVCDF])
 def test_graph_replays_equal_eager_calls(gpu_lib, mode, rows):
-    # 8 rows take the chain kernel; 20 rows the per-position kernels, whose
-    # launches after the first are programmatic dependent launches (graph
-    # edges of that kind once captured)
+    # 8 rows take the chain kernel; 20 rows three chain launches (8-row
+    # slices) in Gumbel mode and the per-position kernels in inverse-CDF
+    # mode; 40 rows the per-position kernels, whose launches after the first
+    # are programmatic dependent launches (graph edges of that kind once
+    # captured)
     api = gpu_lib
     w = W.small(129280, 256, rows, 8, mode, seed=41, padding_rows=(2, 5), spikes=8,
                 temperatures=(0.0, 0.6, 1.0))

@@ -54,6 +54,36 @@ def test_batch_rows_parity(gpu_lib, w):
     assert rep.ok(), rep.summary()
 
 
+@pytest.mark.parametrize("rows", [9, 16, 21, 24])
+def test_chain_row_slices(gpu_lib, rows):
+    # between the chain limit and 24 rows, in Gumbel mode, the automatic path
+    # runs the tcgen05 chain once per 8-row slice; the noise hash takes the
+    # call's row index, so the slices sample what one call would
+    w = W.small(8192, 256, rows, 6, W.GUMBEL, seed=80 + rows, padding_rows=(3, rows - 1),
+                spikes=4, temperatures=(0.0, 0.6, 1.0))
+    inp = W.make_call(w)
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    try:
+        toks, cache = U.run(gpu_lib, w, inp, AUTO, plan=plan)
+        assert plan.query(gpu_lib.Q_LAST_PATH) == CHAIN
+        assert plan.query(gpu_lib.Q_LAST_LAUNCHES) == (rows + 7) // 8
+        rep = U.check(w, inp, toks, cache)
+        assert rep.ok(), rep.summary()
+        # the same call with the noise forked takes the per-position kernels
+        toks2, cache2 = U.run(gpu_lib, w, inp, AUTO, plan=plan, fork=True)
+        assert plan.query(gpu_lib.Q_LAST_PATH) == BATCH
+        rep = U.check(w, inp, toks2, cache2)
+        assert rep.ok(), rep.summary()
+        # inverse-CDF calls of this size take the per-position kernels
+        wc = w.with_(mode=W.INVCDF)
+        toks3, cache3 = U.run(gpu_lib, wc, inp, AUTO, plan=plan)
+        assert plan.query(gpu_lib.Q_LAST_PATH) == BATCH
+        rep = U.check(wc, inp, toks3, cache3)
+        assert rep.ok(), rep.summary()
+    finally:
+        plan.close()
+
+
 def test_batch_calls_share_one_plan(gpu_lib):
     # the per-position path keeps per-row winner words and done counters in
     # the plan; each call must leave them cleared for the next, whatever its
