@@ -165,10 +165,11 @@ def max_over_ranks(value: float) -> float:
     return float(t.item())
 
 
-def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG):
+def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG, threads: int = 0):
     """Time the oracle on a bounded sample of the workload: one call over the
     workload's first live row (all N positions), repeated while the total
-    stays near seconds_hint.  Returns (tokens/s, sample description, cores)."""
+    stays near seconds_hint, on `threads` host threads (0: all cores).
+    Returns (tokens/s, sample description, threads used)."""
     import numpy as np
     import oracle
     from draft_token_markov_gb300 import workloads as W
@@ -180,7 +181,7 @@ def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG):
     b0 = live[0]
     idx = np.full(w.rows, -1, dtype=np.int64)
     idx[b0] = b0
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     base = oracle.bf16_bits(inp["base"])
     args = (base, hb, eb, inp["anchor"].numpy(), inp["temperature"].numpy(),
             inp["seeds"].numpy(), idx, w.mode, w.mult, w.cap)
@@ -194,7 +195,8 @@ def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG):
             break
     tokens = calls * w.steps
     return tokens / el, (f"{calls} oracle call(s) of the {w.name} workload restricted to one "
-                         f"live row ({w.steps} draft tokens each), OpenMP over vocab ids"), cores
+                         f"live row ({w.steps} draft tokens each), OpenMP over vocab ids on "
+                         f"{cores} thread(s)"), cores
 
 
 def run_reference(args):
@@ -318,6 +320,14 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st} in the timed region")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     chain_ms = step_ms
+    # warm: the same calls back to back, no flush between them (reported
+    # beside the cold headline)
+    warm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+               for _ in range(min(args.steps, 50))]
+    for e in warm_ev:
+        step(e)
+    torch.cuda.synchronize()
+    warm_ms = [e[0].elapsed_time(e[1]) for e in warm_ev]
     total_ms = max_over_ranks(sum(step_ms))
 
     # end to end: host (pinned) inputs copied in, tokens copied out, per step
@@ -349,6 +359,8 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores = cpu_oracle_sample(args.cpu_seconds, cfg)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        v1, desc1, _ = cpu_oracle_sample(max(2.0, args.cpu_seconds / 3.0), cfg, threads=1)
+        cpu["single_thread"] = {"value": v1, "unit": UNIT, "sample": desc1}
     ms_per_step = total_ms / args.steps
     value = tokens_per_step * world * args.steps / (total_ms / 1000.0)
     e2e_step = statistics.mean(e2e_ms)
@@ -367,9 +379,11 @@ def run_gpu(args):
         "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
                         "p99": sorted(step_ms)[min(len(step_ms) - 1,
                                                    int(0.99 * len(step_ms)))] * 1000.0,
-                        "chain_kernel_median": statistics.median(chain_ms) * 1000.0},
+                        "chain_kernel_median": statistics.median(chain_ms) * 1000.0,
+                        "warm_median": statistics.median(warm_ms) * 1000.0},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "frac_of_nominal_8000_gbs": achieved / 8000.0,
                      "kernel": {"tcgen05 chain": "chain_tc_kernel", "simple chain": "chain_kernel",
                                 "batch": "batch kernels"}.get(path, path),
                      "algorithmic_bytes_per_launch": alg_bytes,
