@@ -595,17 +595,18 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
         // scan the target block: 16 consecutive ids per thread, in vocab order
         const uint64_t target = s_target;
         const int w0 = cb * kCdfIds, w1 = min(a.V, w0 + kCdfIds);
-        const int c0 = w0 + tid * 16;
-        float y[2][8];
-        bool oky[2];
+        constexpr int kPer = kCdfIds / kBatchThreads;   // consecutive ids per thread
+        const int c0 = w0 + tid * kPer;
+        float y[kPer / 8][8];
+        bool oky[kPer / 8];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kPer / 8; ++u) {
             oky[u] = c0 + 8 * u < w1;
             if (oky[u]) cache8(a, b, i, c0 + 8 * u, y[u]);
         }
         uint64_t mine = 0ull;
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < kPer / 8; ++u)
             if (oky[u]) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mine += cdf_weight_of(y[u][e], T, M);
@@ -623,10 +624,12 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
         uint64_t run = s_blkpre + wpre + incl - mine;
         if (mine && run <= target && target < run + mine) {
             int hit = -1;
-            for (int k = 0; k < 16 && hit < 0; ++k) {
-                if (!oky[k >> 3]) break;
-                run += cdf_weight_of(y[k >> 3][k & 7], T, M);
-                if (run > target) hit = k;
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                if (hit < 0 && oky[k >> 3]) {
+                    run += cdf_weight_of(y[k >> 3][k & 7], T, M);
+                    if (run > target) hit = k;
+                }
             }
             if (hit >= 0) s_tok = c0 + hit;
         }
