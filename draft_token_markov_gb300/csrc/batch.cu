@@ -511,11 +511,12 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     pdl_wait();
-    if (!row_live(a, b)) return;
-    const float T = a.temperature[b];
-    if (!samples(T)) return;
+    // the row's state, temperature and winner word in one round trip (b < rows)
     unsigned long long *ws = win_slot(a, i, b);
+    const int64_t idx = a.row_state_idx[b];
+    const float T = a.temperature[b];
     const uint64_t win = __ldcg(ws);
+    if (idx < 0 || !samples(T)) return;
     if (win == 0ull) return;                  // the logits kernel decided the row
     const float M = key_from_ordered(packed_ordered(win));
 

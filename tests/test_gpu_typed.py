@@ -56,6 +56,10 @@ CASES = [
     ("batch", lambda mode: W.small(3008, 64, 12, 3, mode, seed=73, padding_rows=(4, 9),
                                    spikes=2, mult=0.5, cap=30.0,
                                    temperatures=(0.0, 0.8, 1.0)), BATCH),
+    # 13 rows: two tcgen05 chain slices in Gumbel mode, the per-position
+    # kernels (16-row groups) in inverse-CDF mode
+    ("auto, 13 rows", lambda mode: W.small(8192, 256, 13, 3, mode, seed=74, padding_rows=(6,),
+                                           spikes=2, temperatures=(0.0, 0.6, 1.0)), AUTO),
 ]
 
 
