@@ -6,9 +6,10 @@
 // per-step kernels are launched with programmatic dependent launch).
 //
 // Per position i, in launch order on one stream:
-//   logits  grid (blocks, row groups of 64): bias tiles [16 ids x 64 rows] by
-//           mma.m16n8k16 with the previous tokens' embeddings staged in
-//           shared memory, the epilogue (BF16 rounding, base add, transform,
+//   logits  grid (blocks, row groups of 16 rows up to 16 rows, else 32):
+//           bias tiles [16 ids x group rows] by mma.m16n8k16 with the
+//           previous tokens' embeddings staged in shared memory, the
+//           epilogue (BF16 rounding, base add, transform,
 //           cache store) and each block's best (key, id) per row, merged
 //           into the row's winner word by one u64 atomicMax per block.  The
 //           last block of a row group to finish (a done counter) writes the
@@ -25,7 +26,7 @@
 //
 // Every launch after the first of a call is a programmatic dependent launch:
 // it may start while the kernel before it still runs, does only input-side
-// work (block ranges, L2 prefetch of its base-logit rows) until
+// work (block ranges, L2 prefetch of its head and base-logit rows) until
 // griddepcontrol.wait, and every block of every kernel passes that wait
 // before it reads or writes anything the path writes, and before it exits.
 // A grid therefore completes only after the grid before it has, and a
@@ -71,23 +72,27 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// Loads of data no kernel of the call writes (the head, the base logits),
+// bypassing L1, with an L2 cache policy.
 __device__ __forceinline__ uint4 ld_nc_v4(const void *ptr, uint64_t pol) {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(pol));
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "l"(pol));
     return v;
 }
 __device__ __forceinline__ uint32_t ld_nc_u32(const void *ptr, uint64_t pol) {
     uint32_t v;
-    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(pol));
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+        : "=r"(v)
+        : "l"(ptr), "l"(pol));
     return v;
 }
 __device__ __forceinline__ float2 ld_nc_f2(const void *ptr, uint64_t pol) {
     float2 v;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
-                 : "=f"(v.x), "=f"(v.y)
-                 : "l"(ptr), "l"(pol));
+        : "=f"(v.x), "=f"(v.y)
+        : "l"(ptr), "l"(pol));
     return v;
 }
 __device__ __forceinline__ void st_u32(void *ptr, uint32_t v, uint64_t pol) {
@@ -215,11 +220,10 @@ __device__ __forceinline__ void cache8(const SampleArgs &a, int b, int i, int v,
 }  // namespace
 
 // The logits kernel of position i, for row groups of 16 MT rows.  MMA
-// roles: M = 16 rows (the previous
-// tokens' embeddings, staged in shared memory), N = 8 vocab ids (head rows,
-// read from global), K = rank, so that each thread's accumulators hold pairs
-// of consecutive ids of one row: base logits are read and cache entries
-// written two ids at a time.  Rows of a thread: row0 + 16 m + 8 h + g for
+// roles: M = 16 rows (the previous tokens' embeddings, staged in shared
+// memory), N = 8 vocab ids (head rows, read from global), K = rank, so that
+// each thread's accumulators hold pairs of consecutive ids of one row: base
+// logits are read and cache entries written two ids at a time.  Rows of a thread: row0 + 16 m + 8 h + g for
 // M-tile m < MT and half h < 2 (bit 2 m + h of `live`).  The head fragments
 // of a tile are fetched kDepth k-chunks ahead of their MMAs: the whole tile
 // at once for 16-row groups (few accumulators leave the registers for it),
@@ -231,7 +235,7 @@ batch_logits_kernel(const SampleArgs a, int i) {
     constexpr int kMT = MT;
     constexpr int kChunks = RANK / 32;
     constexpr int kDepth = MT == 1 ? kChunks : 2;
-    extern __shared__ __align__(16) uint16_t e_smem[];      // [64][RANK + kBPad]
+    extern __shared__ __align__(16) uint16_t e_smem[];      // [kGroupRows][RANK + kBPad]
     __shared__ unsigned long long s_best[kGroupRows];
     __shared__ float s_T[kGroupRows];
     __shared__ int s_resc[kGroupRows];
