@@ -167,26 +167,39 @@ def max_over_ranks(value: float) -> float:
     return float(t.item())
 
 
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(cfg: int):
+    """The oracle's arguments for the workload's first live row (drawn once
+    per process; the timed samples reuse them)."""
+    if cfg not in _ORACLE_INPUTS:
+        import numpy as np
+        import oracle
+        from draft_token_markov_gb300 import workloads as W
+        w = W.CONFIGS[cfg]
+        head, embed = W.make_weights(w)
+        inp = W.make_call(w)
+        hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
+        live = [b for b in range(w.rows) if int(inp["row_state_idx"][b]) >= 0]
+        b0 = live[0]
+        idx = np.full(w.rows, -1, dtype=np.int64)
+        idx[b0] = b0
+        base = oracle.bf16_bits(inp["base"])
+        _ORACLE_INPUTS[cfg] = (w, (base, hb, eb, inp["anchor"].numpy(),
+                                   inp["temperature"].numpy(), inp["seeds"].numpy(), idx,
+                                   w.mode, w.mult, w.cap))
+    return _ORACLE_INPUTS[cfg]
+
+
 def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG, threads: int = 0):
     """Time the oracle on a bounded sample of the workload: one call over the
     workload's first live row (all N positions), repeated while the total
     stays near seconds_hint, on `threads` host threads (0: all cores).
     Returns (tokens/s, sample description, threads used)."""
-    import numpy as np
     import oracle
-    from draft_token_markov_gb300 import workloads as W
-    w = W.CONFIGS[cfg]
-    head, embed = W.make_weights(w)
-    inp = W.make_call(w)
-    hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
-    live = [b for b in range(w.rows) if int(inp["row_state_idx"][b]) >= 0]
-    b0 = live[0]
-    idx = np.full(w.rows, -1, dtype=np.int64)
-    idx[b0] = b0
+    w, args = _oracle_inputs(cfg)
     cores = threads or os.cpu_count() or 1
-    base = oracle.bf16_bits(inp["base"])
-    args = (base, hb, eb, inp["anchor"].numpy(), inp["temperature"].numpy(),
-            inp["seeds"].numpy(), idx, w.mode, w.mult, w.cap)
     t0 = time.perf_counter()
     calls = 0
     while True:
@@ -208,10 +221,13 @@ def run_reference(args):
     vals = []
     desc = cores = None
     cfg = WORKLOADS[args.workload]
+    # each step a bounded sample, sized so that the whole run stays near two
+    # minutes whatever K and W are (at least one oracle call per step)
+    per_step = max(0.05, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_oracle_sample(2.0, cfg)
+        cpu_oracle_sample(per_step, cfg)
     for _ in range(args.steps):
-        v, desc, cores = cpu_oracle_sample(8.0, cfg)
+        v, desc, cores = cpu_oracle_sample(per_step, cfg)
         vals.append(v)
     value = statistics.mean(vals)
     from draft_token_markov_gb300 import workloads as W
