@@ -1125,20 +1125,45 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 const uint32_t tag32 = epoch;
                 if (tid < kChainRows) c.sum[tid] = 0ull;
                 __syncthreads();
-                for (int b = 0; b < R && b < kChainRows; ++b) {
-                    if (!c.sampling[b]) continue;
-                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                    const float M = key_from_ordered(o);
-                    if (o == 0xffffffffu || isinf(M)) continue;
-                    const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                    uint64_t part = 0ull;
-                    for (int v = v_begin + tid; v < v_end; v += kThreads) {
-                        const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
-                        part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                // kGR rows a time: every cached logit of the group is loaded
+                // before any weight, so the rows share one read latency
+                constexpr int kMaxIds = (kTmemChunks + kSmemChunks) / (RANK / 64) * 128;
+                constexpr int kPT = (kMaxIds + kThreads - 1) / kThreads;   // ids per thread
+                constexpr int kGR = RANK == 64 ? 2 : 4;
+                for (int b0 = 0; b0 < R && b0 < kChainRows; b0 += kGR) {
+                    float xs[kGR][kPT];
+                    bool use[kGR];
+#pragma unroll
+                    for (int r = 0; r < kGR; ++r) {
+                        const int b = b0 + r;
+                        const uint32_t o = b < R && b < kChainRows ? (uint32_t)(c.win[b] >> 32) : 0u;
+                        use[r] = b < R && b < kChainRows && c.sampling[b] && o != 0xffffffffu &&
+                                 !isinf(key_from_ordered(o));
+                        const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
+#pragma unroll
+                        for (int k = 0; k < kPT; ++k) {
+                            const int v = v_begin + tid + k * kThreads;
+                            xs[r][k] = 0.0f;
+                            if (use[r] && v < v_end)
+                                xs[r][k] = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
+                        }
                     }
+#pragma unroll
+                    for (int r = 0; r < kGR; ++r) {
+                        if (!use[r]) continue;
+                        const int b = b0 + r;
+                        const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
+                        uint64_t part = 0ull;
+#pragma unroll
+                        for (int k = 0; k < kPT; ++k) {
+                            if (v_begin + tid + k * kThreads >= v_end) break;
+                            const float x = __fdiv_rn(xs[r][k], c.T[b]);
+                            part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                        }
     #pragma unroll
-                    for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-                    if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
+                        for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+                        if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
+                    }
                 }
                 __syncthreads();
                 if (tid < kChainRows && c.sampling[tid]) {
