@@ -263,3 +263,27 @@ def test_bad_arguments_launch_nothing(gpu_lib):
     assert call() == 0
     assert gpu_lib.markov_plan_status(plan) == 0
     plan.close()
+
+
+@pytest.mark.parametrize("path", [CHAIN, BATCH, SIMPLE])
+def test_infinite_keys_take_the_lowest_id(gpu_lib, path):
+    # inverse CDF at T = 0.5: row 0 has two +inf base logits; row 1 has finite
+    # logits near the BF16 maximum whose key l / T overflows to +inf, the
+    # largest of them not at the lowest id; row 3 is all -inf (token 0).
+    # +inf keys decide the token directly: the lowest id with a +inf key.
+    w = W.small(4096, 128, 4, 3, W.INVCDF, seed=90, temperatures=(0.5,))
+    inp = W.make_call(w)
+    base = inp["base"].float()
+    for i in range(w.steps):
+        base[0, i, [100, 3000]] = float("inf")
+        base[1, i, 500] = 2.9e38
+        base[1, i, 2000] = 2.5e38
+        base[1, i, 510] = 3.3e38      # same vocab block as 500, larger logit
+        base[3, i, :] = float("-inf")
+    inp["base"] = base.to(torch.bfloat16)
+    toks, cache = U.run(gpu_lib, w, inp, path)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+    assert toks[0].tolist() == [100] * w.steps
+    assert toks[1].tolist() == [500] * w.steps
+    assert toks[3].tolist() == [0] * w.steps
