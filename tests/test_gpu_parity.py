@@ -8,6 +8,7 @@ import torch
 import oracle
 from draft_token_markov_gb300 import workloads as W
 from tests import gpu_util as U
+from tests.acceptance import check_typed
 
 pytestmark = pytest.mark.gpu
 
@@ -287,3 +288,60 @@ def test_infinite_keys_take_the_lowest_id(gpu_lib, path):
     assert toks[0].tolist() == [100] * w.steps
     assert toks[1].tolist() == [500] * w.steps
     assert toks[3].tolist() == [0] * w.steps
+
+
+@pytest.mark.parametrize("path", [AUTO, BATCH])
+def test_gumbel_nan_and_tie_rows_above_the_chain_limit(gpu_lib, path):
+    # 12 rows in Gumbel mode: the automatic path runs two chain slices, the
+    # forced one the per-position kernels (16-row groups); a NaN row takes
+    # its lowest NaN id, a tie row's equal maxima the lowest id, and +inf
+    # logits win over finite ones
+    w = W.small(4096, 128, 12, 4, W.GUMBEL, seed=91, tie_row=3, nan_row=5, padding_rows=(7,),
+                temperatures=(0.0, 0.8, 1.0))
+    inp = W.make_call(w)
+    base = inp["base"].float()
+    for i in range(w.steps):
+        base[9, i, [40, 2900]] = float("inf")
+    inp["base"] = base.to(torch.bfloat16)
+    toks, cache = U.run(gpu_lib, w, inp, path)
+    rep = U.check(w, inp, toks, cache)
+    assert rep.ok(), rep.summary()
+    assert toks[9].tolist() == [40] * w.steps
+
+
+@pytest.mark.parametrize("path", [CHAIN, SIMPLE, BATCH])
+@pytest.mark.parametrize("base_f32", [False, True], ids=["bf16 base", "f32 base"])
+def test_odd_base_strides(gpu_lib, path, base_f32):
+    # base logits as a view with odd row and position strides (elements):
+    # the per-position kernels' paired base loads need even strides and
+    # take single-element loads here; every path must read the same values
+    w = W.small(4096, 128, 5, 3, W.GUMBEL, seed=92, padding_rows=(2,),
+                temperatures=(0.0, 0.7, 1.0))
+    if path == BATCH:
+        w = w.with_(rows=12, padding_rows=(2, 9))
+    inp = W.make_call(w, base_f32=base_f32)
+    R, N, V = w.rows, w.steps, w.vocab
+    big = torch.zeros((R, N, V + 3), dtype=inp["base"].dtype, device="cuda")
+    big[:, :, 1:V + 1] = inp["base"].cuda()
+    view = big[:, :, 1:V + 1]
+    assert view.stride(1) % 2 == 1 and view.stride(0) % 2 == 1
+    h, e, hb, eb = U.weights(w)
+    plan = gpu_lib.Plan(V, w.rank, N, R)
+    try:
+        plan.set_path(path)
+        d = U.to_dev(inp)
+        toks, cache = U.sentinel_outputs(R, N, V)
+        gpu_lib.markov_chain_sample(plan, view, h.cuda(), e.cuda(), d["anchor"], d["temperature"],
+                                    d["seeds"], d["row_state_idx"], w.mode, w.mult, w.cap, toks,
+                                    cache)
+        assert gpu_lib.markov_plan_status(plan) == 0
+        t = toks.cpu().numpy()
+        c = cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    finally:
+        plan.close()
+    if base_f32:
+        rep = check_typed(inp, hb, eb, w.mode, w.mult, w.cap, t, c, False, U.SENT_T, U.SENT_C,
+                          nthreads=U.NTHREADS)
+    else:
+        rep = U.check(w, inp, t, c)
+    assert rep.ok(), rep.summary()
