@@ -33,10 +33,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft tokens/s and µs per N-step Markov call; % of GB300 HBM roofline"
 UNIT = "draft tokens/s"
-WORKLOAD_CFG = 2
-# --workload names: the default is the DeepSeek-V4.1 chain the headline is
-# quoted on; the others measure the remaining workloads' paths
-WORKLOADS = {"deepseek": 2, "latency": 3, "softcap": 4, "batch": 5, "tiny": 1}
+# --workload names (workloads.BY_NAME): the default is the DeepSeek-V4.1
+# chain the headline is quoted on; the others measure the remaining paths
+DEFAULT_WORKLOAD = "deepseek"
+WORKLOAD_NAMES = ("batch", "deepseek", "latency", "softcap", "tiny")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chain_deepseek_traffic.json")
 
 
@@ -170,14 +170,14 @@ def max_over_ranks(value: float) -> float:
 _ORACLE_INPUTS = {}
 
 
-def _oracle_inputs(cfg: int):
+def _oracle_inputs(name: str):
     """The oracle's arguments for the workload's first live row (drawn once
     per process; the timed samples reuse them)."""
-    if cfg not in _ORACLE_INPUTS:
+    if name not in _ORACLE_INPUTS:
         import numpy as np
         import oracle
         from draft_token_markov_gb300 import workloads as W
-        w = W.CONFIGS[cfg]
+        w = W.BY_NAME[name]
         head, embed = W.make_weights(w)
         inp = W.make_call(w)
         hb, eb = oracle.bf16_bits(head), oracle.bf16_bits(embed)
@@ -186,19 +186,20 @@ def _oracle_inputs(cfg: int):
         idx = np.full(w.rows, -1, dtype=np.int64)
         idx[b0] = b0
         base = oracle.bf16_bits(inp["base"])
-        _ORACLE_INPUTS[cfg] = (w, (base, hb, eb, inp["anchor"].numpy(),
+        _ORACLE_INPUTS[name] = (w, (base, hb, eb, inp["anchor"].numpy(),
                                    inp["temperature"].numpy(), inp["seeds"].numpy(), idx,
                                    w.mode, w.mult, w.cap))
-    return _ORACLE_INPUTS[cfg]
+    return _ORACLE_INPUTS[name]
 
 
-def cpu_oracle_sample(seconds_hint: float = 20.0, cfg: int = WORKLOAD_CFG, threads: int = 0):
+def cpu_oracle_sample(seconds_hint: float = 20.0, name: str = DEFAULT_WORKLOAD,
+                      threads: int = 0):
     """Time the oracle on a bounded sample of the workload: one call over the
     workload's first live row (all N positions), repeated while the total
     stays near seconds_hint, on `threads` host threads (0: all cores).
     Returns (tokens/s, sample description, threads used)."""
     import oracle
-    w, args = _oracle_inputs(cfg)
+    w, args = _oracle_inputs(name)
     cores = threads or os.cpu_count() or 1
     t0 = time.perf_counter()
     calls = 0
@@ -220,18 +221,18 @@ def run_reference(args):
         return
     vals = []
     desc = cores = None
-    cfg = WORKLOADS[args.workload]
+    name = args.workload
     # each step a bounded sample, sized so that the whole run stays near two
     # minutes whatever K and W are (at least one oracle call per step)
     per_step = max(0.05, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        cpu_oracle_sample(per_step, cfg)
+        cpu_oracle_sample(per_step, name)
     for _ in range(args.steps):
-        v, desc, cores = cpu_oracle_sample(per_step, cfg)
+        v, desc, cores = cpu_oracle_sample(per_step, name)
         vals.append(v)
     value = statistics.mean(vals)
     from draft_token_markov_gb300 import workloads as W
-    w = W.CONFIGS[cfg]
+    w = W.BY_NAME[name]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.steps / value,
@@ -257,8 +258,8 @@ def run_gpu(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = WORKLOADS[args.workload]
-    w = W.CONFIGS[cfg]
+    name = args.workload
+    w = W.BY_NAME[name]
     if args.rows:
         # the workload with another row count (its padding rows below it kept)
         w = w.with_(rows=args.rows, padding_rows=tuple(b for b in w.padding_rows
@@ -375,9 +376,9 @@ def run_gpu(args):
     traffic = None if typed else _traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, cores = cpu_oracle_sample(args.cpu_seconds, cfg)
+        v, desc, cores = cpu_oracle_sample(args.cpu_seconds, name)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
-        v1, desc1, _ = cpu_oracle_sample(max(2.0, args.cpu_seconds / 3.0), cfg, threads=1)
+        v1, desc1, _ = cpu_oracle_sample(max(2.0, args.cpu_seconds / 3.0), name, threads=1)
         cpu["single_thread"] = {"value": v1, "unit": UNIT, "sample": desc1}
     ms_per_step = total_ms / args.steps
     value = tokens_per_step * world * args.steps / (total_ms / 1000.0)
@@ -439,7 +440,7 @@ def main():
                     help="force a path (default: the library's automatic choice)")
     ap.add_argument("--rows", type=int, default=0,
                     help="run the workload with this many rows instead of its own")
-    ap.add_argument("--workload", default="deepseek", choices=sorted(WORKLOADS),
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_NAMES,
                     help="deepseek (default, the headline): V=129280 r=256 8 rows N=8; "
                          "latency: 1 row; softcap: V=262144 r=128 inverse CDF; batch: 64 rows "
                          "(the per-position path); tiny: V=4096 r=64")

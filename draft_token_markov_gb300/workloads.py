@@ -69,7 +69,8 @@ BATCH = Workload("large batch V=129280 r=256 rows=64 N=8 inverse-cdf", 129280, 2
                  INVCDF, 0.02, 3.0, temperatures=(0.0, 0.5, 0.8, 1.0, 1.2),
                  padding_rows=tuple(range(7, 64, 8)), gen_seed=1005)
 
-CONFIGS = {1: TINY, 2: DEEPSEEK, 3: LATENCY, 4: SOFTCAP, 5: BATCH}
+BY_NAME = {"tiny": TINY, "deepseek": DEEPSEEK, "latency": LATENCY, "softcap": SOFTCAP,
+           "batch": BATCH}
 
 
 def _randn_bf16(shape, std, g):

@@ -197,14 +197,15 @@ def test_repeated_calls_are_deterministic(gpu_lib):
     plan.close()
 
 
-@pytest.mark.parametrize("cfg,path", [(1, AUTO), (2, AUTO), (4, AUTO), (5, AUTO), (2, SIMPLE),
-                                      (4, SIMPLE)])
-def test_full_workload_parity(gpu_lib, cfg, path):
-    w = W.CONFIGS[cfg]
+@pytest.mark.parametrize("name,path", [("tiny", AUTO), ("deepseek", AUTO), ("softcap", AUTO),
+                                       ("batch", AUTO), ("deepseek", SIMPLE),
+                                       ("softcap", SIMPLE)])
+def test_full_workload_parity(gpu_lib, name, path):
+    w = W.BY_NAME[name]
     inp = W.make_call(w)
     toks, cache = U.run(gpu_lib, w, inp, path)
     rep = U.check(w, inp, toks, cache)
-    print(cfg, rep.summary())
+    print(name, rep.summary())
     assert rep.ok(), rep.summary()
 
 
@@ -225,8 +226,8 @@ def test_latency_workload_calls(gpu_lib):
 def test_tcgen05_chain_takes_the_chain_workloads(gpu_lib):
     # the head of every chain workload fits on chip: the chain path runs the
     # tcgen05 kernel and reports the whole head resident
-    for cfg in (1, 2, 3, 4):
-        w = W.CONFIGS[cfg]
+    for name in ("tiny", "deepseek", "latency", "softcap"):
+        w = W.BY_NAME[name]
         plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
         assert plan.query(gpu_lib.Q_RESIDENT_HEAD_BYTES) == w.vocab * w.rank * 2
         inp = W.make_call(w)
