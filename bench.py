@@ -215,6 +215,13 @@ def cpu_oracle_sample(seconds_hint: float = 20.0, name: str = DEFAULT_WORKLOAD,
                          f"{cores} thread(s)"), cores
 
 
+def reference_step_seconds(steps: int, warmup: int) -> float:
+    """Oracle seconds per reference-arm step: a bounded sample, sized so the
+    whole run stays near two minutes whatever K and W are (each step still
+    makes at least one oracle call)."""
+    return max(0.05, min(8.0, 120.0 / max(1, steps + warmup)))
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -222,9 +229,7 @@ def run_reference(args):
     vals = []
     desc = cores = None
     name = args.workload
-    # each step a bounded sample, sized so that the whole run stays near two
-    # minutes whatever K and W are (at least one oracle call per step)
-    per_step = max(0.05, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = reference_step_seconds(args.steps, args.warmup)
     for _ in range(args.warmup):
         cpu_oracle_sample(per_step, name)
     for _ in range(args.steps):
@@ -261,10 +266,7 @@ def run_gpu(args):
     name = args.workload
     w = W.BY_NAME[name]
     if args.rows:
-        # the workload with another row count (its padding rows below it kept)
-        w = w.with_(rows=args.rows, padding_rows=tuple(b for b in w.padding_rows
-                                                        if b < args.rows),
-                    name=f"{w.name} at rows={args.rows}")
+        w = W.with_rows(w, args.rows)
     base_f32, cache_f32 = args.base_dtype == "f32", args.cache_dtype == "f32"
     head, embed = W.make_weights(w)
     inp = W.make_call(w, base_f32=base_f32)

@@ -73,6 +73,12 @@ BY_NAME = {"tiny": TINY, "deepseek": DEEPSEEK, "latency": LATENCY, "softcap": SO
            "batch": BATCH}
 
 
+def with_rows(w: Workload, rows: int) -> Workload:
+    """The workload with another row count; its padding rows below it stay."""
+    return w.with_(rows=rows, padding_rows=tuple(b for b in w.padding_rows if b < rows),
+                   name=f"{w.name} at rows={rows}")
+
+
 def _randn_bf16(shape, std, g):
     return (torch.randn(shape, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
 
