@@ -151,9 +151,12 @@ markov_status markov_noise_join(markov_plan *plan, void *stream);
  *   logit_cache   device, BF16 [rows, N, V], element (b, i, v) at
  *                 b * cache_s0 + i * cache_s1 + v; pointer and strides
  *                 16-byte aligned (sharded_markov page, sample: cache asserts).
- * Rows up to markov_chain_max_rows take one persistent launch; larger calls
- * take the per-position kernels (sharded_markov page, module docstring:
- * larger batches take the fused loop).  EINVAL on a bad shape, stride,
+ * Rows up to markov_chain_max_rows take one persistent launch; Gumbel calls
+ * of up to 24 rows one persistent launch per 8-row slice (the noise hash
+ * takes each row's index in the call); larger calls take the per-position
+ * kernels (sharded_markov page, module docstring: larger batches take the
+ * fused loop).  The path actually taken and its launch count are reported by
+ * markov_plan_query.  EINVAL on a bad shape, stride,
  * alignment or mode; ENOTRESIDENT if the persistent grid cannot be
  * co-resident; ECUDA if a launch fails. */
 markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits,
