@@ -44,6 +44,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "gumbel_bounds.cuh"
 #include "tc.cuh"
 
 namespace dtm {
@@ -196,44 +197,6 @@ __device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__rest
 
 namespace {
 
-// One byte per (position, id, row) holding an upper bound on the Gumbel
-// value: q = ceil((bound + 4) * 12).  Every value the hash can give lies in
-// (-2.8, 16.7), so q fits a byte; q / 12 - 4 >= bound >= the exact value.
-__device__ __forceinline__ uint32_t quantize_upper(float g_up) {
-    const float t = ceilf(__fmul_rn(__fadd_rn(g_up, 4.0f), 12.0f));
-    return t < 0.0f ? 0u : (t > 255.0f ? 255u : (uint32_t)t);
-}
-__device__ __forceinline__ float dequantize_upper(uint32_t q) {
-    return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f) + 0.001f;
-}
-// A lower bound on the Gumbel value from the same byte: the fast estimate
-// lies within 2e-4 of the exact value and q - 1 < (estimate + 0.01 + 4) 12,
-// so the value exceeds (q - 1) / 12 - 4 - 0.0103.
-__device__ __forceinline__ float dequantize_lower(uint32_t q) {
-    return __fmaf_rn((float)q, 1.0f / 12.0f, -4.0f - 1.0f / 12.0f - 0.02f);
-}
-
-// The exact Gumbel key fp32(l / T) + gumbel of one id, given its hash.
-__device__ __forceinline__ float exact_key(float l, float T, uint64_t h) {
-    const float x = (T == 1.0f) ? l : __fdiv_rn(l, T);
-    return __fadd_rn(x, dm_gumbel_from_hash(h));
-}
-
-// An upper bound on gumbel = -log(-log u) for the u of hash h.  w = -ln u
-// from the hardware log2 (absolute error <= 2^-22 on [1/2, 2), 2 ulp
-// elsewhere) while u <= 0.999, where w >= 1e-3 keeps its relative error
-// below 2e-4; above, the series d + d^2/2 + d^3/3 of -ln(1 - d), d = 1 - u
-// (exact) <= 1e-3.  Then -ln w adds at most ~3e-6, so the estimate is within
-// 2e-4 of the exact value and the 0.01 margin makes it a bound.
-__device__ __forceinline__ float gumbel_upper(uint64_t h) {
-    const uint32_t m = (uint32_t)(h >> 41);
-    const float u = __fsub_rn(__uint_as_float(0x3f800000u | m), 0x1.fffffep-1f);
-    const float d = __fsub_rn(1.0f, u);
-    const float ws = d * (1.0f + d * (0.5f + d * (1.0f / 3.0f)));
-    const float wl = -__log2f(u) * 0.6931472f;
-    const float w = u > 0.999f ? ws : wl;
-    return -__log2f(w) * 0.6931472f + 0.01f;
-}
 
 // The noise-bound bytes of position p for this CTA's ids, 8 row bytes per
 // id, written by a group of NT threads (thread te takes ids v_begin + te +
@@ -440,12 +403,6 @@ __device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, f
     atomicMax(&c.cbest[i & 1][b], ((unsigned long long)o << 32) | ((unsigned long long)(0x3FFFFu - v) << 14));
 }
 
-// An upper bound on the Gumbel key of an id from its logit and noise byte.
-__device__ __forceinline__ float key_upper(float lf, float invT, uint32_t qb) {
-    const float xa = lf * invT;
-    return __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
-}
-
 // Two upper bounds as FP16 pair, rounded toward +inf (still upper bounds;
 // NaN stays NaN, beyond the FP16 range becomes +inf).
 __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
@@ -645,11 +602,10 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             const float lf = lf4[j];
             ku[j] = 0.0f;
             if ((gum_m >> j) & 1u) {
-                const float xa = lf * invT[j];
                 const uint32_t qb = (cq >> (8 * j)) & 0xffu;
-                const float kl = __fadd_rn(__fmaf_rn(fabsf(xa), -1e-5f, xa), dequantize_lower(qb));
+                const float kl = key_lower(lf, invT[j], qb);
                 lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
-                ku[j] = __fadd_rn(__fmaf_rn(fabsf(xa), 1e-5f, xa), dequantize_upper(qb));
+                ku[j] = key_upper(lf, invT[j], qb);
             } else if ((live_m >> j) & 1u) {
                 float key = lf;
                 if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[rb + j]);

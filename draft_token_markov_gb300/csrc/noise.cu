@@ -8,6 +8,7 @@
 // hash and two logarithms per element; each thread makes 4 consecutive ids
 // and stores them as one 16-byte vector.
 #include "common.cuh"
+#include "gumbel_bounds.cuh"
 
 namespace dtm {
 
@@ -52,11 +53,33 @@ cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
 
 __global__ void device_math_kernel(int fn, const float *__restrict__ x, float *__restrict__ y,
                                    int64_t n) {
+    if (fn == 9) {
+        // Gumbel key bounds on triples (l, T, uniform mantissa m as bits):
+        // the key's lower bound, its upper bound (from m's noise byte and
+        // the rounded 1 / T, as the chain computes them) and the exact key
+        for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; 3 * t + 2 < n;
+             t += (int64_t)gridDim.x * blockDim.x) {
+            const float l = x[3 * t], T = x[3 * t + 1];
+            const uint64_t h = (uint64_t)(__float_as_uint(x[3 * t + 2]) & 0x7fffffu) << 41;
+            const uint32_t q = quantize_upper(gumbel_upper(h));
+            const float invT = __fdiv_rn(1.0f, T);
+            y[3 * t] = key_lower(l, invT, q);
+            y[3 * t + 1] = key_upper(l, invT, q);
+            y[3 * t + 2] = exact_key(l, T, h);
+        }
+        return;
+    }
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         float v = x[j];
         float r;
         switch (fn) {
+            case 6:
+                // the noise byte of the uniform mantissa m (x holds m's bits)
+                r = (float)quantize_upper(gumbel_upper((uint64_t)(__float_as_uint(v) & 0x7fffffu) << 41));
+                break;
+            case 7: r = dequantize_upper((uint32_t)v); break;
+            case 8: r = dequantize_lower((uint32_t)v); break;
             case 0: r = dm_log(v); break;
             case 1: r = dm_exp(v); break;
             case 2: r = dm_tanh(v); break;

@@ -95,8 +95,10 @@ extern "C" markov_status markov_chain_sample_static(
     if (!(output_multiplier == output_multiplier) || output_multiplier - output_multiplier != 0.0f ||
         soft_cap != soft_cap)
         return MARKOV_EINVAL;
-    // the static scratch bounds: the noise of every row and position
-    if ((size_t)rows * N * V * sizeof(float) > kNoiseBytes) return MARKOV_EUNSUPPORTED;
+    // the static scratch bounds: the Gumbel noise of every row and position
+    // (inverse-CDF calls draw none)
+    if (mode == MARKOV_GUMBEL && (size_t)rows * N * V * sizeof(float) > kNoiseBytes)
+        return MARKOV_EUNSUPPORTED;
 
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return MARKOV_EDEVICE;

@@ -211,14 +211,20 @@ markov_status markov_chain_sample_typed(markov_plan *plan, const void *base_logi
  *   vocab, rank and num_steps given directly; it runs the noise kernel and
  *   the simple persistent chain (the MARKOV_PATH_CHAIN_SIMPLE path), so its
  *   outputs equal that path's bit for bit.
- *   Limits: rows <= 8, and rows * num_steps * vocab <= 8388608 (the noise
- *   must fit 32 MiB); larger calls return MARKOV_EUNSUPPORTED before any
- *   work is enqueued.  Every call clears the array's control words on
- *   `stream` first.  All calls share the array, which keeps the last call's
- *   contents: calls that may overlap on the GPU (other streams, other host
- *   threads) race and must be serialized by the caller.  A device-side bounded
- *   wait that gives up leaves that call's outputs incomplete; it is not
- *   reported (markov_plan_status needs a plan). */
+ *   Limits: rows <= 8; in MARKOV_GUMBEL mode also rows * num_steps * vocab
+ *   <= 8388608 (the Gumbel noise must fit 32 MiB; inverse-CDF calls draw no
+ *   noise and take any vocab up to the library's 262144).  Larger calls
+ *   return MARKOV_EUNSUPPORTED before any work is enqueued.  Every call
+ *   clears the array's control words on `stream` first.  All calls share the
+ *   array, which keeps the last call's contents: calls that may overlap on
+ *   the GPU (other streams, other host threads) race and must be serialized
+ *   by the caller.
+ *   Device-side errors are not reported (reporting needs a plan's
+ *   markov_plan_status), so the caller must pass valid device data: every
+ *   live row's anchor token in [0, vocab) (an anchor outside it samples from
+ *   id 0 and the call still returns MARKOV_OK).  The kernels' bounded waits
+ *   give up after a fixed 100 ms; a wait that gives up leaves that call's
+ *   outputs incomplete, also unreported. */
 markov_status markov_chain_sample_static(int32_t vocab, int32_t rank, int32_t num_steps,
                                          const uint16_t *base_logits, int64_t base_s0,
                                          int64_t base_s1, const uint16_t *head,
@@ -254,9 +260,16 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
  * -log(-log x), 4 fp32 -> BF16 round-to-nearest-even (result bits in the
  * low 16 bits of the output word, read as uint32), 5 the same rounding by
  * the packed two-value conversion the tcgen05 chain's epilogue uses (a NaN
- * gives some NaN; 0xDEAD if the two packed halves disagree).  These are the
- * functions the kernels use; exposed so they can be compared bit for bit with
- * an independent implementation.  EINVAL for an unknown fn. */
+ * gives some NaN; 0xDEAD if the two packed halves disagree).  The Gumbel
+ * pruning bounds of the tcgen05 chain: fn 6 the noise byte q of a uniform
+ * mantissa m < 2^23 passed as the input word's bits (u = (m + 1/2) 2^-23),
+ * fn 7 / 8 the upper / lower noise bound of the byte q passed as a float
+ * value; fn 9 on triples (l, T, m bits), n a multiple of 3: the Gumbel key's
+ * lower bound, its upper bound and the exact key fp32(l / T) + gumbel(u) as
+ * the chain computes them.  These are the functions the kernels use;
+ * exposed so they can be compared bit for bit with an independent
+ * implementation, or checked against it as bounds.  EINVAL for an unknown
+ * fn. */
 markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n,
                                  void *stream);
 

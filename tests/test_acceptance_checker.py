@@ -127,3 +127,46 @@ def test_typed_checker_accepts_oracle_and_rejects_mistakes():
         c3 = cache.copy()
         c3[1, 0, 0] = c3[2, 0, 0]                               # a padding row written
         assert not chk(toks, c3).ok()
+
+
+def test_no_vacuous_report_asserts():
+    # asserting a report's bound ok method (no call) is always true: every use
+    # must call it, and a report has no truth value of its own
+    import pathlib
+    import re
+    root = pathlib.Path(__file__).resolve().parent.parent
+    files = list((root / "tests").glob("*.py")) + [root / "__graft_entry__.py"]
+    bad = []
+    for f in files:
+        for n, line in enumerate(f.read_text().splitlines(), 1):
+            if re.search(r"\.ok\b(?!\s*\()", line) and "def ok" not in line:
+                bad.append(f"{f.name}:{n}")
+    assert not bad, bad
+    from tests.acceptance import Report
+    try:
+        bool(Report())
+    except TypeError:
+        pass
+    else:
+        raise AssertionError("a Report must not have a truth value")
+
+
+def test_typed_relaxation_is_one_ulp_without_cancellation():
+    # the fp32-cache rule's wider bias set comes from cancellation only: for
+    # dot products whose terms all have one sign it is the oracle's bias one
+    # ulp either way, and under cancellation it can be wider
+    from tests.acceptance import _bias_candidates, bf16_nudges
+    rng = np.random.default_rng(3)
+    r = 256
+    h = oracle.bf16_rne(np.abs(rng.standard_normal((64, r))).astype(np.float32) * 0.02)
+    e = oracle.bf16_rne(np.abs(rng.standard_normal((4, r))).astype(np.float32) * 0.02)
+    for v in range(64):
+        for p in range(4):
+            nb = set(bf16_nudges(oracle.bias_one(h, e, v, p)))
+            assert _bias_candidates(h, e, v, p) == nb, (v, p)
+    # cancellation: a row and its negation plus a tiny term
+    hc = np.concatenate([h[:1, : r // 2], h[:1, : r // 2]], axis=1).copy()
+    ec = np.concatenate([e[:1, : r // 2], e[:1, : r // 2] ^ np.uint16(0x8000)], axis=1).copy()
+    hc[0, 0] = oracle.bf16_rne(np.array([1e-4], np.float32))[0]
+    wide = _bias_candidates(hc, ec, 0, 0)
+    assert len(wide) > 3

@@ -67,3 +67,61 @@ def test_packed_bf16_rounding_bit_identical(gpu_lib):
     nan = np.isnan(x)
     assert np.array_equal(y[~nan], ref[~nan])
     assert np.all((y[nan] & 0x7FFF) > 0x7F80)
+
+
+def _uniform_of_mantissa(m: np.ndarray) -> np.ndarray:
+    return ((m.astype(np.float64) + 0.5) * 2.0**-23).astype(np.float32)
+
+
+def test_gumbel_noise_bounds_exhaustive(gpu_lib):
+    # the tcgen05 chain prunes Gumbel rows with one noise byte per (id, row):
+    # for every u the hash can give, the byte's lower and upper ends must
+    # bracket the exact noise the oracle computes, and the byte must not
+    # saturate (a saturated byte would not be a bound)
+    m = np.arange(1 << 23, dtype=np.uint32)
+    q = _dev(gpu_lib, 6, m.view(np.float32))
+    assert q.min() > 0.0 and q.max() < 255.0
+    assert np.array_equal(q, np.round(q))
+    lo = _dev(gpu_lib, 8, q)
+    hi = _dev(gpu_lib, 7, q)
+    u = _uniform_of_mantissa(m)
+    g = -oracle.log(-oracle.log(u))
+    assert np.all(lo <= g), float(np.max(lo - g))
+    assert np.all(g <= hi), float(np.max(g - hi))
+    # the byte is a useful bound: its upper end within a byte step of g
+    assert float(np.max(hi - g)) < 1.0 / 12.0 + 0.02
+
+
+def _key_triples(rng, n):
+    l = np.concatenate([
+        rng.standard_normal(n).astype(np.float32) * np.float32(3.0),
+        rng.standard_normal(n).astype(np.float32) * np.float32(300.0),
+        (rng.standard_normal(n) * 1e30).astype(np.float32),
+        np.array([0.0, -0.0, 1e-45, -1e-45, 1e-38, -1e-38, 3.3e38, -3.3e38, np.inf, -np.inf,
+                  64.0, -64.0], dtype=np.float32)])
+    Ts = np.array([0.05, 0.6, 1.0, 3.0], dtype=np.float32)
+    T = np.concatenate([Ts[rng.integers(0, 4, l.size - n)],
+                        np.exp(rng.uniform(-4.0, 2.5, n)).astype(np.float32)])
+    rng.shuffle(T)
+    m = rng.integers(0, 1 << 23, l.size, dtype=np.uint32)
+    return l, T, m
+
+
+def test_gumbel_key_bounds_bracket_the_exact_key(gpu_lib):
+    # key_lower <= fp32(l / T) + gumbel(u) <= key_upper for logits of every
+    # scale (BF16 and fp32 caches, overflowing quotients, infinities) and
+    # temperatures 0.05 .. 12; the device's exact key equals the oracle's
+    rng = np.random.default_rng(7)
+    l, T, m = _key_triples(rng, 1 << 20)
+    x = np.empty(3 * l.size, dtype=np.float32)
+    x[0::3], x[1::3], x[2::3] = l, T, m.view(np.float32)
+    y = _dev(gpu_lib, 9, x)
+    lo, hi, ex = y[0::3], y[1::3], y[2::3]
+    with np.errstate(over="ignore", invalid="ignore"):
+        q = np.where(T == np.float32(1.0), l, l / T).astype(np.float32)
+        key = (q + (-oracle.log(-oracle.log(_uniform_of_mantissa(m))))).astype(np.float32)
+    _same(ex, key)
+    lo = np.where(np.isnan(lo), -np.inf, lo)
+    hi = np.where(np.isnan(hi), np.inf, hi)
+    assert np.all(lo <= key), int(np.sum(~(lo <= key)))
+    assert np.all(key <= hi), int(np.sum(~(key <= hi)))

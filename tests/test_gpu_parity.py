@@ -8,11 +8,13 @@ import torch
 import oracle
 from draft_token_markov_gb300 import workloads as W
 from tests import gpu_util as U
+from tests import acceptance as A
 from tests.acceptance import check_typed
 
 pytestmark = pytest.mark.gpu
 
 AUTO, CHAIN, BATCH, SIMPLE = 0, 1, 2, 3
+PATH_NAMES = {AUTO: "auto", CHAIN: "chain", BATCH: "batch", SIMPLE: "simple"}
 
 SMALL = [
     W.small(16, 64, 1, 1, W.GUMBEL, seed=1, temperatures=(1.0,)),
@@ -205,22 +207,28 @@ def test_full_workload_parity(gpu_lib, name, path):
     inp = W.make_call(w)
     toks, cache = U.run(gpu_lib, w, inp, path)
     rep = U.check(w, inp, toks, cache)
-    print(name, rep.summary())
+    A.log(f"{name} ({PATH_NAMES[path]} path)", rep)
     assert rep.ok(), rep.summary()
 
 
 def test_latency_workload_calls(gpu_lib):
-    # the latency workload's calls differ in seed and anchor; a sample of them
+    # the latency workload's calls differ in seed and anchor: 125 of its 1000
+    # calls (every 8th), each checked against the oracle
     w = W.LATENCY
     h, e = W.make_weights(w)
     head, embed = h.cuda(), e.cuda()
     plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
-    for call in (0, 1, 499, 999):
-        inp = W.make_call(w, call)
-        toks, cache = U.run(gpu_lib, w, inp, AUTO, plan=plan, head=head, embed=embed)
-        rep = U.check(w, inp, toks, cache)
-        assert rep.ok(), (call, rep.summary())
-    plan.close()
+    total = A.Report()
+    try:
+        for call in range(0, 1000, 8):
+            inp = W.make_call(w, call)
+            toks, cache = U.run(gpu_lib, w, inp, AUTO, plan=plan, head=head, embed=embed)
+            total.merge(U.check(w, inp, toks, cache), tag=f"call {call}")
+    finally:
+        plan.close()
+    A.log("latency (125 calls, auto path)", total)
+    assert total.positions == 125 * w.steps
+    assert total.ok(), total.summary()
 
 
 def test_tcgen05_chain_takes_the_chain_workloads(gpu_lib):

@@ -5,7 +5,8 @@ scratch in a static device array instead of a plan.
 
 Called through the C ABI and compared, on two calls in a row, with the
 existing entry point's simple chain path, which runs the same kernels: the
-outputs must be identical.  This file is collected last on purpose."""
+outputs must be identical.  Both outputs also pass the oracle's acceptance
+check.  This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -13,6 +14,7 @@ import pytest
 import torch
 
 from draft_token_markov_gb300 import workloads as W
+from tests import acceptance as A
 from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
@@ -58,6 +60,21 @@ def test_static_scratch_entry_point_matches_plan_path(gpu_lib):
         ref = U.run(gpu_lib, w, inp, SIMPLE, head=head, embed=embed)
         assert np.array_equal(got[0], ref[0])
         assert np.array_equal(got[1], ref[1])
+        rep = U.check(w, inp, *got)
+        assert rep.ok(), rep.summary()
+
+
+def test_static_scratch_inverse_cdf_above_the_noise_limit(gpu_lib):
+    # inverse-CDF calls draw no Gumbel noise, so the noise bound does not
+    # apply to them: 8 rows x 16 positions x 262144 ids is accepted
+    w = W.small(262144, 64, 8, 16, W.INVCDF, seed=34, padding_rows=(5,),
+                temperatures=(0.0, 0.8, 1.0))
+    h, e = W.make_weights(w)
+    inp = W.make_call(w)
+    got = _run_static(gpu_lib, w, inp, h.cuda(), e.cuda())
+    rep = U.check(w, inp, *got)
+    A.log("allocation-free entry, inverse CDF V=262144 rows=8 N=16", rep)
+    assert rep.ok(), rep.summary()
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit(gpu_lib):
