@@ -85,3 +85,47 @@ def test_bf16_through_the_typed_entry_equals_the_bf16_call(gpu_lib):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("base_f32,cache_f32", [(True, True), (False, True)])
+def test_typed_full_deepseek_shape(gpu_lib, base_f32, cache_f32):
+    # the DeepSeek-V4.1-shaped chain (V=129280, r=256, 8 rows, 2 padding,
+    # N=8, Gumbel) with an fp32 cache on the tcgen05 chain; the record logs
+    # how often the fp32-cache rule needed a bias beyond one ulp
+    from tests import acceptance as A
+    w = W.DEEPSEEK
+    inp = W.make_call(w, base_f32=base_f32)
+    toks, cache = _run_typed(gpu_lib, w, inp, CHAIN, cache_f32)
+    _, _, hb, eb = U.weights(w)
+    rep = check_typed(inp, hb, eb, w.mode, w.mult, w.cap, toks, cache, cache_f32, U.SENT_T,
+                      SENT_F32_BITS, nthreads=U.NTHREADS)
+    A.log(f"deepseek {'f32' if base_f32 else 'bf16'} base, f32 cache (chain path)", rep)
+    assert rep.ok(), rep.summary()
+
+
+def test_typed_rule_needs_no_wide_bias_without_cancellation(gpu_lib):
+    # head and embed with non-negative entries: no dot product cancels, so
+    # every fp32 cache element is the oracle's or its bias one ulp away
+    w = W.small(12000, 256, 8, 3, W.GUMBEL, seed=77, padding_rows=(5,),
+                temperatures=(0.0, 0.6, 1.0))
+    h, e, _, _ = U.weights(w)
+    h, e = h.float().abs().to(torch.bfloat16), e.float().abs().to(torch.bfloat16)
+    import oracle
+    hb, eb = oracle.bf16_bits(h), oracle.bf16_bits(e)
+    inp = W.make_call(w)
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    try:
+        plan.set_path(CHAIN)
+        d = U.to_dev(inp)
+        toks = torch.full((w.rows, w.steps), U.SENT_T, dtype=torch.int64, device="cuda")
+        cache = torch.full((w.rows, w.steps, w.vocab), SENT_F32_BITS, dtype=torch.int32,
+                           device="cuda").view(torch.float32)
+        gpu_lib.markov_chain_sample(plan, d["base"], h.cuda(), e.cuda(), d["anchor"],
+                                    d["temperature"], d["seeds"], d["row_state_idx"], w.mode,
+                                    w.mult, w.cap, toks, cache)
+        assert gpu_lib.markov_plan_status(plan) == 0
+        t, c = toks.cpu().numpy(), cache.cpu().numpy()
+    finally:
+        plan.close()
+    rep = check_typed(inp, hb, eb, w.mode, w.mult, w.cap, t, c, True, U.SENT_T, SENT_F32_BITS,
+                      nthreads=U.NTHREADS)
+    assert rep.ok(), rep.summary()
+    assert rep.cache_bias_wide == 0, rep.summary()
