@@ -188,8 +188,9 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         int g = T_total < p->sm_count ? T_total : p->sm_count;
         const int max_tiles = (T_total + g - 1) / g;
         int occ = 0;
+        // (the inverse-CDF exchange reads the CTAs' sums 5 per lane: at most 160 CTAs)
         if (chain_tc_prepare() == cudaSuccess && chain_tc_occupancy(&occ) == cudaSuccess &&
-            occ >= 1 && max_tiles * (d.rank / 64) <= chain_tc_max_chunks()) {
+            occ >= 1 && max_tiles * (d.rank / 64) <= chain_tc_max_chunks() && g <= 160) {
             p->tc_ok = true;
             p->tc_grid = g;
         }
@@ -226,6 +227,7 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMemset(p->bwin, 0, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->bcnt, 0, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
@@ -483,6 +485,7 @@ markov_status markov_plan_status(markov_plan *p) {
     // counters, and forget every tagged exchange slot
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
