@@ -292,14 +292,26 @@ def run_gpu(args):
 
     stream = torch.cuda.current_stream(dev)
     L = api.lib()
+    # --calls C: C distinct calls (fresh seeds and anchors, drawn up front and
+    # staged on the device; the base logits are the workload's), one per step
+    calls = None
+    if args.calls:
+        per = [W.make_call(w, k, base_f32=base_f32) for k in range(args.calls)]
+        calls = {key: torch.stack([p[key] for p in per]).to(dev) for key in ("anchor", "seeds")}
+    call_no = [0]
 
     def step(evs=None):
         # one call: the persistent chain kernel draws the noise itself while
         # the head streams in, so a step is a single launch
+        anchor, seeds = d["anchor"], d["seeds"]
+        if calls is not None:
+            k = call_no[0] % args.calls
+            call_no[0] += 1
+            anchor, seeds = calls["anchor"][k], calls["seeds"][k]
         if evs:
             evs[0].record(stream)
-        api.markov_chain_sample(plan, d["base"], head, embed, d["anchor"], d["temperature"],
-                                d["seeds"], d["row_state_idx"], w.mode, w.mult, w.cap, toks,
+        api.markov_chain_sample(plan, d["base"], head, embed, anchor, d["temperature"],
+                                seeds, d["row_state_idx"], w.mode, w.mult, w.cap, toks,
                                 cache, stream)
         if evs:
             evs[1].record(stream)
@@ -329,6 +341,7 @@ def run_gpu(args):
                 flush_l2(k)
                 step()
             torch.cuda.synchronize()
+        call_no[0] = 0
         for k in range(args.steps):
             flush_l2(k)
             step(ev[k])
@@ -396,6 +409,7 @@ def run_gpu(args):
                    "steps_per_call": N,
                    "mode": "gumbel" if w.mode == W.GUMBEL else "inverse cdf", "l2": "flushed before every step (256 MB write, then a 256 MB read of another buffer)",
                    "parallelism": f"replicas x{world}", "path": path,
+                   "distinct_calls": args.calls or 1,
                    "resident_head_bytes": plan.query(api.Q_RESIDENT_HEAD_BYTES)},
         "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
                         "p99": sorted(step_ms)[min(len(step_ms) - 1,
@@ -440,6 +454,9 @@ def main():
                     help="element type of the logits cache")
     ap.add_argument("--path", default="auto", choices=["auto", "chain", "batch", "simple"],
                     help="force a path (default: the library's automatic choice)")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="time this many distinct calls (fresh seeds and anchors per call, staged "
+                         "on the device up front), one per timed step; sets --steps")
     ap.add_argument("--rows", type=int, default=0,
                     help="run the workload with this many rows instead of its own")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_NAMES,
@@ -447,6 +464,8 @@ def main():
                          "latency: 1 row; softcap: V=262144 r=128 inverse CDF; batch: 64 rows "
                          "(the per-position path); tiny: V=4096 r=64")
     args = ap.parse_args()
+    if args.calls:
+        args.steps = args.calls
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -12,41 +12,33 @@
 // Per CTA: a contiguous run of 128-id vocab tiles (at most 28 chunks of
 // [128 ids x 64 K]).  The first 15 chunks live in Tensor Memory as MMA A
 // operands (32 columns each), the rest in shared memory in the 128-byte
-// swizzled K-major layout the TMA writes.  The 32 free TMEM columns hold two
-// 16-column accumulators, and each accumulator takes TWO tiles at once: the
-// B operand (the 8 rows' embeddings, N = 16) is read through two views of
-// one shared-memory buffer, [E, 0] for the first tile (its bias lands in
-// columns 0-7) and [0, E] for the second (columns 8-15); each MMA adds
-// exact zeros to the other half.  Measured on GB300: one issuing warp costs
-// ~50 cycles per M=128, N=16, K=16 MMA whatever the A source, two issuing
-// warps ~25 cycles per MMA together, so two issuers with two tiles per
-// accumulator round give the tensor pipe four tiles in flight.
+// swizzled K-major layout the TMA writes; two 16-column TMEM accumulators
+// take the bias tiles.  Measured on GB300: an M=128, N=16, K=16 BF16 MMA
+// costs ~9 cycles with A in TMEM (enough issuing threads) and ~39 with A in
+// shared memory (bandwidth), and all MMA paths share one tensor pipe, so TMEM
+// holds as much of the head as fits.
 //
 // Warp roles (20 warps, 640 threads):
-//   0      issues the MMAs of the tiles whose A chunks start in TMEM, two
-//          tiles per round into accumulator 0
-//   1      the same for the shared-memory tiles, accumulator 1
+//   0, 1   the MMAs of the even / odd tiles into accumulator 0 / 1 (one
+//          elected lane each, one shared copy of the issue loop)
 //   2      lane 0: TMA producer of the head chunks (position 0 only); later
-//          positions: the next position's base logits into L2
+//          positions: the next position's base logits into L2, and during
+//          each exchange this CTA's candidate embedding rows into L2
 //   3      lane 0: copies the TMEM-resident chunks from their shared-memory
 //          staging slot into TMEM (position 0 only); later: base prefetch
-//   4-19   the epilogue: warp 4 + 4c + q reads TMEM lane quarter q of
-//          accumulator c / 2, half c % 2 (one tile), so each thread owns one
-//          vocab id and all 8 rows; at position 0, before it, the noise
-//          bounds of position 0 while the head streams in; after every
-//          position, the next position's noise bounds while the winners
-//          are exchanged
-//   0-3    after each position: the exchange of every row's key with the
-//          other CTAs and the staging of markov_embed[token] of rows w and
+//   4-19   the epilogue (warps 4-11 accumulator 0, 12-19 accumulator 1); at
+//          position 0, before it, the noise bounds of position 0 while the
+//          head streams in; after every position, the next position's
+//          noise bounds while the winners are exchanged
+//   0-3    after each position: warp 0 exchanges every row's key with the
+//          other CTAs, and warps 0-3 stage markov_embed[token] of rows w and
 //          w + 4 as the next position's B operand
-// Cross-CTA exchange: every CTA stores its per-row best key, tagged with the
-// call's position epoch, into its own slot of a [position][row][CTA] array;
-// every CTA polls all slots of its rows until every tag is current and
-// takes the maximum (one L2 round trip after the last store, no counter and
-// no second read).  Inverse-CDF rows exchange the maximum this way, then
-// per-CTA exact integer weight sums (tagged in their top bits); every CTA
-// then finds the CTA whose prefix range holds the target and scans that
-// CTA's cached logits itself (no third exchange).
+// Cross-CTA exchange (Gumbel and greedy rows): each CTA folds its per-row
+// best key into one word per (position, row) with red.max and then adds 1
+// to the position's counter (release); one thread per CTA polls the
+// counter (acquire, bounded) until all CTAs have counted and reads the
+// winners.  Inverse-CDF rows keep per-CTA slots tagged with the position
+// epoch (maximum, then sums and the owner's scan).
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -62,39 +54,36 @@ namespace {
 constexpr int kEpiWarps = 16;             // epilogue warps 4..19
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 128 + kEpiThreads;   // 4 control warps, then the epilogue warps
+constexpr int kRowsT = 4;                 // rows per epilogue thread
 constexpr int kTmemChunks = 15;           // A chunks in TMEM (32 columns each)
 constexpr int kSmemChunks = 13;           // A chunks in shared memory (16 KB each)
 constexpr int kMaxChunks = kTmemChunks + kSmemChunks;
 constexpr uint32_t kChunkBytes = 128 * 128;   // 128 rows x 64 BF16
 constexpr uint32_t kDCol = 480;           // accumulators: columns 480..495, 496..511
+constexpr uint32_t kBChunkBytes = 16 * 128;   // B operand: 16 rows x 64 BF16 per K-chunk
 constexpr uint32_t kIdesc = tc::idesc_bf16(128, 16);
 constexpr uint32_t kSmemHead = kSmemChunks * kChunkBytes;
-// B operand: per K-chunk kc an 8-row block E_kc (the rows' embeddings, 128 B
-// per row) between zero blocks: [Z][E_0][Z][E_1][Z][E_2][Z][E_3][Z], 1 KB
-// each; the view starting at E_kc is [E, 0], the one starting at the zero
-// block before it [0, E]
-constexpr uint32_t kSmemB = (2 * 4 + 1) * 1024;
+constexpr uint32_t kSmemB = 4 * kBChunkBytes;
 constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
-constexpr uint32_t kKeyTagMask = 0x3FFFu;   // packed key: ordered key 32 | id 18 | tag 14
-constexpr int kSumTagShift = 52;            // sum slots: tag 12 | sum 52
 
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
     uint64_t cpdone[kSmemChunks];    // slot s copied into TMEM
-    uint64_t accf[2];                // accumulator w holds a finished tile pair
-    uint64_t accr[2];                // accumulator w read out by its 8 epilogue warps
-    uint64_t fin[2];                 // issuer w's MMAs all complete (exit)
+    uint64_t dfull[2];               // accumulator b holds a finished tile
+    uint64_t dfree[2];               // accumulator b read out by its epilogue
+    uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
+    uint64_t bstaged;                // the next position's B operand is staged
+    uint64_t sdone;                  // the shared-memory tile's bias is in sbias
     // Per position parity (a position's values are read while the next
     // one's are written): per row, the CTA's best packed key and, for Gumbel
-    // rows, the CTA's threshold (ordered key of the largest key lower bound).
+    // rows, the CTA's threshold (ordered key of the largest key lower
+    // bound); the Gumbel survivor list and its length.
+    float sbias[128][kChainRows];    // the last tile's bias sums (mma.sync path)
     unsigned long long cbest[2][kChainRows];
     uint32_t lcta[2][kChainRows];
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
-    uint64_t wtot[kThreads / 32];    // inverse-CDF scan: per-warp weight totals
-    int cstar[kChainRows];           // inverse CDF: the CTA holding the target
-    uint64_t rem[kChainRows];        // the target minus the prefix before that CTA
-    uint32_t tok[kChainRows];        // the token the scan found
+    uint64_t scan[kThreads / 32];    // inverse-CDF scan: per-warp weight totals
     uint32_t tmem_base;
     uint32_t tmem_ready;             // chunks copied into TMEM so far
     uint32_t abort;
@@ -143,7 +132,7 @@ __device__ __forceinline__ void clear_position(Ctl &c, int par) {
 }
 
 // This CTA's abort flag (shared memory: cheap enough for hot loops).
-__device__ __forceinline__ bool aborted(const Ctl &c) {
+__device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &) {
     return *(volatile const uint32_t *)&c.abort != 0u;
 }
 
@@ -159,24 +148,63 @@ __device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a, bool glob
     return s;
 }
 
+// packed key: ordered key (32) | 0x3FFFF - id (18) | epoch tag (14)
 __device__ __forceinline__ uint32_t unpack_id(uint64_t p) {
     return 0x3FFFFu - (uint32_t)((p >> 14) & 0x3FFFFu);
 }
 
-// The tiles of CTA `cta` of G: [t0, t1) of T_total 128-id tiles.
-__device__ __forceinline__ void cta_tiles(int cta, int G, int T_total, int &t0, int &t1) {
-    t0 = (int)((int64_t)cta * T_total / G);
-    t1 = (int)((int64_t)(cta + 1) * T_total / G);
+// Row b's maximum over all CTAs' slots, once every slot carries `tag`.  A
+// round issues all of its loads before it looks at any (a compile-time
+// bound: with a loop over the runtime CTA count the loads went out one L2
+// round trip apart, and a round took microseconds).
+constexpr int kMaxGrid = 160;             // CTAs the exchanges take
+__device__ __forceinline__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t deadline,
+                         const SampleArgs &a, uint64_t &out) {
+    constexpr int kPer = kMaxGrid / 32;
+    const int lane = threadIdx.x & 31;
+    for (uint32_t spin = 0;; ++spin) {
+        uint64_t k[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            k[u] = lane + 32 * u < G ? tc::ld_relaxed_u64(slots + lane + 32 * u) : (uint64_t)tag;
+        bool fresh = true;
+        uint64_t m = 0ull;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            if ((uint32_t)(k[u] & 0x3FFFu) != tag) fresh = false;
+            m = k[u] > m ? k[u] : m;
+        }
+        if (__all_sync(0xffffffffu, fresh)) {
+            out = tc::warp_max_u64(m);
+            return true;
+        }
+        if ((spin & 15u) == 15u) {
+            bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
+            if (__any_sync(0xffffffffu, bad)) return false;
+        }
+    }
 }
 
-// Stage 8 elements of markov_embed[p] (16-byte piece `lane` of the row) as
-// row b of the B operand's E blocks (K-major, 128-byte swizzle: piece k of
-// row b at piece k ^ b).
+}  // namespace
+
+namespace {
+
+// Stage markov_embed[p] as row b of the B operand (16 rows x RANK, K-major,
+// 128-byte swizzle, one 2 KB block per 64-element K-chunk).
 template <int RANK>
-__device__ __forceinline__ void stage_row(uint8_t *b_s, const uint4 v, int b, int lane) {
-    const int chunk = lane >> 3, piece = lane & 7;
-    *reinterpret_cast<uint4 *>(b_s + (2 * chunk + 1) * 1024 + b * 128 + ((piece ^ b) << 4)) = v;
+__device__ __forceinline__ void stage_embed(uint8_t *b_s, const uint16_t *__restrict__ embed,
+                                            int64_t p, int b, int lane) {
+    if (lane < RANK / 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(embed + p * RANK + 8 * lane);
+        const int chunk = lane >> 3, piece = lane & 7;
+        *reinterpret_cast<uint4 *>(b_s + chunk * kBChunkBytes + b * 128 + ((piece ^ b) << 4)) = v;
+    }
 }
+
+}  // namespace
+
+namespace {
+
 
 // The noise-bound bytes of position p for this CTA's ids, 8 row bytes per
 // id, written by a group of NT threads (thread te takes ids v_begin + te +
@@ -248,100 +276,134 @@ __device__ __noinline__ float transform_f32(float s, const Transform &tf) {
     return y;
 }
 
-// Tiles of issuer w: [0, n0) for issuer 0 (their first chunk is in TMEM),
-// [n0, nt) for issuer 1; each round takes two of them (a pair).
-__device__ __forceinline__ int issuer_first(int w, int n0) { return w == 0 ? 0 : n0; }
-__device__ __forceinline__ int issuer_last(int w, int n0, int nt) { return w == 0 ? n0 : nt; }
-
-// The MMAs of issuer W (warp W) at position i: per round a tile pair (ta,
-// tb) into accumulator W, ta through the [E, 0] view of B (columns 0-7) and
-// tb through [0, E] (columns 8-15); per tile, K chunk by K chunk, 4 MMAs
-// of K = 16, with A in TMEM (chunk j < kTmemChunks) or in shared memory.
-// The first MMA of ta starts the accumulator (its [E, 0] view also zeroes
-// tb's half), all others accumulate.  The whole warp runs the loop and one
-// elected lane issues.  Position 0 awaits each chunk as the head streams in.
+// The MMAs of accumulator W (issued by warp W): tiles W, W + 2, ...; per
+// tile, K chunk by K chunk, 4 MMAs of K = 16 each, with A in TMEM (chunk j
+// < kTmemChunks) or in shared memory.  The whole warp runs the loop and one
+// elected lane issues.  Both warps run one copy of this code, kept small:
+// the kernel's code is far larger than the SM's instruction caches, and an
+// unrolled issue loop (16 KB per copy) measured several times slower inside
+// the kernel than alone, its fetches competing with the epilogue's.
+// Position 0 awaits each chunk as the head streams in.
 template <int RANK>
 __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const uint32_t tmem, const int W,
-                                            const int i, const int n0, const int nt, const int ntm,
+                                            const int i, const int nt, const int ntm,
                                             const uint32_t b_sa, const uint32_t head_sa,
                                             const uint64_t timeout, uint32_t &uses) {
     constexpr int cpt = RANK / 64;
     const int lane = threadIdx.x & 31;
     const uint32_t d = tmem + kDCol + 16u * (uint32_t)W;
     const uint64_t bdesc0 = tc::sw128_desc(b_sa), adesc0 = tc::sw128_desc(head_sa);
-    const int first = issuer_first(W, n0), last = issuer_last(W, n0, nt);
 #pragma unroll 1
-    for (int ta = first; ta < last; ta += 2) {
-        if (__any_sync(0xffffffffu, aborted(c))) break;
+    for (int k = W; k < nt; k += 2) {
+        if (__any_sync(0xffffffffu, aborted(c, a))) break;
         bool freed = true;
         if (uses > 0)
-            freed = tc::mbar_wait(tc::smem_u32(&c.accr[W]), (uses - 1) & 1u, tc::now_ns() + timeout);
+            freed = tc::mbar_wait(tc::smem_u32(&c.dfree[W]), (uses - 1) & 1u, tc::now_ns() + timeout);
         if (!__all_sync(0xffffffffu, freed)) {
             if (lane == 0) fail(c, a, 4u, 0x1000u + i);
             break;
         }
         tc::fence_after_sync();
         bool ok = true;
-        const int ntile = ta + 1 < last ? 2 : 1;
 #pragma unroll 1
-        for (int h = 0; h < ntile && ok; ++h) {
-            const int k = ta + h;
-            // [E, 0] starts at E_kc (block 2 kc + 1), [0, E] at block 2 kc
-            const uint64_t bview = bdesc0 + (uint64_t)(h == 0 ? (1024 >> 4) : 0);
-#pragma unroll 1
-            for (int kc = 0; kc < cpt; ++kc) {
-                const int j = k * cpt + kc;
-                if (i == 0) {
-                    const uint64_t dl = tc::now_ns() + timeout;
-                    if (j < kTmemChunks) {
-                        while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
-                            if (tc::now_ns() > dl || aborted(c)) { ok = false; break; }
-                        }
-                        tc::fence_after_sync();
-                    } else {
-                        // a parity wait only tells phases apart one at a time:
-                        // every earlier load of this slot (the TMEM chunks
-                        // staged in it) must be complete first
-                        while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
-                            if (tc::now_ns() > dl || aborted(c)) { ok = false; break; }
-                        }
-                        int s;
-                        uint32_t u;
-                        chunk_slot(j, ntm, s, u);
-                        if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
-                    }
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) {
-                        if (lane == 0) fail(c, a, 4u, 0x2000u + j);
-                        break;
-                    }
-                }
-                // descriptors advance by (bytes >> 4) in their address field
-                const uint64_t bd = bview + (uint64_t)((kc * 2048) >> 4);
-                const uint32_t acc0 = (h == 0 && kc == 0) ? 0u : 1u;
+        for (int kc = 0; kc < cpt; ++kc) {
+            const int j = k * cpt + kc;
+            if (i == 0) {
+                const uint64_t dl = tc::now_ns() + timeout;
                 if (j < kTmemChunks) {
-                    const uint32_t at = tmem + 32u * (uint32_t)j;
-                    tc::mma_tmemA_elect(d, at, bd, kIdesc, acc0);
-                    tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
-                    tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
-                    tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
+                    while (*(volatile uint32_t *)&c.tmem_ready <= (uint32_t)j) {
+                        if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                    }
+                    tc::fence_after_sync();
                 } else {
-                    const uint64_t ad = adesc0 + (uint64_t)(((uint32_t)(j - kTmemChunks) * kChunkBytes) >> 4);
-                    tc::mma_smemA_elect(d, ad, bd, kIdesc, acc0);
-                    tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
-                    tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
-                    tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
+                    // a parity wait only tells phases apart one at a time:
+                    // every earlier load of this slot (the TMEM chunks
+                    // staged in it) must be complete first
+                    while (*(volatile uint32_t *)&c.tmem_ready < (uint32_t)ntm) {
+                        if (tc::now_ns() > dl || aborted(c, a)) { ok = false; break; }
+                    }
+                    int s;
+                    uint32_t u;
+                    chunk_slot(j, ntm, s, u);
+                    if (ok) ok = tc::mbar_wait(tc::smem_u32(&c.full[s]), u & 1u, dl);
                 }
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) fail(c, a, 4u, 0x2000u + j);
+                    break;
+                }
+            }
+            // descriptors advance by (bytes >> 4) in their address field
+            const uint64_t bd = bdesc0 + (uint64_t)((kc * kBChunkBytes) >> 4);
+            const uint32_t acc0 = kc == 0 ? 0u : 1u;
+            if (j < kTmemChunks) {
+                const uint32_t at = tmem + 32u * (uint32_t)j;
+                tc::mma_tmemA_elect(d, at, bd, kIdesc, acc0);
+                tc::mma_tmemA_elect(d, at + 8u, bd + 2u, kIdesc, 1u);
+                tc::mma_tmemA_elect(d, at + 16u, bd + 4u, kIdesc, 1u);
+                tc::mma_tmemA_elect(d, at + 24u, bd + 6u, kIdesc, 1u);
+            } else {
+                const uint64_t ad = adesc0 + (uint64_t)(((uint32_t)(j - kTmemChunks) * kChunkBytes) >> 4);
+                tc::mma_smemA_elect(d, ad, bd, kIdesc, acc0);
+                tc::mma_smemA_elect(d, ad + 2u, bd + 2u, kIdesc, 1u);
+                tc::mma_smemA_elect(d, ad + 4u, bd + 4u, kIdesc, 1u);
+                tc::mma_smemA_elect(d, ad + 6u, bd + 6u, kIdesc, 1u);
             }
         }
         if (!ok) break;
-        tc::commit_elect(tc::smem_u32(&c.accf[W]));
+        tc::commit_elect(tc::smem_u32(&c.dfull[W]));
         ++uses;
     }
     __syncwarp();
 }
 
-// The exact Gumbel key of survivor (id v, row b, cached logit lf) folded
+// The bias sums of tile `kt` (its 4 K chunks in shared memory, 128-byte
+// swizzled K-major as the TMA wrote them) for ids 16 m .. 16 m + 15 and the
+// 8 rows, by one warp: 16 mma.sync m16n8k16 (BF16 in, fp32 sums) with
+// fragments from ldmatrix, into c.sbias.  The sums' order differs from the
+// tcgen05 tiles' only in the last bit of a few fp32 sums.
+template <int RANK>
+__device__ __forceinline__ void simt_tile(Ctl &c, int kt, int ntm, int m, uint32_t b_sa,
+                                          uint32_t head_sa) {
+    constexpr int cpt = RANK / 64;
+    const int lane = threadIdx.x & 31;
+    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;
+    const int mi = lane >> 3;                       // ldmatrix.x4: matrix of this lane's address
+    const int ra = 16 * m + (mi & 1) * 8 + (lane & 7);   // A row (id within the tile)
+    const int nb = lane & 7, hb = (lane >> 3) & 1;       // ldmatrix.x2: B row, K half
+#pragma unroll 1
+    for (int kc = 0; kc < cpt; ++kc) {
+        int slot;
+        uint32_t ph;
+        chunk_slot(kt * cpt + kc, ntm, slot, ph);
+        const uint32_t sa = head_sa + (uint32_t)slot * kChunkBytes + (uint32_t)ra * 128u;
+        const uint32_t sb = b_sa + (uint32_t)kc * kBChunkBytes + (uint32_t)nb * 128u;
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+            const uint32_t ua = (uint32_t)(2 * sub + (mi >> 1)) ^ (uint32_t)(ra & 7);
+            const uint32_t ub = (uint32_t)(2 * sub + hb) ^ (uint32_t)nb;
+            uint32_t a0, a1, a2, a3, b0, b1;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(sa + (ua << 4)));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                         : "=r"(b0), "=r"(b1)
+                         : "r"(sb + (ub << 4)));
+            asm volatile(
+                "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    }
+    const int id = 16 * m + (lane >> 2), col = (lane & 3) * 2;
+    c.sbias[id][col] = d0;
+    c.sbias[id][col + 1] = d1;
+    c.sbias[id + 8][col] = d2;
+    c.sbias[id + 8][col + 1] = d3;
+}
+
+// The exact key of Gumbel survivor (id v, row b, cached logit lf) folded
 // into the CTA's best key of that row (shared-memory atomic maximum).
 __device__ __forceinline__ void survivor_key(Ctl &c, int i, uint32_t v, int b, float lf) {
     const uint64_t h = dm_splitmix64(c.hri[i][b] ^ (uint64_t)v);
@@ -355,10 +417,12 @@ __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
     return __halves2half2(__float2half_ru(lo), __float2half_ru(hi));
 }
 
-// The epilogue of one position, run by the 16 warps 4-19: warp 4 + 4 cm + q
-// serves accumulator W = cm / 2, half hh = cm % 2 (the pair's first or
-// second tile), TMEM lane quarter q (the only lanes a warp may read), so
-// each thread owns one id per tile and all 8 rows (the tile's 8 columns).
+// The epilogue of one position, run by the 16 warps 4-19: warp 4 + ew
+// serves accumulator wg = ew / 8 (the even / odd tiles), TMEM lane quarter
+// q = warp % 4 (the only lanes a warp may read) and rows rb..rb+3, rb =
+// 4 ((ew / 4) % 2), so each thread owns one id per tile and 4 of the 8 rows
+// (the MMA's N columns).  Two warps per lane quarter halve every thread's
+// dependent chains, which bound this code.
 //
 // Pass 1, per tile as its bias arrives: the cached logits (two rows per
 // packed BF16 conversion), written out; for rows whose key is exact here
@@ -376,124 +440,146 @@ __device__ __forceinline__ __half2 half2_up(float lo, float hi) {
 // (some row is a Gumbel row) is CTA-uniform.
 template <int RANK, bool kCdf, int DT>
 __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint32_t tmem,
-                                         const int i, const int t0, const int n0, const int nt,
+                                         const int i, const int t0, const int nt, const int nts,
+                                         const int ntm, const uint32_t b_sa, const uint32_t head_sa,
                                          const bool gum_any, const uint64_t timeout, uint32_t &dcount) {
-    // tiles a warp may see per position: 2 at rank 256 (the pass-2 queue is
-    // kept in registers), more at smaller ranks (read back from L2)
-    constexpr bool kRegs = RANK == 256;
+    constexpr int cpt = RANK / 64;
+    constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
+    constexpr bool kRegs = kTilesWG <= 4;                  // pass-2 tiles kept in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ew = warp - 4, q = warp & 3, cm = ew >> 2, W = cm >> 1, hh = cm & 1;
-    const int first = issuer_first(W, n0), last = issuer_last(W, n0, nt);
+    const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1, rb = kRowsT * hr;
     const int V = a.V;
     const int par = i & 1;
-    uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;   // bit b = row b
+    uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;   // this thread's 4 rows, bit j = row rb + j
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        live_m |= c.live[b] ? (1u << b) : 0u;
-        samp_m |= c.sampling[b] ? (1u << b) : 0u;
-        div_m |= (c.sampling[b] && c.T[b] != 1.0f) ? (1u << b) : 0u;
+    for (int j = 0; j < kRowsT; ++j) {
+        live_m |= c.live[rb + j] ? (1u << j) : 0u;
+        samp_m |= c.sampling[rb + j] ? (1u << j) : 0u;
+        div_m |= (c.sampling[rb + j] && c.T[rb + j] != 1.0f) ? (1u << j) : 0u;
     }
     // Gumbel rows get the bound treatment; inverse-CDF rows divide by T
     const uint32_t gum_m = kCdf ? 0u : (samp_m & live_m);
     div_m = kCdf ? (div_m & live_m) : 0u;
-    const uint2 *gq = reinterpret_cast<const uint2 *>(a.noise) + (int64_t)i * V;
+    const uint32_t *gq = reinterpret_cast<const uint32_t *>(a.noise) + ((int64_t)i * V) * 2 + hr;
     // DT bit 0: fp32 base logits, bit 1: fp32 cache (else BF16)
     constexpr bool kBaseF32 = (DT & 1) != 0, kCacheF32 = (DT & 2) != 0;
-    const int64_t bofs = (int64_t)i * a.base_s1;
-    const int64_t cofs = (int64_t)i * a.cache_s1;
+    const int64_t bofs = (int64_t)i * a.base_s1 + rb * a.base_s0;
+    const int64_t cofs = (int64_t)i * a.cache_s1 + rb * a.cache_s0;
     const uint16_t *base_i = kBaseF32 ? nullptr : a.base + bofs;
     const float *base_fi = kBaseF32 ? a.base_f + bofs : nullptr;
     uint16_t *cache_i = kCacheF32 ? nullptr : a.cache + cofs;
     float *cache_fi = kCacheF32 ? a.cache_f + cofs : nullptr;
 
-    // exact-key rows: the best ordered key and its id; Gumbel rows: the
-    // largest key lower bound (float bits) in bo
-    uint32_t bo[kChainRows], bv[kChainRows];
+    uint32_t bo[kRowsT], bv[kRowsT];   // best ordered (exact) key and its id
+    float lbm[kRowsT], invT[kRowsT];   // Gumbel rows: largest key lower bound
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        bo[b] = ((gum_m >> b) & 1u) ? 0xff800000u : 0u;
-        bv[b] = 0u;
+    for (int j = 0; j < kRowsT; ++j) {
+        bo[j] = 0u;
+        bv[j] = 0u;
+        lbm[j] = __uint_as_float(0xff800000u);
+        invT[j] = c.invT[rb + j];
     }
-    // the last 2 tiles' packed logits and FP16 key upper bounds, newest first
-    uint32_t k0[4] = {0u, 0u, 0u, 0u}, k1[4] = {0u, 0u, 0u, 0u};
-    __half2 u0[4], u1[4];
+    // the last 4 tiles' packed logits and FP16 key upper bounds (rows j, j+1)
+    // newest first
+    uint32_t k0[2] = {0u, 0u}, k1[2] = {0u, 0u}, k2[2] = {0u, 0u}, k3[2] = {0u, 0u};
+    __half2 u0[2], u1[2], u2[2], u3[2];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) u0[j] = u1[j] = __float2half2_rn(0.0f);
-    // the next tile's base logits: fp32 bits per row, or BF16 pairs (rows
-    // 2j, 2j + 1 in the low / high half of word j)
-    constexpr int kNB = kBaseF32 ? kChainRows : kChainRows / 2;
-    uint32_t nb[kNB];
-    uint2 nq;
-    auto load_tile = [&](int k, uint32_t (&bb)[kNB], uint2 &qq) {
+    for (int j = 0; j < 2; ++j) u0[j] = u1[j] = u2[j] = u3[j] = __float2half2_rn(0.0f);
+    uint32_t nb[kRowsT];
+    uint32_t nq;
+    auto load_tile = [&](int k, uint32_t (&bb)[kRowsT], uint32_t &qq) {
         const int v = (t0 + k) * 128 + q * 32 + lane;
-        const bool ok2 = k < last && v < V;
-        if (kBaseF32) {
+        const bool ok2 = k < nt && v < V;
 #pragma unroll
-            for (int b = 0; b < kChainRows; ++b)
-                bb[b % kNB] = (ok2 && ((live_m >> b) & 1u)) ? __float_as_uint(__ldg(base_fi + b * a.base_s0 + v)) : 0u;
-        } else {
-#pragma unroll
-            for (int j = 0; j < kChainRows / 2; ++j) {
-                const uint32_t lo = (ok2 && ((live_m >> (2 * j)) & 1u)) ? (uint32_t)__ldg(base_i + (2 * j) * a.base_s0 + v) : 0u;
-                const uint32_t hi = (ok2 && ((live_m >> (2 * j + 1)) & 1u)) ? (uint32_t)__ldg(base_i + (2 * j + 1) * a.base_s0 + v) : 0u;
-                bb[j] = lo | (hi << 16);
-            }
-        }
-        qq = (ok2 && gum_m != 0u) ? __ldcg(gq + v) : make_uint2(0u, 0u);
+        for (int j = 0; j < kRowsT; ++j)
+            bb[j] = (ok2 && ((live_m >> j) & 1u))
+                        ? (kBaseF32 ? __float_as_uint(__ldg(base_fi + j * a.base_s0 + v))
+                                    : (uint32_t)__ldg(base_i + j * a.base_s0 + v))
+                        : 0u;
+        qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
-    load_tile(first + hh, nb, nq);
+    load_tile(wg, nb, nq);
     bool ok = true;
+    if (nts >= 0 && wg == 1) {
+        // group 1, before its first tile: the bias of tile nts, 16 ids per
+        // warp, with mma.sync (m16n8k16, fp32 sums) from the tile's shared-
+        // memory A chunks and the staged B rows, into sbias
+        bool st = true;
+        if (lane == 0)
+            st = tc::mbar_wait(tc::smem_u32(&c.bstaged), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+        st = __shfl_sync(0xffffffffu, st, 0);
+        if (!st) {
+            if (lane == 0) fail(c, a, 4u, 0xC000u + i);
+        } else {
+            simt_tile<RANK>(c, nts, ntm, ew - 8, b_sa, head_sa);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.sdone));
+    }
     int ntw = 0;   // tiles this warp processed
 #pragma unroll 1
-    for (int ta = first; ta < last; ta += 2) {
-        const int k = ta + hh;
-        const bool has = k < last;
-        uint32_t cb[kNB];
+    for (int k = wg; k < nt; k += 2) {
+        uint32_t cb[kRowsT];
 #pragma unroll
-        for (int b = 0; b < kNB; ++b) cb[b] = nb[b];
-        const uint2 cq = nq;
+        for (int j = 0; j < kRowsT; ++j) cb[j] = nb[j];
+        const uint32_t cq = nq;
         load_tile(k + 2, nb, nq);
-        if (lane == 0)
-            ok = tc::mbar_wait(tc::smem_u32(&c.accf[W]), dcount & 1u, tc::now_ns() + timeout);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) {
-            if (lane == 0) fail(c, a, 4u, 0x6000u + i);
+        if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) {
+            ok = false;
             break;
         }
-        ++dcount;
-        tc::fence_after_sync();
-        uint32_t r[8];
-        if (has) {
-            tc::ld_32x32b_x8(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * W + 8u * hh, r);
+        uint32_t r[4];
+        if (k == nts) {
+            // the mma.sync tile (group 0's last): its bias from sbias
+            if (lane == 0)
+                ok = tc::mbar_wait(tc::smem_u32(&c.sdone), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(c, a, 4u, 0xD000u + i);
+                break;
+            }
+            const float4 sb = *reinterpret_cast<const float4 *>(&c.sbias[q * 32 + lane][rb]);
+            r[0] = __float_as_uint(sb.x);
+            r[1] = __float_as_uint(sb.y);
+            r[2] = __float_as_uint(sb.z);
+            r[3] = __float_as_uint(sb.w);
+        } else {
+            if (lane == 0)
+                ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) fail(c, a, 4u, 0x6000u + i);
+                break;
+            }
+            ++dcount;
+            tc::fence_after_sync();
+            tc::ld_32x32b_x4(tmem + ((uint32_t)(q * 32) << 16) + kDCol + 16u * wg + (uint32_t)rb, r);
             tc::wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.dfree[wg]));
         }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.accr[W]));
-        if (!has) continue;
         // nothing that waits on this tile's base loads may be scheduled
         // before the accumulator is handed back
 #pragma unroll
-        for (int b = 0; b < kNB; ++b) asm volatile("" : "+r"(cb[b]));
-#pragma unroll
-        for (int b = 0; b < 8; ++b) asm volatile("" : "+r"(r[b]));
+        for (int j = 0; j < kRowsT; ++j) asm volatile("" : "+r"(cb[j]));
+        asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
         const int v = (t0 + k) * 128 + q * 32 + lane;
         const bool valid = v < V;
         // bias = bf16(sum); logit = cache_round(f32(base) + f32(bias)), two
         // rows a time (BF16 caches: packed; fp32 caches: kept in fp32)
-        uint32_t lp[4];
-        float lf8[kChainRows];
+        uint32_t lp[2];
+        float lf4[kRowsT];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const uint32_t bb = bf16x2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            const float b0 = kBaseF32 ? __uint_as_float(cb[(2 * j) % kNB]) : __uint_as_float(cb[j % kNB] << 16);
-            const float b1 = kBaseF32 ? __uint_as_float(cb[(2 * j + 1) % kNB])
-                                      : __uint_as_float(cb[j % kNB] & 0xffff0000u);
+            const float b0 = kBaseF32 ? __uint_as_float(cb[2 * j]) : __uint_as_float(cb[2 * j] << 16);
+            const float b1 = kBaseF32 ? __uint_as_float(cb[2 * j + 1]) : __uint_as_float(cb[2 * j + 1] << 16);
             const float s0 = __fadd_rn(b0, __uint_as_float(bb << 16));
             const float s1 = __fadd_rn(b1, __uint_as_float(bb & 0xffff0000u));
             if (kCacheF32) {
-                lf8[2 * j] = s0;
-                lf8[2 * j + 1] = s1;
+                lf4[2 * j] = s0;
+                lf4[2 * j + 1] = s1;
             } else {
                 lp[j] = bf16x2_rn(s0, s1);
             }
@@ -501,49 +587,53 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         if (kCacheF32) {
             if (a.tf.has_transform) {
 #pragma unroll
-                for (int b = 0; b < kChainRows; ++b) lf8[b] = transform_f32(lf8[b], a.tf);
+                for (int j = 0; j < kRowsT; ++j) lf4[j] = transform_f32(lf4[j], a.tf);
             }
 #pragma unroll
-            for (int b = 0; b < kChainRows; ++b)
-                if (valid && ((live_m >> b) & 1u)) cache_fi[b * a.cache_s0 + v] = lf8[b];
+            for (int j = 0; j < kRowsT; ++j)
+                if (valid && ((live_m >> j) & 1u)) cache_fi[j * a.cache_s0 + v] = lf4[j];
         } else {
             if (a.tf.has_transform) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) lp[j] = transform_pair(lp[j], a.tf);
+                lp[0] = transform_pair(lp[0], a.tf);
+                lp[1] = transform_pair(lp[1], a.tf);
             }
 #pragma unroll
-            for (int b = 0; b < kChainRows; ++b) {
-                lf8[b] = __uint_as_float((b & 1) ? (lp[b >> 1] & 0xffff0000u) : (lp[b >> 1] << 16));
-                if (valid && ((live_m >> b) & 1u))
-                    cache_i[b * a.cache_s0 + v] = (uint16_t)(lp[b >> 1] >> (16 * (b & 1)));
+            for (int j = 0; j < kRowsT; ++j) {
+                lf4[j] = __uint_as_float((j & 1) ? (lp[j >> 1] & 0xffff0000u) : (lp[j >> 1] << 16));
+                if (valid && ((live_m >> j) & 1u))
+                    cache_i[j * a.cache_s0 + v] = (uint16_t)(lp[j >> 1] >> (16 * (j & 1)));
             }
         }
-        float ku[kChainRows];
+        float ku[kRowsT];
 #pragma unroll
-        for (int b = 0; b < kChainRows; ++b) {
-            const float lf = lf8[b];
-            ku[b] = 0.0f;
-            if ((gum_m >> b) & 1u) {
-                const uint32_t qb = ((b < 4 ? cq.x : cq.y) >> (8 * (b & 3))) & 0xffu;
-                const float kl = key_lower(lf, c.invT[b], qb);
-                bo[b] = (valid && kl > __uint_as_float(bo[b])) ? __float_as_uint(kl) : bo[b];
-                ku[b] = key_upper(lf, c.invT[b], qb);
-            } else if ((live_m >> b) & 1u) {
+        for (int j = 0; j < kRowsT; ++j) {
+            const float lf = lf4[j];
+            ku[j] = 0.0f;
+            if ((gum_m >> j) & 1u) {
+                const uint32_t qb = (cq >> (8 * j)) & 0xffu;
+                const float kl = key_lower(lf, invT[j], qb);
+                lbm[j] = (valid && kl > lbm[j]) ? kl : lbm[j];
+                ku[j] = key_upper(lf, invT[j], qb);
+            } else if ((live_m >> j) & 1u) {
                 float key = lf;
-                if (kCdf && ((div_m >> b) & 1u)) key = __fdiv_rn(lf, c.T[b]);
+                if (kCdf && ((div_m >> j) & 1u)) key = __fdiv_rn(lf, c.T[rb + j]);
                 const uint32_t o = ordered_key(key);
-                const bool better = valid && o > bo[b];
-                bo[b] = better ? o : bo[b];
-                bv[b] = better ? (uint32_t)v : bv[b];
+                const bool better = valid && o > bo[j];
+                bo[j] = better ? o : bo[j];
+                bv[j] = better ? (uint32_t)v : bv[j];
             }
         }
         if (kRegs && gum_m != 0u) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 if (!kCacheF32) {
+                    k3[j] = k2[j];
+                    k2[j] = k1[j];
                     k1[j] = k0[j];
                     k0[j] = lp[j];
                 }
+                u3[j] = u2[j];
+                u2[j] = u1[j];
                 u1[j] = u0[j];
                 u0[j] = half2_up(ku[2 * j], ku[2 * j + 1]);
             }
@@ -552,12 +642,12 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     }
     // rows with exact keys: the warp's best into the CTA's
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        if (((gum_m >> b) & 1u) || !((live_m >> b) & 1u)) continue;
+    for (int j = 0; j < kRowsT; ++j) {
+        if ((gum_m >> j) & 1u) continue;
         const uint64_t pk =
-            bo[b] != 0u ? (((uint64_t)bo[b] << 32) | ((uint64_t)(0x3FFFFu - bv[b]) << 14)) : 0ull;
+            bo[j] != 0u ? (((uint64_t)bo[j] << 32) | ((uint64_t)(0x3FFFFu - bv[j]) << 14)) : 0ull;
         const uint64_t m = tc::warp_max_u64(pk);
-        if (lane == 0 && m != 0ull) atomicMax(&c.cbest[par][b], (unsigned long long)m);
+        if (lane == 0 && m != 0ull) atomicMax(&c.cbest[par][rb + j], (unsigned long long)m);
     }
     if (!gum_any) return;
 
@@ -567,59 +657,55 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     // lower bound on the CTA's best key, and it already holds this warp's)
     // selects the ids whose upper bound reaches it; their lanes compute
     // their exact keys.  A group that finishes its tiles early does this
-    // while the others still work on theirs.
-    uint32_t lw = 0u;   // lane b < 8: ordered warp threshold of row b
+    // while the other still works on its last tile.
+    uint32_t lw = 0u;   // lane j < 4: ordered warp threshold of row rb + j
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        const uint32_t m =
-            __reduce_max_sync(0xffffffffu, ((gum_m >> b) & 1u) ? ordered_key(__uint_as_float(bo[b])) : 0u);
-        lw = lane == b ? m : lw;
+    for (int j = 0; j < kRowsT; ++j) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, ((gum_m >> j) & 1u) ? ordered_key(lbm[j]) : 0u);
+        lw = lane == j ? m : lw;
     }
-    if (ok && ntw > 0 && lane < kChainRows && lw != 0u) atomicMax(&c.lcta[par][lane], lw);
+    if (ok && ntw > 0 && lane < kRowsT && lw != 0u) atomicMax(&c.lcta[par][rb + lane], lw);
     __syncwarp();
-    float Lc[kChainRows];
+    float Lc[kRowsT];
 #pragma unroll
-    for (int b = 0; b < kChainRows; ++b) {
-        const uint32_t o = *(volatile uint32_t *)&c.lcta[par][b];
+    for (int j = 0; j < kRowsT; ++j) {
+        const uint32_t o = *(volatile uint32_t *)&c.lcta[par][rb + j];
         // no bound recorded (no valid id): nothing can survive
-        Lc[b] = o != 0u ? key_from_ordered(o) : __uint_as_float(0x7f800000u);
+        Lc[j] = o != 0u ? key_from_ordered(o) : __uint_as_float(0x7f800000u);
     }
     if (kRegs && ok) {
-        uint32_t cand = 0u;   // bit 8 r + b: queued tile r (newest first), row b survives
-        __half2 L[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            L[j] = __halves2half2(__float2half_rd(Lc[2 * j]), __float2half_rd(Lc[2 * j + 1]));
-        auto slot = [&](int r, const __half2 (&uu)[4]) {
-            const int k = first + hh + 2 * (ntw - 1 - r);
+        uint32_t cand = 0u;   // bit 4 r + j: queued tile r (newest first), row rb + j survives
+        const __half2 L01 = __halves2half2(__float2half_rd(Lc[0]), __float2half_rd(Lc[1]));
+        const __half2 L23 = __halves2half2(__float2half_rd(Lc[2]), __float2half_rd(Lc[3]));
+        auto slot = [&](int r, const __half2 (&uu)[2]) {
+            const int k = wg + 2 * (ntw - 1 - r);
             const int v = (t0 + k) * 128 + q * 32 + lane;
             if (r < ntw && v < V) {
-                uint32_t b8 = 0u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t mj = __hgeu2_mask(uu[j], L[j]);
-                    b8 |= ((mj & 1u) | ((mj >> 15) & 2u)) << (2 * j);
-                }
-                cand |= (b8 & gum_m) << (8 * r);
+                const uint32_t m01 = __hgeu2_mask(uu[0], L01), m23 = __hgeu2_mask(uu[1], L23);
+                const uint32_t b4 = (m01 & 1u) | ((m01 >> 15) & 2u) | ((m23 & 1u) << 2) | ((m23 >> 13) & 8u);
+                cand |= (b4 & gum_m) << (4 * r);
             }
         };
         slot(0, u0);
         slot(1, u1);
+        slot(2, u2);
+        slot(3, u3);
         while (cand != 0u) {
             const int bit = __ffs(cand) - 1;
             cand &= cand - 1u;
-            const int r = bit >> 3, b = bit & 7;
-            const int k = first + hh + 2 * (ntw - 1 - r);
+            const int r = bit >> 2, j = bit & 3;
+            const int k = wg + 2 * (ntw - 1 - r);
             const uint32_t v = (uint32_t)((t0 + k) * 128 + q * 32 + lane);
             float lf;
             if (kCacheF32) {
                 // an fp32 cache's logit, read back (this thread wrote it)
-                lf = cache_fi[b * a.cache_s0 + v];
+                lf = cache_fi[j * a.cache_s0 + v];
             } else {
-                const uint32_t pr = r == 0 ? k0[b >> 1] : k1[b >> 1];
-                lf = __uint_as_float(((pr >> (16 * (b & 1))) & 0xffffu) << 16);
+                const uint32_t pr = (j < 2) ? (r == 0 ? k0[0] : r == 1 ? k1[0] : r == 2 ? k2[0] : k3[0])
+                                            : (r == 0 ? k0[1] : r == 1 ? k1[1] : r == 2 ? k2[1] : k3[1]);
+                lf = __uint_as_float(((pr >> (16 * (j & 1))) & 0xffffu) << 16);
             }
-            survivor_key(c, i, v, b, lf);
+            survivor_key(c, i, v, rb + j, lf);
         }
     }
     if (!kRegs && ok) {
@@ -627,69 +713,20 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         // noise bytes are read back (L2) tile by tile, exact bounds
 #pragma unroll 1
         for (int r = 0; r < ntw; ++r) {
-            const int k = first + hh + 2 * r;
+            const int k = wg + 2 * r;
             const int v = (t0 + k) * 128 + q * 32 + lane;
             if (v >= V) continue;
-            const uint2 qq = __ldcg(gq + v);
+            const uint32_t qq = __ldcg(gq + 2 * v);
 #pragma unroll
-            for (int b = 0; b < kChainRows; ++b) {
-                if (!((gum_m >> b) & 1u)) continue;
-                const float lf = kCacheF32 ? __ldcg(cache_fi + b * a.cache_s0 + v)
-                                           : __uint_as_float((uint32_t)__ldcg(cache_i + b * a.cache_s0 + v) << 16);
-                const uint32_t qb = ((b < 4 ? qq.x : qq.y) >> (8 * (b & 3))) & 0xffu;
-                if (!(key_upper(lf, c.invT[b], qb) < Lc[b])) survivor_key(c, i, (uint32_t)v, b, lf);
+            for (int j = 0; j < kRowsT; ++j) {
+                if (!((gum_m >> j) & 1u)) continue;
+                const float lf = kCacheF32 ? __ldcg(cache_fi + j * a.cache_s0 + v)
+                                           : __uint_as_float((uint32_t)__ldcg(cache_i + j * a.cache_s0 + v) << 16);
+                if (!(key_upper(lf, invT[j], (qq >> (8 * j)) & 0xffu) < Lc[j]))
+                    survivor_key(c, i, (uint32_t)v, rb + j, lf);
             }
         }
     }
-}
-
-// Poll the [G] tagged key slots of rows b0 and b1 (slot arrays s0, s1;
-// a row whose `use` bit is clear is skipped) until every CTA's key carries
-// `tag`; the warp's maximum packed key of each row.  Both rows' loads are in
-// flight together.  False after the deadline or when another CTA has
-// recorded an error.
-__device__ __forceinline__ bool poll_rows(const uint64_t *s0, const uint64_t *s1, uint32_t use, int G,
-                                          uint32_t tag, uint64_t deadline, const SampleArgs &a,
-                                          uint64_t &out0, uint64_t &out1) {
-    const int lane = threadIdx.x & 31;
-    for (uint32_t spin = 0;; ++spin) {
-        bool fresh = true;
-        uint64_t m0 = 0ull, m1 = 0ull;
-        for (int cc = lane; cc < G; cc += 32) {
-            if (use & 1u) {
-                const uint64_t k = tc::ld_relaxed_u64(s0 + cc);
-                fresh = fresh && (uint32_t)(k & kKeyTagMask) == tag;
-                m0 = k > m0 ? k : m0;
-            }
-            if (use & 2u) {
-                const uint64_t k = tc::ld_relaxed_u64(s1 + cc);
-                fresh = fresh && (uint32_t)(k & kKeyTagMask) == tag;
-                m1 = k > m1 ? k : m1;
-            }
-        }
-        if (__all_sync(0xffffffffu, fresh)) {
-            out0 = tc::warp_max_u64(m0) & ~(uint64_t)kKeyTagMask;
-            out1 = tc::warp_max_u64(m1) & ~(uint64_t)kKeyTagMask;
-            return true;
-        }
-        if ((spin & 15u) == 15u) {
-            const bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
-            if (__any_sync(0xffffffffu, bad)) return false;
-        }
-    }
-}
-
-// The exact integer weight floor(exp(fp32(l / T) - M) 2^40) of one cached
-// logit (inverse CDF; a logit of -inf or one far below M weighs 0).
-__device__ __forceinline__ uint64_t cdf_weight(float l, float T, float M) {
-    const float x = __fdiv_rn(l, T);
-    return (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
-}
-
-template <int DT>
-__device__ __forceinline__ float cached_logit(const SampleArgs &a, int64_t row_ofs, int v) {
-    return (DT & 2) ? __ldcg(a.cache_f + row_ofs + v)
-                    : dm_bf16_f32((uint32_t)__ldcg(a.cache + row_ofs + v));
 }
 
 }  // namespace
@@ -712,13 +749,11 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     const int G = gridDim.x, cta = blockIdx.x;
     const int R = a.rows, N = a.N, V = a.V;
     const int T_total = (V + 127) / 128;
-    int t0, t1;
-    cta_tiles(cta, G, T_total, t0, t1);
+    const int t0 = (int)((int64_t)cta * T_total / G);
+    const int t1 = (int)((int64_t)(cta + 1) * T_total / G);
     const int nt = t1 - t0;
     const int nch = nt * cpt;
     const int ntm = nch < kTmemChunks ? nch : kTmemChunks;
-    // issuer 0 takes the tiles whose first chunk is in TMEM
-    const int n0 = nt < (kTmemChunks + cpt - 1) / cpt ? nt : (kTmemChunks + cpt - 1) / cpt;
     const int v_begin = t0 * 128;
     const int v_end = t1 * 128 < V ? t1 * 128 : V;
     const int Gp = (G + kKeyPad - 1) / kKeyPad * kKeyPad;
@@ -730,10 +765,12 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             tc::mbar_init(tc::smem_u32(&c.cpdone[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(tc::smem_u32(&c.accf[b]), 1);
-            tc::mbar_init(tc::smem_u32(&c.accr[b]), 8);   // 2 halves x 4 lane quarters
+            tc::mbar_init(tc::smem_u32(&c.dfull[b]), 1);
+            tc::mbar_init(tc::smem_u32(&c.dfree[b]), kEpiWarps / 2);
             tc::mbar_init(tc::smem_u32(&c.fin[b]), 1);
         }
+        tc::mbar_init(tc::smem_u32(&c.bstaged), 1);
+        tc::mbar_init(tc::smem_u32(&c.sdone), kEpiWarps / 2);
         tc::mbar_init_fence();
         c.tmem_ready = 0u;
         clear_position(c, 0);
@@ -743,14 +780,25 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     }
     if (tid < kChainRows) {
         const int b = tid;
-        const bool live = b < R && a.row_state_idx[b] >= 0;
+        // the row's four arguments in one round trip (not each behind the
+        // row_state_idx test)
+        int64_t idx = -1, seed = 0;
+        float T = 0.0f;
+        int32_t anc = 0;
+        if (b < R) {
+            idx = a.row_state_idx[b];
+            T = a.temperature[b];
+            seed = a.seeds[b];
+            anc = a.anchor[b];
+        }
+        const bool live = idx >= 0;
+        if (!live) T = 0.0f;
         c.live[b] = live;
-        const float T = live ? a.temperature[b] : 0.0f;
         c.T[b] = T;
         c.sampling[b] = live && samples(T);
-        c.seed[b] = live ? (uint64_t)a.seeds[b] : 0ull;
+        c.seed[b] = live ? (uint64_t)seed : 0ull;
         c.invT[b] = samples(T) ? 1.0f / T : 1.0f;
-        int64_t p = live ? (int64_t)a.anchor[b] : 0;
+        int64_t p = live ? (int64_t)anc : 0;
         if (p < 0 || p >= V) {
             set_status(a.status, 1u /* MARKOV_EINVAL */, 0x100u + b);
             p = 0;
@@ -765,9 +813,14 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         const int b = tid % kChainRows, i2 = tid / kChainRows;
         c.hri[i2][b] = dm_row_step_hash(c.seed[b], (uint32_t)(a.row_base + b), (uint32_t)i2);
     }
-    if (warp < kChainRows && c.live[warp] && lane < RANK / 8)
-        stage_row<RANK>(b_s, *reinterpret_cast<const uint4 *>(a.embed + c.prev[warp] * RANK + 8 * lane),
-                        warp, lane);
+    if (cta == 0 && tid < kMaxSteps * kChainRows) {
+        // the next call's exchange words (the other call parity; the previous
+        // call, which used them, has completed): back to zero
+        const size_t np = (size_t)((c.call + 1u) & 1u);
+        a.win_max[(np * kMaxSteps * kChainRows + tid) * kLineU64] = 0ull;
+        if (tid < kMaxSteps) a.win_cnt[(np * kMaxSteps + tid) * kLineU32] = 0u;
+    }
+    if (warp < kChainRows && c.live[warp]) stage_embed<RANK>(b_s, a.embed, c.prev[warp], warp, lane);
     tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -781,17 +834,22 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     const bool gum_any = gum_mask != 0u;
 
     // per-role persistent state
-    uint32_t uses = 0;          // issuer: tile pairs issued into its accumulator
-    uint32_t dcount = 0;        // epilogue: tile pairs consumed from its accumulator
+    uint32_t uses = 0;          // issuer: tiles issued into its accumulator
+    uint32_t dcount = 0;        // epilogue: tiles consumed from its accumulator
     uint32_t issued[kSmemChunks];   // producer: loads issued per slot
 #pragma unroll
     for (int s = 0; s < kSmemChunks; ++s) issued[s] = 0u;
 
     bool stop = __syncthreads_or(c.abort != 0u);
     for (int i = 0; i < N && !stop; ++i) {
+        // A CTA with the full 7 tiles of rank 256 takes its last tile's bias
+        // through mma.sync in the epilogue warps after position 0: the
+        // tcgen05 tiles then pair up in 3 rounds of the two accumulators
+        // instead of 4.  (Its A chunks are in shared memory.)
+        const int nts = (MODE == 0 && RANK == 256 && nt == kMaxChunks / cpt && i > 0) ? nt - 1 : -1;
         // ------------------------------------- phase A: MMA and epilogue
         if (warp < 2) {
-            issue_tiles<RANK>(c, a, tmem, warp, i, n0, nt, ntm, b_sa, head_sa, timeout, uses);
+            issue_tiles<RANK>(c, a, tmem, warp, i, nts >= 0 ? nts : nt, ntm, b_sa, head_sa, timeout, uses);
         } else if (warp < 4 && i > 0) {
             // warps 2 and 3 after the head load: the next position's base
             // logits into L2, off the chain's critical path
@@ -799,7 +857,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         } else if (warp == 2) {
             if (lane == 0 && i == 0) {
                 for (int j = 0; j < nch; ++j) {
-                    if (aborted(c)) break;
+                    if (aborted(c, a)) break;
                     int s;
                     uint32_t ph;
                     chunk_slot(j, ntm, s, ph);
@@ -825,7 +883,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 // chunks share a slot: a parity wait sees one phase at a time)
                 bool early = false;
                 for (int j = 0; j <= ntm; ++j) {
-                    if (aborted(c)) break;
+                    if (aborted(c, a)) break;
                     int sp = 0;
                     uint32_t pp = 0u;
                     if (j > 0) chunk_slot(j - 1, ntm, sp, pp);
@@ -878,49 +936,78 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 }
                 if (N > 1) prefetch_base<kEpiThreads>(c, a, 1, v_begin, v_end, te);
             }
-            epilogue<RANK, MODE == 1, DT>(c, a, tmem, i, t0, n0, nt, gum_any, timeout, dcount);
+            if (MODE == 1)
+                epilogue<RANK, true, DT>(c, a, tmem, i, t0, nt, -1, ntm, b_sa, head_sa, false, timeout, dcount);
+            else
+                epilogue<RANK, false, DT>(c, a, tmem, i, t0, nt, nts, ntm, b_sa, head_sa, gum_any, timeout, dcount);
         }
         stop = __syncthreads_or(stop_vote(c, a, MODE != 0));
         if (stop) break;
 
         // ------------------------------- phase B: agree on every row's winner
         const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
-        const uint32_t tag = epoch & kKeyTagMask;
-        uint64_t *slots_i = a.tc_keys + (size_t)i * kChainRows * Gp;   // [row][Gp]
-        if (warp < 4) {
-            // warp 0 lane b stores row b's best key, tagged; lanes of warp 1
-            // warm L2 with this CTA's candidates' embedding rows (the winning
-            // CTA's prefetch serves every CTA's gather); warps 0-3 poll rows
-            // w and w + 4
-            if (warp == 0 && lane < kChainRows && c.live[lane])
-                tc::st_relaxed_u64(slots_i + (size_t)lane * Gp + cta,
-                                   ((uint64_t)c.cbest[i & 1][lane] & ~(uint64_t)kKeyTagMask) | tag);
-            if (warp == 1 && lane < kChainRows && c.live[lane] && i + 1 < N) {
-                const uint64_t m = c.cbest[i & 1][lane];
-                const uint32_t id = unpack_id(m);
-                if (m != 0ull && id < (uint32_t)V) {
-                    const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)id * RANK);
-#pragma unroll
-                    for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
-                }
-            }
-            const uint32_t use = (c.live[warp] ? 1u : 0u) | (c.live[warp + 4] ? 2u : 0u);
-            if (use != 0u) {
-                uint64_t w0 = 0ull, w1 = 0ull;
-                if (!poll_rows(slots_i + (size_t)warp * Gp, slots_i + (size_t)(warp + 4) * Gp, use, G, tag,
-                               tc::now_ns() + timeout, a, w0, w1)) {
-                    if (lane == 0) fail(c, a, 4u, 0x7000u + i);
-                    w0 = w1 = 0ull;
-                }
-                if (lane == 0) {
-                    c.win[warp] = w0;
-                    c.win[warp + 4] = w1;
-                }
-            }
-        }
+        const uint32_t tag = epoch & 0x3FFFu;
         if (MODE == 0) {
+            // Gumbel and greedy rows: warp 0 reports this CTA's best key per
+            // row and collects the winners; warps 0-3 stage the winners'
+            // embeddings (rows w and w + 4) as the next B operand.  Every CTA
+            // folds its keys into one word per (position, row) with red.max
+            // and then adds 1 to the position's counter (release); lane 0
+            // waits until all G CTAs have counted (acquire) and reads the 8
+            // words: one polled word per CTA keeps the L2 traffic low.  The
+            // words of one call parity are zeroed by the previous call.
+            if (warp == 0 || warp == 2) {
+                if (warp == 0) {
+                    // lane b < 8: row b's best key in this CTA
+                    const size_t par = (size_t)(c.call & 1u);
+                    uint64_t *wm = a.win_max + ((par * kMaxSteps + i) * kChainRows) * kLineU64;
+                    uint32_t *wc = a.win_cnt + (par * kMaxSteps + i) * kLineU32;
+                    // lane b < 8 folds row b's best key in (one instruction for
+                    // all rows); the warp barrier orders the reds before lane
+                    // 0's release
+                    if (lane < kChainRows && c.live[lane])
+                        tc::red_max_u64(wm + lane * kLineU64, (uint64_t)c.cbest[i & 1][lane]);
+                    __syncwarp();
+                    if (lane == 0) {
+                        bool ok = true;
+                        tc::red_release_add_u32(wc, 1u);
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        for (uint32_t spin = 0;; ++spin) {
+                            if ((int32_t)(ld_acquire_u32(wc) - (uint32_t)G) >= 0) break;
+                            if ((spin & 15u) == 15u &&
+                                (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (ok) {
+                            // all 8 loads in flight before any result is used
+                            uint64_t w8[kChainRows];
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b)
+                                w8[b] = c.live[b] ? tc::ld_relaxed_u64(wm + b * kLineU64) : 0ull;
+#pragma unroll
+                            for (int b = 0; b < kChainRows; ++b) c.win[b] = w8[b];
+                        } else {
+                            fail(c, a, 4u, 0x7000u + i);
+                        }
+                    }
+                    __syncwarp();
+                } else if (lane < kChainRows && c.live[lane]) {
+                    // warp 2: this CTA's candidate of row b = lane into L2
+                    // while the winners are agreed (the winning CTA's
+                    // prefetch serves every CTA's staging gather)
+                    const uint64_t m = c.cbest[i & 1][lane];
+                    const uint32_t id = unpack_id(m);
+                    if (m != 0ull && id < (uint32_t)V && i + 1 < N) {
+                        const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)id * RANK);
+#pragma unroll
+                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
+                    }
+                }
+            }
             if (warp < 4) {
-                __syncwarp();
+                asm volatile("bar.sync 3, 128;" ::: "memory");
                 // warps 0-3 stage rows w and w + 4: both gathers in flight at once
                 const int rb2[2] = {warp, warp + 4};
                 uint32_t idr[2];
@@ -929,10 +1016,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 for (int h = 0; h < 2; ++h) {
                     const int b = rb2[h];
                     uint32_t id = unpack_id(c.win[b]);
-                    if (c.live[b] && (c.win[b] == 0ull || id >= (uint32_t)V)) {
-                        // no CTA reported a key for a live row (or the poll
-                        // gave up): never index embed with it
-                        if (lane == 0 && !aborted(c)) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB000u + i);
+                    if (c.live[b] && id >= (uint32_t)V) {
+                        // no CTA reported a key for a live row: an internal
+                        // error; never index embed with it
+                        if (lane == 0) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB000u + i);
                         id = 0u;
                     }
                     idr[h] = c.live[b] ? id : 0u;
@@ -948,14 +1035,21 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         c.prev[b] = (int64_t)idr[h];
                         if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)idr[h];
                     }
-                    if (i + 1 < N && lane < RANK / 8) stage_row<RANK>(b_s, ev[h], b, lane);
+                    if (i + 1 < N && lane < RANK / 8) {
+                        const int chunk = lane >> 3, piece = lane & 7;
+                        *reinterpret_cast<uint4 *>(b_s + chunk * kBChunkBytes + b * 128 + ((piece ^ b) << 4)) = ev[h];
+                    }
                 }
+            }
+            if (warp < 4) {
                 // the control warps alone close the position: the next MMAs
                 // need only the staged B operand
                 tc::fence_proxy_async_smem();
                 tc::fence_before_sync();
                 asm volatile("bar.sync 4, 128;" ::: "memory");
                 tc::fence_after_sync();
+                // the epilogue warps' mma.sync tile reads the staged rows too
+                if (tid == 0 && i + 1 < N) tc::mbar_arrive(tc::smem_u32(&c.bstaged));
             } else if (i + 1 < N) {
                 // the epilogue warps clear the next position's CTA maxima (their
                 // last reader finished before this position's phase-A barrier),
@@ -967,176 +1061,186 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 if (gum_any) noise_bounds<kEpiThreads>(c, a, i + 1, gum_mask, v_begin, v_end, tid - 128);
                 asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
             }
-            // an error seen by the control warps stops the CTA at the next
-            // position's phase-A barrier
         } else {
+            if (warp < kChainRows) {
+                const int b = warp;
+                const uint64_t m = c.cbest[i & 1][b];
+                uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * kTcReplicas * Gp;
+                if (lane < kTcReplicas) tc::st_relaxed_u64(slots + lane * Gp + cta, (m & ~0x3FFFull) | tag);
+                slots += (cta % kTcReplicas) * Gp;
+                if (c.live[b]) {
+                    if (lane == 0 && m != 0ull) {
+                        const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;
+                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(reinterpret_cast<const uint8_t *>(er) + o);
+                    }
+                    uint64_t w = 0ull;
+                    if (!poll_max(slots, G, tag, tc::now_ns() + timeout, a, w)) {
+                        if (lane == 0) fail(c, a, 4u, 0x7000u + i);
+                    } else if (lane == 0) {
+                        c.win[b] = w;
+                    }
+                }
+            }
             stop = __syncthreads_or(stop_vote(c, a));
             if (stop) break;
 
             // inverse CDF: rows whose maximum M is finite need the exact integer
-            // weight sums floor(exp(x - M) 2^40); every CTA learns every CTA's
-            // sum, finds the CTA whose prefix range holds mulhi64(H, S) and
-            // scans that CTA's cached logits for the token
-            uint32_t cdf_m = 0u;
-#pragma unroll
-            for (int b = 0; b < kChainRows; ++b) {
-                if (b >= R || !c.sampling[b]) continue;
-                const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                if (o != 0xffffffffu && !isinf(key_from_ordered(o))) cdf_m |= 1u << b;
+            // weight sums floor(exp(x - M) 2^40), then the CTA whose prefix range
+            // holds mulhi64(H, S) scans its ids for the token
+            bool cdf_any = false;
+            if (MODE == 1) {
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.sampling[b]) continue;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) cdf_any = true;
+                }
             }
-            if (cdf_m != 0u) {
-                const uint32_t stag = epoch & 0xFFFu;
+            if (cdf_any) {
+                const uint32_t tag32 = epoch;
                 if (tid < kChainRows) c.sum[tid] = 0ull;
                 __syncthreads();
-                // 4 rows a time: every cached logit of the group is loaded
+                // kGR rows a time: every cached logit of the group is loaded
                 // before any weight, so the rows share one read latency
-                constexpr int kMaxIds = kMaxChunks / cpt * 128;
+                constexpr int kMaxIds = (kTmemChunks + kSmemChunks) / (RANK / 64) * 128;
                 constexpr int kPT = (kMaxIds + kThreads - 1) / kThreads;   // ids per thread
                 constexpr int kGR = RANK == 64 ? 2 : 4;
-                for (int b0 = 0; b0 < kChainRows; b0 += kGR) {
-                    if (!((cdf_m >> b0) & ((1u << kGR) - 1u))) continue;
+                for (int b0 = 0; b0 < R && b0 < kChainRows; b0 += kGR) {
                     float xs[kGR][kPT];
+                    bool use[kGR];
 #pragma unroll
-                    for (int rr = 0; rr < kGR; ++rr) {
-                        const int b = b0 + rr;
+                    for (int r = 0; r < kGR; ++r) {
+                        const int b = b0 + r;
+                        const uint32_t o = b < R && b < kChainRows ? (uint32_t)(c.win[b] >> 32) : 0u;
+                        use[r] = b < R && b < kChainRows && c.sampling[b] && o != 0xffffffffu &&
+                                 !isinf(key_from_ordered(o));
                         const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
 #pragma unroll
-                        for (int kk = 0; kk < kPT; ++kk) {
-                            const int v = v_begin + tid + kk * kThreads;
-                            xs[rr][kk] = ((cdf_m >> b) & 1u) && v < v_end ? cached_logit<DT>(a, crow, v) : 0.0f;
+                        for (int k = 0; k < kPT; ++k) {
+                            const int v = v_begin + tid + k * kThreads;
+                            xs[r][k] = 0.0f;
+                            if (use[r] && v < v_end)
+                                xs[r][k] = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
                         }
                     }
 #pragma unroll
-                    for (int rr = 0; rr < kGR; ++rr) {
-                        const int b = b0 + rr;
-                        if (!((cdf_m >> b) & 1u)) continue;
+                    for (int r = 0; r < kGR; ++r) {
+                        if (!use[r]) continue;
+                        const int b = b0 + r;
                         const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
                         uint64_t part = 0ull;
 #pragma unroll
-                        for (int kk = 0; kk < kPT; ++kk) {
-                            if (v_begin + tid + kk * kThreads >= v_end) break;
-                            part += cdf_weight(xs[rr][kk], c.T[b], M);
+                        for (int k = 0; k < kPT; ++k) {
+                            if (v_begin + tid + k * kThreads >= v_end) break;
+                            const float x = __fdiv_rn(xs[r][k], c.T[b]);
+                            part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
                         }
-#pragma unroll
+    #pragma unroll
                         for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
                         if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
                     }
                 }
                 __syncthreads();
-                // publish (release: this CTA's cache writes are visible to a
-                // CTA that reads the tagged sum)
-                if (tid < kChainRows && ((cdf_m >> tid) & 1u)) {
-                    uint64_t *sl = a.tc_sums + ((size_t)i * kChainRows + tid) * Gp + cta;
-                    const uint64_t w = c.sum[tid] | ((uint64_t)stag << kSumTagShift);
+                // each row's sum tagged in its top 12 bits (a CTA's sum is
+                // below 4096 ids x 2^40), stored with release: this CTA's
+                // cache writes are visible to a CTA that reads the tagged sum
+                const uint32_t stag = tag32 & 0xFFFu;
+                if (tid < kChainRows && c.sampling[tid]) {
+                    uint64_t *sl = a.tc_sums + ((int64_t)i * kChainRows + tid) * Gp + cta;
+                    const uint64_t w = c.sum[tid] | ((uint64_t)stag << 52);
                     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(sl), "l"(w) : "memory");
                 }
-                // warp b: every CTA's sum of row b, the total S, the target
-                // t = mulhi64(H, S) and the CTA whose prefix range holds it
-                if (warp < kChainRows && ((cdf_m >> warp) & 1u)) {
+                // every CTA learns every row's total and its own prefix
+                __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
+                if (warp < kChainRows && c.sampling[warp]) {
                     const int b = warp;
-                    const uint64_t *sl = a.tc_sums + ((size_t)i * kChainRows + b) * Gp;
-                    constexpr int kPer = 5;   // CTAs per lane (G <= 160)
-                    const int c0 = lane * kPer;
-                    uint64_t s5[kPer];
-                    const uint64_t dl = tc::now_ns() + timeout;
-                    bool okp = true;
-                    for (uint32_t spin = 0;; ++spin) {
-                        bool fresh = true;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) {
+                        const uint64_t *sl = a.tc_sums + ((int64_t)i * kChainRows + b) * Gp;
+                        constexpr int kPer = kMaxGrid / 32;
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        bool ok = true;
+                        uint64_t s5[kPer];
+                        for (uint32_t spin = 0;; ++spin) {
+                            // all loads of a round in flight together
+                            uint64_t w5[kPer];
 #pragma unroll
-                        for (int u = 0; u < kPer; ++u) {
-                            s5[u] = 0ull;
-                            if (c0 + u < G) {
-                                const uint64_t w = tc::ld_relaxed_u64(sl + c0 + u);
-                                fresh = fresh && (uint32_t)(w >> kSumTagShift) == stag;
-                                s5[u] = w & ((1ull << kSumTagShift) - 1ull);
-                            }
-                        }
-                        if (__all_sync(0xffffffffu, fresh)) break;
-                        if ((spin & 15u) == 15u &&
-                            __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
-                            okp = false;
-                            break;
-                        }
-                    }
-                    if (!okp) {
-                        if (lane == 0) fail(c, a, 4u, 0x8000u + i);
-                    } else {
-                        // acquire: the cache writes of the CTAs whose sums were read
-                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                        uint64_t mine = 0ull;
-#pragma unroll
-                        for (int u = 0; u < kPer; ++u) mine += s5[u];
-                        uint64_t incl = mine;
-#pragma unroll
-                        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                            if (lane >= o2) incl += y;
-                        }
-                        const uint64_t S = __shfl_sync(0xffffffffu, incl, 31);
-                        const uint64_t t = __umul64hi(dm_cdf_hash(c.hri[i][b]), S);
-                        uint64_t run = incl - mine;
-                        if (run <= t && t < run + mine) {
+                            for (int u = 0; u < kPer; ++u)
+                                w5[u] = lane + 32 * u < G ? tc::ld_relaxed_u64(sl + lane + 32 * u)
+                                                          : ((uint64_t)stag << 52);
+                            bool fresh = true;
 #pragma unroll
                             for (int u = 0; u < kPer; ++u) {
-                                if (c0 + u < G && run <= t && t < run + s5[u]) {
-                                    c.cstar[b] = c0 + u;
-                                    c.rem[b] = t - run;
-                                }
-                                run += s5[u];
+                                fresh = fresh && (uint32_t)(w5[u] >> 52) == stag;
+                                s5[u] = w5[u] & ((1ull << 52) - 1ull);
                             }
+                            if (__all_sync(0xffffffffu, fresh)) break;
+                            if ((spin & 15u) == 15u &&
+                                __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) {
+                            if (lane == 0) fail(c, a, 4u, 0x8000u + i);
+                        } else {
+                            // acquire: the cache writes of the CTAs whose sums were read
+                            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                            uint64_t tot = 0ull, pre = 0ull;
+#pragma unroll
+                            for (int u = 0; u < kPer; ++u) {
+                                tot += s5[u];
+                                if (lane + 32 * u < cta) pre += s5[u];
+                            }
+    #pragma unroll
+                            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                                tot += __shfl_xor_sync(0xffffffffu, tot, o2);
+                                pre += __shfl_xor_sync(0xffffffffu, pre, o2);
+                            }
+                            if (lane == 0) { s_tot[b] = tot; s_pre[b] = pre; }
                         }
                     }
                 }
                 stop = __syncthreads_or(stop_vote(c, a));
                 if (stop) break;
-                // every CTA scans the target CTA's ids of each row itself: the
-                // threads split into 4 groups of 5 warps, one row per group
-                constexpr int kGroupWarps = (kThreads / 32) / 4;
-                constexpr int kGroupThreads = kGroupWarps * 32;
-                constexpr int kScanPer = (kMaxIds + kGroupThreads - 1) / kGroupThreads;
-                const int grp = warp / kGroupWarps, gt = tid - grp * kGroupThreads;
-                for (int b0 = 0; b0 < kChainRows; b0 += 4) {
-                    if (!((cdf_m >> b0) & 0xFu)) continue;
-                    const int b = b0 + grp;
-                    const bool mine_row = (cdf_m >> b) & 1u;
-                    int u0 = 0, per = 0;
-                    float xs[kScanPer];
-                    uint64_t wsum = 0ull;
-                    if (mine_row) {
-                        int s0, s1;
-                        cta_tiles(c.cstar[b], G, T_total, s0, s1);
-                        u0 = s0 * 128;
-                        const int u1 = s1 * 128 < V ? s1 * 128 : V;
-                        per = (u1 - u0 + kGroupThreads - 1) / kGroupThreads;
+                for (int b = 0; b < R && b < kChainRows; ++b) {
+                    if (!c.sampling[b]) continue;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o == 0xffffffffu || isinf(M)) continue;
+                    const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
+                    const uint64_t H = dm_cdf_hash(c.hri[i][b]);
+                    const uint64_t target = __umul64hi(H, S);
+                    if (P <= target && target < P + Sc) {
                         const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                        const int my0 = u0 + gt * per;
-#pragma unroll
-                        for (int kk = 0; kk < kScanPer; ++kk)
-                            xs[kk] = (kk < per && my0 + kk < u1) ? cached_logit<DT>(a, crow, my0 + kk)
-                                                                 : __uint_as_float(0xff800000u);
-                        const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
-#pragma unroll
-                        for (int kk = 0; kk < kScanPer; ++kk)
-                            if (kk < per) wsum += cdf_weight(xs[kk], c.T[b], M);
-                    }
-                    uint64_t incl = wsum;
-#pragma unroll
-                    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                        if (lane >= o2) incl += y;
-                    }
-                    if (lane == 31) c.wtot[warp] = incl;
-                    __syncthreads();
-                    if (mine_row) {
-                        uint64_t run = incl - wsum;
-                        for (int w2 = grp * kGroupWarps; w2 < warp; ++w2) run += c.wtot[w2];
-                        const uint64_t t = c.rem[b];
-                        if (run <= t && t < run + wsum) {
-                            const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
-                            for (int kk = 0; kk < kScanPer && kk < per; ++kk) {
-                                run += cdf_weight(xs[kk], c.T[b], M);
-                                if (run > t) {
-                                    c.tok[b] = (uint32_t)(u0 + gt * per + kk);
+                        const int len = v_end - v_begin;
+                        const int chunk = (len + kThreads - 1) / kThreads;
+                        const int c0 = v_begin + tid * chunk;
+                        const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
+                        uint64_t mine = 0ull;
+                        for (int v = c0; v < c1; ++v) {
+                            const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
+                            mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                        }
+                        uint64_t incl = mine;
+    #pragma unroll
+                        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+                            if (lane >= o2) incl += y;
+                        }
+                        if (lane == 31) c.scan[warp] = incl;
+                        __syncthreads();
+                        uint64_t wpre = 0ull;
+                        for (int w = 0; w < warp; ++w) wpre += c.scan[w];
+                        uint64_t run = P + wpre + incl - mine;
+                        if (run <= target && target < run + mine) {
+                            for (int v = c0; v < c1; ++v) {
+                                const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
+                                run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                                if (run > target) {
+                                    tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
+                                                       ((uint64_t)v << 32) | tag32);
                                     break;
                                 }
                             }
@@ -1144,30 +1248,52 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                     __syncthreads();
                 }
-                if (tid < kChainRows && ((cdf_m >> tid) & 1u))
-                    c.win[tid] = (c.win[tid] & 0xffffffff00000000ull) | ((uint64_t)(0x3FFFFu - c.tok[tid]) << 14);
-                __syncthreads();
+                // everyone learns the tokens the owners found
+                if (warp < kChainRows && c.sampling[warp] && lane == 0) {
+                    const int b = warp;
+                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                    const float M = key_from_ordered(o);
+                    if (o != 0xffffffffu && !isinf(M)) {
+                        const uint64_t *slot = a.tok_slots + (int64_t)i * kChainRows + b;
+                        const uint64_t dl = tc::now_ns() + timeout;
+                        uint64_t t = 0ull;
+                        for (;;) {
+                            t = tc::ld_relaxed_u64(slot);
+                            if ((uint32_t)t == tag32) break;
+                            if (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u) {
+                                fail(c, a, 4u, 0x9000u + i);
+                                break;
+                            }
+                        }
+                        const uint32_t v = (uint32_t)(t >> 32);
+                        if ((uint32_t)t == tag32 && v < (uint32_t)V)
+                            c.win[b] = (c.win[b] & 0xffffffff00000000ull) |
+                                       ((uint64_t)(0x3FFFFu - v) << 14);
+                        else if ((uint32_t)t == tag32)
+                            fail(c, a, 6u, 0xA000u + i);
+                    }
+                }
+                stop = __syncthreads_or(stop_vote(c, a));
+                if (stop) break;
             }
 
             // ------------------------- the token, and the next position's B operand
             if (warp < kChainRows && c.live[warp]) {
                 const int b = warp;
                 uint32_t id = unpack_id(c.win[b]);
-                if (c.sampling[b]) {
+                if (MODE == 1 && c.sampling[b]) {
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     if (o != 0xffffffffu && key_from_ordered(o) == __uint_as_float(0xff800000u)) id = 0u;
                 }
-                if (c.win[b] == 0ull || id >= (uint32_t)V) {
-                    if (lane == 0 && !aborted(c)) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB100u + i);
+                if (id >= (uint32_t)V) {
+                    if (lane == 0) fail(c, a, 6u /* MARKOV_EDEVICE */, 0xB100u + i);
                     id = 0u;
                 }
                 if (lane == 0) {
                     c.prev[b] = (int64_t)id;
                     if (cta == 0) a.tokens[b * a.tok_s0 + i] = (int64_t)id;
                 }
-                if (i + 1 < N && lane < RANK / 8)
-                    stage_row<RANK>(b_s, *reinterpret_cast<const uint4 *>(a.embed + (int64_t)id * RANK + 8 * lane),
-                                    b, lane);
+                if (i + 1 < N) stage_embed<RANK>(b_s, a.embed, (int64_t)id, b, lane);
             }
             // the next position's CTA maxima (last read before this
             // position's phase-A barrier)
@@ -1197,7 +1323,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     __syncthreads();
     tc::fence_after_sync();
     if (warp == 0) tc::tmem_dealloc(tmem, 512);
-    if (cta == 0 && tid == 0 && !aborted(c) && ld_acquire_u32(a.status) == 0u)
+    if (cta == 0 && tid == 0 && !aborted(c, a) && ld_acquire_u32(a.status) == 0u)
         *(volatile uint32_t *)a.call_counter = c.call + 1u;
 }
 
