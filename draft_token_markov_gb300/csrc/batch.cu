@@ -689,7 +689,8 @@ static void (*logits_kernel(int r, bool base_f32))(const SampleArgs, int) {
     }
 }
 
-cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches) {
+cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches, const CUtensorMap *tmap,
+                         int sms) {
     // the launch variant by row count: 16-row groups (whole-tile head
     // prefetch) up to 16 rows, 32-row groups above
     const int mt = a.rows <= 16 ? 1 : 2;
@@ -704,11 +705,21 @@ cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches
     void (*logits)(const SampleArgs, int) =
         mt == 1 ? logits_kernel<1>(a.r, a.base_f != nullptr) : logits_kernel<2>(a.r, a.base_f != nullptr);
     if (!logits) return cudaErrorInvalidValue;
+    // the tcgen05 logits kernel: row groups of 64, one CTA per SM shared out
+    // over the groups, each CTA a contiguous run of 128-id tiles
+    const int tgroups = (a.rows + 63) / 64;
+    const int tiles = (a.V + 127) / 128;
+    int tctas = sms > 0 ? sms / tgroups : 1;
+    if (tctas < 1) tctas = 1;
+    if (tctas > tiles) tctas = tiles;
     int n = 0;
     cudaError_t e = cudaSuccess;
     for (int i = 0; i < a.N && e == cudaSuccess; ++i) {
         // the first launch of a call waits for the stream as usual
-        e = launch_one(logits, dim3(nblk, groups), smem, stream, i > 0, a, i);
+        if (tmap)
+            e = launch_batch_tc_logits(a, *tmap, i, tctas, stream, i > 0);
+        else
+            e = launch_one(logits, dim3(nblk, groups), smem, stream, i > 0, a, i);
         ++n;
         if (e == cudaSuccess && a.mode == 1) {
             e = launch_one(batch_cdf_kernel, dim3(nb2, a.rows), 0, stream, true, a, i, nb2);

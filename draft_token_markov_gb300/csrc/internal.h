@@ -90,7 +90,15 @@ cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
 cudaError_t launch_device_math(int fn, const float *x, float *y, int64_t n, cudaStream_t s);
 cudaError_t chain_occupancy(int *blocks_per_sm);
 cudaError_t launch_chain(const SampleArgs &a, cudaStream_t stream);
-cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches);
+// tmap: the head's TMA descriptor; with it the per-position logits run on
+// the tcgen05 kernel (batch_tc.cu) over `sms` multiprocessors, without it on
+// the mma.sync kernel
+cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches,
+                         const CUtensorMap *tmap = nullptr, int sms = 0);
+cudaError_t batch_tc_prepare();
+size_t batch_tc_smem(int rank);
+cudaError_t launch_batch_tc_logits(const SampleArgs &a, const CUtensorMap &tmap, int i, int ctas,
+                                   cudaStream_t stream, bool pdl);
 int batch_blocks(int V);
 size_t chain_tc_smem();
 int chain_tc_max_chunks();

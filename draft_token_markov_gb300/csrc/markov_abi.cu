@@ -29,6 +29,7 @@ struct markov_plan {
     size_t keys_n = 0;
     // the tcgen05 chain: tagged exchange slots and the head's TMA descriptor
     bool tc_ok = false;
+    bool batch_tc_ok = false;     // the per-position logits on the tcgen05 kernel
     int tc_grid = 0;
     uint64_t *tc_keys = nullptr;
     uint64_t *tc_sums = nullptr;
@@ -197,6 +198,8 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaGetLastError();
     }
 
+    p->batch_tc_ok = batch_tc_prepare() == cudaSuccess;
+    cudaGetLastError();
     const int Gp = (p->chain_grid + kKeyPad - 1) / kKeyPad * kKeyPad;
     size_t chain_keys = (size_t)kMaxSteps * 2 * kChainRows * Gp;
     size_t batch_keys = (size_t)d.max_rows * p->batch_grid;
@@ -403,7 +406,8 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
     a.bcnt = p->bcnt;
     a.timeout_ns = (uint64_t)p->d.timeout_ms * 1000000ull;
 
-    if (use_tc && p->tmap_head != head) {
+    const bool batch_tc = !chain && p->batch_tc_ok;
+    if ((use_tc || batch_tc) && p->tmap_head != head) {
         if (!encode_head_map(&p->tmap, head, V, r)) return MARKOV_ECUDA;
         p->tmap_head = head;
     }
@@ -463,7 +467,7 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
             p->batch_dirty = false;
         }
         int n = 0;
-        cudaError_t e = launch_batch(a, s, &n);
+        cudaError_t e = launch_batch(a, s, &n, batch_tc ? &p->tmap : nullptr, p->sm_count);
         if (e != cudaSuccess) { cudaGetLastError(); p->batch_dirty = true; return MARKOV_ECUDA; }
         launches += n;
         p->last_path = MARKOV_PATH_BATCH;
