@@ -6,7 +6,9 @@
 // per-step kernels are launched with programmatic dependent launch).
 //
 // Per position i, in launch order on one stream:
-//   logits  grid (blocks, row groups of 16 rows up to 16 rows, else 32):
+//   logits  grid (blocks, row groups of 16 rows up to 16 rows, else 32),
+//           or the tcgen05 logits kernel (batch_tc.cu) when the plan has
+//           the head's tensor map:
 //           bias tiles [16 ids x group rows] by mma.m16n8k16 with the
 //           previous tokens' embeddings staged in shared memory, the
 //           epilogue (BF16 rounding, base add, transform,
@@ -16,10 +18,11 @@
 //           token of every row the winner decides: all rows in Gumbel mode,
 //           greedy rows and rows with a NaN, +inf or all -inf maximum in
 //           inverse-CDF mode;
-//   cdf     (inverse CDF only) grid (vocab blocks of 4096 ids, rows): the
-//           block's integer weight sum floor(exp(x - M) 2^40); the last
-//           block of a row scans the row's block sums for mulhi64(H, S),
-//           then the target block's weights, and writes the token.
+//   cdf     (inverse CDF only) grid (vocab blocks of kCdfIds ids, rows):
+//           the integer weights floor(exp(x - M) 2^40) summed per 256-id
+//           unit; the last block of a row scans the row's unit sums for
+//           mulhi64(H, S), then one warp the target unit's weights, and
+//           writes the token.
 // The next position's logits kernel reads token i from draft_tokens.  Every
 // block that takes the last-block step resets the counter and the winner
 // word it consumed, so each call leaves them zero for the next.
@@ -34,6 +37,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace dtm {
 
@@ -194,7 +198,7 @@ __device__ __noinline__ uint32_t transform_two_bf16(uint32_t lp, const Transform
 
 // Integer inverse-CDF weight floor(exp(x / T - M) 2^40) of cached logit x.
 __device__ __forceinline__ uint64_t cdf_weight_of(float x, float T, float M) {
-    return (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(__fdiv_rn(x, T), M)), 0x1p40f));
+    return dm_cdf_weight(__fsub_rn(__fdiv_rn(x, T), M));
 }
 
 // Eight consecutive cached logits (row b, position i, ids v .. v + 7, v a
@@ -505,12 +509,41 @@ batch_logits_kernel(const SampleArgs a, int i) {
     }
 }
 
-__global__ void __launch_bounds__(kBatchThreads)
-batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
+// Eight consecutive cached logits as fp32, read once more (the cache's last
+// read of the position: evict-first in L2).
+__device__ __forceinline__ void cache8_last(const SampleArgs &a, int b, int i, int v, uint64_t pol,
+                                            float (&x)[8]) {
+    const int64_t o = b * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
+    if (a.cache_f) {
+        const uint4 p = tc::ld_nc_v4_hint(a.cache_f + o, pol);
+        const uint4 q = tc::ld_nc_v4_hint(a.cache_f + o + 4, pol);
+        x[0] = __uint_as_float(p.x); x[1] = __uint_as_float(p.y);
+        x[2] = __uint_as_float(p.z); x[3] = __uint_as_float(p.w);
+        x[4] = __uint_as_float(q.x); x[5] = __uint_as_float(q.y);
+        x[6] = __uint_as_float(q.z); x[7] = __uint_as_float(q.w);
+    } else {
+        const uint4 p = tc::ld_nc_v4_hint(a.cache + o, pol);
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    }
+}
+
+// The inverse-CDF step of position i for the rows the logits kernel left
+// open: grid (blocks of kCdfIds ids, rows).  A block's warp takes 256
+// consecutive ids per round (8 per lane), so each (round, warp) is one
+// 256-id unit of the vocabulary; its weight sum goes to the row's unit
+// array (a.sums + b nu, in id order).  The last block of the row scans the
+// unit sums for the target mulhi64(H, S), then one warp re-reads the target
+// unit's 256 ids and scans their weights for the token.
+__global__ void __launch_bounds__(kBatchThreads, 4)
+batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
     __shared__ unsigned long long s_w[kBW];
-    __shared__ unsigned long long s_blkpre, s_target;
-    __shared__ long long s_tok;
-    __shared__ int s_blk, s_flag;
+    __shared__ unsigned long long s_pre, s_target;
+    __shared__ int s_unit, s_flag;
     const int b = blockIdx.y, c = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
@@ -523,125 +556,111 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2) {
     if (idx < 0 || !samples(T)) return;
     if (win == 0ull) return;                  // the logits kernel decided the row
     const float M = key_from_ordered(packed_ordered(win));
+    const uint64_t pol = tc::policy_evict_first();
+    uint64_t *units = a.sums + (int64_t)b * nu;
 
-    // this block's weight sum: 8 consecutive ids per 16-byte load, both
-    // loads issued before any weight (consecutive threads, consecutive ids)
-    const int v0 = c * kCdfIds, v1 = min(a.V, v0 + kCdfIds);
-    constexpr int kU = kCdfIds / (8 * kBatchThreads);
-    float x[kU][8];
-    bool ok[kU];
+    // every round's 8 logits are loaded before any weight
+    const int v0 = c * kCdfIds;
+    float x[kCdfRounds][8];
+    bool ok[kCdfRounds];
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-        const int vv = v0 + (u * kBatchThreads + tid) * 8;
-        ok[u] = vv < v1;
-        if (ok[u]) cache8(a, b, i, vv, x[u]);
+    for (int r = 0; r < kCdfRounds; ++r) {
+        const int vv = v0 + r * (8 * kBatchThreads) + tid * 8;
+        ok[r] = vv < a.V;
+        if (ok[r]) cache8_last(a, b, i, vv, pol, x[r]);
     }
-    uint64_t part = 0ull;
 #pragma unroll
-    for (int u = 0; u < kU; ++u)
-        if (ok[u]) {
+    for (int r = 0; r < kCdfRounds; ++r) {
+        uint64_t part = 0ull;
+        if (ok[r]) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) part += cdf_weight_of(x[u][e], T, M);
+            for (int e = 0; e < 8; ++e) part += cdf_weight_of(x[r][e], T, M);
         }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if (lane == 0) s_w[warp] = part;
-    __syncthreads();
-    if (tid == 0) {
-        uint64_t sum = 0ull;
-        for (int w = 0; w < kBW; ++w) sum += s_w[w];
-        a.sums[(int64_t)b * nb2 + c] = sum;
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        const int u = (c * kCdfRounds + r) * kBW + warp;
+        if (lane == 0 && u < nu) units[u] = part;
     }
     if (!last_block(row_counter(a, i, b), (uint32_t)nb2, &s_flag)) return;
 
-    // last block of the row: the block whose prefix range holds the target
+    // last block of the row: the unit whose prefix range holds the target;
+    // thread t takes units 4t .. 4t + 3 (nu <= 4 kBatchThreads)
     if (tid == 0) {
         *row_counter(a, i, b) = 0u;
-        s_tok = -1;
+        s_unit = -1;
     }
-    if (warp == 0) {
-        const unsigned long long *sums =
-            reinterpret_cast<const unsigned long long *>(a.sums + (int64_t)b * nb2);
-        const uint64_t x0 = 2 * lane < nb2 ? __ldcg(sums + 2 * lane) : 0ull;
-        const uint64_t x1 = 2 * lane + 1 < nb2 ? __ldcg(sums + 2 * lane + 1) : 0ull;
-        uint64_t incl = x0 + x1;
+    uint64_t w4[4];
+    uint64_t mine = 0ull;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const uint64_t S = __shfl_sync(0xffffffffu, incl, 31);
-        const uint64_t excl = incl - x0 - x1;
-        const uint64_t H =
-            dm_cdf_hash(dm_row_step_hash((uint64_t)a.seeds[b], (uint32_t)b, (uint32_t)i));
-        const uint64_t target = __umul64hi(H, S);
-        int hit = -1;
-        uint64_t hitpre = 0ull;
-        if (x0 && excl <= target && target < excl + x0) {
-            hit = 2 * lane;
-            hitpre = excl;
-        } else if (x1 && excl + x0 <= target && target < excl + x0 + x1) {
-            hit = 2 * lane + 1;
-            hitpre = excl + x0;
-        }
-        const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
-        const int src = m ? __ffs(m) - 1 : 0;
-        const int cb = __shfl_sync(0xffffffffu, hit, src);
-        const uint64_t pre = __shfl_sync(0xffffffffu, hitpre, src);
-        if (lane == 0) {
-            s_blk = m ? cb : -1;
-            s_blkpre = pre;
+    for (int k = 0; k < 4; ++k) {
+        const int u = 4 * tid + k;
+        w4[k] = u < nu ? __ldcg(reinterpret_cast<const unsigned long long *>(units) + u) : 0ull;
+        mine += w4[k];
+    }
+    uint64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_w[warp] = incl;
+    __syncthreads();
+    uint64_t wpre = 0ull, S = 0ull;
+#pragma unroll
+    for (int w = 0; w < kBW; ++w) {
+        wpre += w < warp ? s_w[w] : 0ull;
+        S += s_w[w];
+    }
+    const uint64_t target =
+        __umul64hi(dm_cdf_hash(dm_row_step_hash((uint64_t)a.seeds[b], (uint32_t)b, (uint32_t)i)), S);
+    uint64_t pre = wpre + incl - mine;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (w4[k] && pre <= target && target < pre + w4[k]) {
+            s_unit = 4 * tid + k;
+            s_pre = pre;
             s_target = target;
         }
+        pre += w4[k];
     }
     __syncthreads();
-    const int cb = s_blk;
-    if (cb >= 0) {
-        // scan the target block: 16 consecutive ids per thread, in vocab order
-        const uint64_t target = s_target;
-        const int w0 = cb * kCdfIds, w1 = min(a.V, w0 + kCdfIds);
-        constexpr int kPer = kCdfIds / kBatchThreads;   // consecutive ids per thread
-        const int c0 = w0 + tid * kPer;
-        float y[kPer / 8][8];
-        bool oky[kPer / 8];
+    const int u = s_unit;
+    if (warp != 0) return;
+    int64_t tok = -1;
+    if (u >= 0) {
+        // the target unit: lane l takes ids 256 u + 8 l .. + 7, in order
+        const uint64_t tgt = s_target;
+        const int v = u * 256 + lane * 8;
+        float y[8];
+        uint64_t wl = 0ull;
+        if (v < a.V) {
+            cache8_last(a, b, i, v, pol, y);
 #pragma unroll
-        for (int u = 0; u < kPer / 8; ++u) {
-            oky[u] = c0 + 8 * u < w1;
-            if (oky[u]) cache8(a, b, i, c0 + 8 * u, y[u]);
+            for (int e = 0; e < 8; ++e) wl += cdf_weight_of(y[e], T, M);
         }
-        uint64_t mine = 0ull;
-#pragma unroll
-        for (int u = 0; u < kPer / 8; ++u)
-            if (oky[u]) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mine += cdf_weight_of(y[u][e], T, M);
-            }
-        uint64_t incl = mine;
+        uint64_t inc = wl;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const uint64_t z = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += z;
         }
-        if (lane == 31) s_w[warp] = incl;
-        __syncthreads();
-        uint64_t wpre = 0ull;
-        for (int w = 0; w < warp; ++w) wpre += s_w[w];
-        uint64_t run = s_blkpre + wpre + incl - mine;
-        if (mine && run <= target && target < run + mine) {
-            int hit = -1;
+        uint64_t run = s_pre + inc - wl;
+        int hit = -1;
+        if (wl && run <= tgt && tgt < run + wl) {
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                if (hit < 0 && oky[k >> 3]) {
-                    run += cdf_weight_of(y[k >> 3][k & 7], T, M);
-                    if (run > target) hit = k;
-                }
+            for (int e = 0; e < 8; ++e) {
+                run += cdf_weight_of(y[e], T, M);
+                if (hit < 0 && run > tgt) hit = e;
             }
-            if (hit >= 0) s_tok = c0 + hit;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const int h = __shfl_sync(0xffffffffu, hit, src);
+            tok = (int64_t)u * 256 + src * 8 + h;
         }
     }
-    __syncthreads();
-    if (tid == 0) {
-        int64_t tok = s_tok;
+    if (lane == 0) {
         if (tok < 0) {
             set_status(a.status, 6u /* MARKOV_EDEVICE */, 0x200u + i);
             tok = 0;
@@ -699,6 +718,7 @@ cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches
     // one wave: the plan's vocab blocks shared out over the row groups
     const int nblk = a.grid / groups > 0 ? a.grid / groups : 1;
     const int nb2 = (a.V + kCdfIds - 1) / kCdfIds;
+    const int nu = (a.V + 255) / 256;            // 256-id weight units per row
     const size_t smem = (size_t)group_rows * (a.r + kBPad) * sizeof(uint16_t);
     *launches = 0;
     if (nb2 > 64 || a.rows > kMaxRows || a.N > kMaxSteps) return cudaErrorInvalidValue;
@@ -722,7 +742,7 @@ cudaError_t launch_batch(const SampleArgs &a, cudaStream_t stream, int *launches
             e = launch_one(logits, dim3(nblk, groups), smem, stream, i > 0, a, i);
         ++n;
         if (e == cudaSuccess && a.mode == 1) {
-            e = launch_one(batch_cdf_kernel, dim3(nb2, a.rows), 0, stream, true, a, i, nb2);
+            e = launch_one(batch_cdf_kernel, dim3(nb2, a.rows), 0, stream, true, a, i, nb2, nu);
             ++n;
         }
     }

@@ -108,6 +108,14 @@ __device__ __forceinline__ uint32_t bt_ordered(float k) {
     return (b & 0x7fffffffu) > 0x7f800000u ? 0xffffffffu : o;
 }
 
+// One 32-byte global store (the address 32-byte aligned).
+__device__ __forceinline__ void st_v8(void *p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                      uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1),
+                 "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
 // The output-logit transforms (out of line: only transformed heads take them).
 __device__ __noinline__ float bt_transform_f32(float s, const Transform tf) {
     float y = __fmul_rn(s, tf.mult);
@@ -169,14 +177,16 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
     tc::fence_after_sync();
     const uint32_t tmem = c.tmem_base;
     int produced = 0;
+    // the head stays in L2 across positions; base logits are read once
+    const uint64_t keep = tc::policy_evict_last();
     if (warp == 0 && lane == 0) {
         // the first stages' head chunks (the head is an input: never written)
         for (int s = 0; s < kBtStages; ++s) c.issued[s] = 0u;
         for (; produced < nch && produced < kBtStages; ++produced) {
             const uint32_t bar = tc::smem_u32(&c.full[produced]);
             tc::mbar_expect_tx(bar, kBtChunk);
-            tc::tma_load_2d(st_sa + produced * kBtChunk, &tmap, (produced % cpt) * 64,
-                            (t0 + produced / cpt) * 128, bar);
+            tc::tma_load_2d_hint(st_sa + produced * kBtChunk, &tmap, (produced % cpt) * 64,
+                                 (t0 + produced / cpt) * 128, bar, keep);
             ++c.issued[produced];
         }
     }
@@ -250,14 +260,14 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
             for (int j = produced; j < nch; ++j) {
                 if (bt_aborted(c)) break;
                 const int s = j % kBtStages;
-                if (!tc::mbar_wait(tc::smem_u32(&c.empty[s]), (uint32_t)((j / kBtStages) - 1) & 1u,
-                                   tc::now_ns() + timeout)) {
+                if (!tc::mbar_wait_for(tc::smem_u32(&c.empty[s]), (uint32_t)((j / kBtStages) - 1) & 1u, timeout)) {
                     bt_fail(c, a, 0x310u);
                     break;
                 }
                 const uint32_t bar = tc::smem_u32(&c.full[s]);
                 tc::mbar_expect_tx(bar, kBtChunk);
-                tc::tma_load_2d(st_sa + s * kBtChunk, &tmap, (j % cpt) * 64, (t0 + j / cpt) * 128, bar);
+                tc::tma_load_2d_hint(st_sa + s * kBtChunk, &tmap, (j % cpt) * 64, (t0 + j / cpt) * 128, bar,
+                                     keep);
                 ++c.issued[s];
             }
         }
@@ -271,7 +281,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 if (bt_aborted(c)) break;
                 const int ab = p & 1, use = p >> 1;
                 if (use > 0 &&
-                    !tc::mbar_wait(tc::smem_u32(&c.accr[ab]), (uint32_t)(use - 1) & 1u, tc::now_ns() + timeout)) {
+                    !tc::mbar_wait_for(tc::smem_u32(&c.accr[ab]), (uint32_t)(use - 1) & 1u, timeout)) {
                     bt_fail(c, a, 0x320u);
                     break;
                 }
@@ -285,8 +295,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
 #pragma unroll
                     for (int kc = 0; kc < cpt; ++kc) {
                         const int j = k * cpt + kc, s = j % kBtStages;
-                        if (!tc::mbar_wait(tc::smem_u32(&c.full[s]), (uint32_t)(j / kBtStages) & 1u,
-                                           tc::now_ns() + timeout)) {
+                        if (!tc::mbar_wait_for(tc::smem_u32(&c.full[s]), (uint32_t)(j / kBtStages) & 1u, timeout)) {
                             ok = false;
                             break;
                         }
@@ -323,8 +332,15 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
         const bool vec = ((reinterpret_cast<uintptr_t>(kBaseF32 ? (const void *)a.base_f : (const void *)a.base) &
                            15u) == 0u) &&
                          (a.base_s0 % kEpV) == 0 && (a.base_s1 % kEpV) == 0;
-        uint32_t bo = 0u, bid = 0u;   // the row's best ordered key and its id
+        // the row's best key so far and its id (kNone: no key yet)
+        constexpr uint32_t kNone = 0xffffffffu;
+        float bf = 0.0f;
+        uint32_t bid = kNone;
+        // 32-byte cache stores need 32-byte aligned rows
+        const bool st32 = ((reinterpret_cast<uintptr_t>(cache_f32 ? (void *)a.cache_f : (void *)a.cache) & 31u) == 0u) &&
+                          ((a.cache_s0 * (cache_f32 ? 4 : 2)) % 32) == 0 && ((a.cache_s1 * (cache_f32 ? 4 : 2)) % 32) == 0;
         constexpr int kNB = kBaseF32 ? 32 : 16;      // base words of 32 ids
+        const uint64_t once = tc::policy_evict_first();
         // the base logits of this thread's 32 ids of pair p (zeros outside)
         auto load_base = [&](int p, uint32_t (&w)[kNB]) {
             const int k = 2 * p + hy;
@@ -336,7 +352,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 for (int u = 0; u < 32; u += 4) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
                     if (on && vec && v0 + u < V) {
-                        x = __ldg(reinterpret_cast<const uint4 *>(src + u));
+                        x = tc::ld_nc_v4_hint(src + u, once);
                     } else if (on && !vec) {
                         x.x = v0 + u < V ? __float_as_uint(__ldg(src + u)) : 0u;
                         x.y = v0 + u + 1 < V ? __float_as_uint(__ldg(src + u + 1)) : 0u;
@@ -354,7 +370,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 for (int u = 0; u < 16; u += 4) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
                     if (on && vec && v0 + 2 * u < V) {
-                        x = __ldg(reinterpret_cast<const uint4 *>(src + 2 * u));
+                        x = tc::ld_nc_v4_hint(src + 2 * u, once);
                     } else if (on && !vec) {
                         uint32_t y[4];
 #pragma unroll
@@ -387,7 +403,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
             const int ab = p & 1;
             bool ok = true;
             if (lane == 0)
-                ok = tc::mbar_wait(tc::smem_u32(&c.accf[ab]), (uint32_t)(p >> 1) & 1u, tc::now_ns() + timeout);
+                ok = tc::mbar_wait_for(tc::smem_u32(&c.accf[ab]), (uint32_t)(p >> 1) & 1u, timeout);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) bt_fail(c, a, 0x340u);
@@ -397,7 +413,6 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
             const int k = 2 * p + hy;
             const int v0 = (t0 + k) * 128 + 32 * cg;
             const bool on = live && k < nt && v0 < V;
-            const bool full = v0 + 32 <= V;
             const uint32_t dcol = tmem + ((uint32_t)(q * 32) << 16) + kBtD + (uint32_t)(ab * 128 + 32 * cg);
 #pragma unroll
             for (int h16 = 0; h16 < 2; ++h16) {
@@ -411,8 +426,8 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&c.accr[ab]));
                 }
-                if (!on) continue;
                 const int vh = v0 + 16 * h16;
+                if (!on || vh >= V) continue;
                 // 8 id pairs: bias = bf16(sum); l = f32(base) + f32(bias),
                 // rounded to the cache's type and transformed
                 uint32_t lp[8];
@@ -441,66 +456,111 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                     lf[2 * j] = l0;
                     lf[2 * j + 1] = l1;
                 }
-                // the cache: 16-byte stores (its rows are 16-byte aligned);
-                // the vocab tail (V a multiple of 16) by whole stores
+                // the cache: one 32-byte store per 16 BF16 ids where the
+                // cache rows are 32-byte aligned, else 16-byte stores (the
+                // rows are 16-byte aligned); the vocabulary is a multiple of
+                // 16, so a half is whole
                 if (cache_f32) {
                     float *dst = a.cache_f + crow + vh;
+                    if (st32) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (full || vh + 4 * u < V)
+                        for (int u = 0; u < 2; ++u)
+                            st_v8(dst + 8 * u, __float_as_uint(lf[8 * u]), __float_as_uint(lf[8 * u + 1]),
+                                  __float_as_uint(lf[8 * u + 2]), __float_as_uint(lf[8 * u + 3]),
+                                  __float_as_uint(lf[8 * u + 4]), __float_as_uint(lf[8 * u + 5]),
+                                  __float_as_uint(lf[8 * u + 6]), __float_as_uint(lf[8 * u + 7]));
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
                             *reinterpret_cast<float4 *>(dst + 4 * u) =
                                 make_float4(lf[4 * u], lf[4 * u + 1], lf[4 * u + 2], lf[4 * u + 3]);
+                    }
                 } else {
                     uint16_t *dst = a.cache + crow + vh;
+                    if (st32) {
+                        st_v8(dst, lp[0], lp[1], lp[2], lp[3], lp[4], lp[5], lp[6], lp[7]);
+                    } else {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (full || vh + 8 * u < V)
+                        for (int u = 0; u < 2; ++u)
                             *reinterpret_cast<uint4 *>(dst + 8 * u) =
                                 make_uint4(lp[4 * u], lp[4 * u + 1], lp[4 * u + 2], lp[4 * u + 3]);
+                    }
                 }
                 // keys: the logit, or for a sampling Gumbel row fp32(l / T)
-                // + the call's noise; ids in increasing order, so a strict
-                // comparison keeps the lowest id of equal keys
-                float gn[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) gn[u] = 0.0f;
+                // + the call's noise
+                float key[16];
                 if (gum) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        if (full || vh + 4 * u < V) {
-                            const float4 x = __ldg(reinterpret_cast<const float4 *>(nrow + vh) + u);
-                            gn[4 * u] = x.x;
-                            gn[4 * u + 1] = x.y;
-                            gn[4 * u + 2] = x.z;
-                            gn[4 * u + 3] = x.w;
-                        }
+                        const float4 x = __ldg(reinterpret_cast<const float4 *>(nrow + vh) + u);
+                        key[4 * u] = __fadd_rn(__fdiv_rn(lf[4 * u], T), x.x);
+                        key[4 * u + 1] = __fadd_rn(__fdiv_rn(lf[4 * u + 1], T), x.y);
+                        key[4 * u + 2] = __fadd_rn(__fdiv_rn(lf[4 * u + 2], T), x.z);
+                        key[4 * u + 3] = __fadd_rn(__fdiv_rn(lf[4 * u + 3], T), x.w);
                     }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) key[u] = lf[u];
+                }
+                // the half's best: a tree of strict comparisons, the
+                // lower-id side winning ties (16 keys in id order), and a
+                // NaN / infinity test (x 0 is NaN for both)
+                float tv[8];
+                uint32_t ti[8];
+                float poison = 0.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const bool r = key[2 * j + 1] > key[2 * j];
+                    tv[j] = r ? key[2 * j + 1] : key[2 * j];
+                    ti[j] = r ? 2u * j + 1u : 2u * j;
+                    poison = __fmaf_rn(key[2 * j], 0.0f, poison);
+                    poison = __fmaf_rn(key[2 * j + 1], 0.0f, poison);
                 }
 #pragma unroll
-                for (int e2 = 0; e2 < 16; ++e2) {
-                    float key = lf[e2];
-                    if (gum) key = __fadd_rn(__fdiv_rn(key, T), gn[e2]);
-                    const uint32_t o = bt_ordered(key);
-                    const bool better = (full || vh + e2 < V) && o > bo;
-                    bo = better ? o : bo;
-                    bid = better ? (uint32_t)(vh + e2) : bid;
+                for (int w = 4; w >= 1; w >>= 1) {
+#pragma unroll
+                    for (int j = 0; j < w; ++j) {
+                        const bool r = tv[2 * j + 1] > tv[2 * j];
+                        tv[j] = r ? tv[2 * j + 1] : tv[2 * j];
+                        ti[j] = r ? ti[2 * j + 1] : ti[2 * j];
+                    }
+                }
+                if (poison == 0.0f) {
+                    // halves come in increasing id order: a strict
+                    // comparison keeps the earlier of equal keys
+                    const bool better = bid == kNone || tv[0] > bf;
+                    bf = better ? tv[0] : bf;
+                    bid = better ? (uint32_t)vh + ti[0] : bid;
+                } else {
+                    // a NaN or an infinity in the half: the exact ordered
+                    // keys (a NaN above all, the lowest NaN id first)
+                    uint32_t ob = bid == kNone ? 0u : bt_ordered(bf);
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const uint32_t o = bt_ordered(key[e2]);
+                        const bool better = o > ob;
+                        ob = better ? o : ob;
+                        bf = better ? key[e2] : bf;
+                        bid = better ? (uint32_t)(vh + e2) : bid;
+                    }
                 }
             }
         }
         // the thread's best into the block's (4 threads share a row)
-        if (live && bo)
-            atomicMax(&c.best[rr], ((unsigned long long)bo << 32) | (unsigned long long)(0xffffffffu - bid));
+        if (live && bid != kNone)
+            atomicMax(&c.best[rr],
+                      ((unsigned long long)bt_ordered(bf) << 32) | (unsigned long long)(0xffffffffu - bid));
     }
 
     // ---- every async operation completes before TMEM is released
     if (warp == 1 && lane == 0) {
         tc::commit(tc::smem_u32(&c.fin));
-        tc::mbar_wait(tc::smem_u32(&c.fin), 0u, tc::now_ns() + 1000000000ull);
+        tc::mbar_wait_for(tc::smem_u32(&c.fin), 0u, 1000000000ull);
     }
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < kBtStages; ++s) {
             if (c.issued[s] == 0u) continue;
-            tc::mbar_wait(tc::smem_u32(&c.full[s]), (c.issued[s] - 1u) & 1u, tc::now_ns() + 1000000000ull);
+            tc::mbar_wait_for(tc::smem_u32(&c.full[s]), (c.issued[s] - 1u) & 1u, 1000000000ull);
         }
     }
     tc::fence_before_sync();

@@ -230,8 +230,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                 uint64_t part = 0ull;
                 for (int v = v_begin + tid; v < v_end; v += kChainThreads) {
                     float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
-                    float w = dm_exp(__fsub_rn(x, M));
-                    part += (uint64_t)__float2ull_rz(__fmul_rn(w, 0x1p40f));
+                    part += dm_cdf_weight(__fsub_rn(x, M));
                 }
 #pragma unroll
                 for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
@@ -283,7 +282,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                     uint64_t mine = 0ull;
                     for (int v = c0; v < c1; ++v) {
                         float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
-                        mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                        mine += dm_cdf_weight(__fsub_rn(x, M));
                     }
                     // exclusive scan of `mine` over the CTA, in thread order
                     uint64_t incl = mine;
@@ -300,7 +299,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const SampleArg
                     if (run <= target && target < run + mine) {
                         for (int v = c0; v < c1; ++v) {
                             float x = __fdiv_rn(cache_value(a, b, i, v), rs.T[b]);
-                            run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                            run += dm_cdf_weight(__fsub_rn(x, M));
                             if (run > target) {
                                 tok_slot[b] = (uint64_t)v;
                                 break;

@@ -298,7 +298,7 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
         if (__any_sync(0xffffffffu, aborted(c, a))) break;
         bool freed = true;
         if (uses > 0)
-            freed = tc::mbar_wait(tc::smem_u32(&c.dfree[W]), (uses - 1) & 1u, tc::now_ns() + timeout);
+            freed = tc::mbar_wait_for(tc::smem_u32(&c.dfree[W]), (uses - 1) & 1u, timeout);
         if (!__all_sync(0xffffffffu, freed)) {
             if (lane == 0) fail(c, a, 4u, 0x1000u + i);
             break;
@@ -506,7 +506,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         // memory A chunks and the staged B rows, into sbias
         bool st = true;
         if (lane == 0)
-            st = tc::mbar_wait(tc::smem_u32(&c.bstaged), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+            st = tc::mbar_wait_for(tc::smem_u32(&c.bstaged), (uint32_t)(i - 1) & 1u, timeout);
         st = __shfl_sync(0xffffffffu, st, 0);
         if (!st) {
             if (lane == 0) fail(c, a, 4u, 0xC000u + i);
@@ -532,7 +532,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
         if (k == nts) {
             // the mma.sync tile (group 0's last): its bias from sbias
             if (lane == 0)
-                ok = tc::mbar_wait(tc::smem_u32(&c.sdone), (uint32_t)(i - 1) & 1u, tc::now_ns() + timeout);
+                ok = tc::mbar_wait_for(tc::smem_u32(&c.sdone), (uint32_t)(i - 1) & 1u, timeout);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(c, a, 4u, 0xD000u + i);
@@ -545,7 +545,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             r[3] = __float_as_uint(sb.w);
         } else {
             if (lane == 0)
-                ok = tc::mbar_wait(tc::smem_u32(&c.dfull[wg]), dcount & 1u, tc::now_ns() + timeout);
+                ok = tc::mbar_wait_for(tc::smem_u32(&c.dfull[wg]), dcount & 1u, timeout);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(c, a, 4u, 0x6000u + i);
@@ -891,13 +891,13 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         int s;
                         uint32_t ph;
                         chunk_slot(j, ntm, s, ph);
-                        if (!tc::mbar_wait(tc::smem_u32(&c.full[s]), ph & 1u, tc::now_ns() + timeout)) {
+                        if (!tc::mbar_wait_for(tc::smem_u32(&c.full[s]), ph & 1u, timeout)) {
                             fail(c, a, 4u, 0x4000u + j);
                             break;
                         }
                         if (j > 0 && sp == s) {
                             // (already complete: this load waited for it)
-                            if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[sp]), pp & 1u, tc::now_ns() + timeout)) {
+                            if (!tc::mbar_wait_for(tc::smem_u32(&c.cpdone[sp]), pp & 1u, timeout)) {
                                 fail(c, a, 4u, 0x5000u + j - 1);
                                 break;
                             }
@@ -913,7 +913,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                     if (j > 0 && !early) {
                         // chunk j - 1, in another slot than chunk j's
-                        if (!tc::mbar_wait(tc::smem_u32(&c.cpdone[sp]), pp & 1u, tc::now_ns() + timeout)) {
+                        if (!tc::mbar_wait_for(tc::smem_u32(&c.cpdone[sp]), pp & 1u, timeout)) {
                             fail(c, a, 4u, 0x5000u + j - 1);
                             break;
                         }
@@ -1133,7 +1133,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         for (int k = 0; k < kPT; ++k) {
                             if (v_begin + tid + k * kThreads >= v_end) break;
                             const float x = __fdiv_rn(xs[r][k], c.T[b]);
-                            part += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                            part += dm_cdf_weight(__fsub_rn(x, M));
                         }
     #pragma unroll
                         for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
@@ -1221,7 +1221,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         uint64_t mine = 0ull;
                         for (int v = c0; v < c1; ++v) {
                             const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
-                            mine += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                            mine += dm_cdf_weight(__fsub_rn(x, M));
                         }
                         uint64_t incl = mine;
     #pragma unroll
@@ -1237,7 +1237,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         if (run <= target && target < run + mine) {
                             for (int v = c0; v < c1; ++v) {
                                 const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
-                                run += (uint64_t)__float2ull_rz(__fmul_rn(dm_exp(__fsub_rn(x, M)), 0x1p40f));
+                                run += dm_cdf_weight(__fsub_rn(x, M));
                                 if (run > target) {
                                     tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
                                                        ((uint64_t)v << 32) | tag32);
@@ -1310,13 +1310,12 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     if (warp < 2) {
         __syncwarp();
         tc::commit_elect(tc::smem_u32(&c.fin[warp]));
-        tc::mbar_wait(tc::smem_u32(&c.fin[warp]), 0u, tc::now_ns() + 1000000000ull);
+        tc::mbar_wait_for(tc::smem_u32(&c.fin[warp]), 0u, 1000000000ull);
     }
     if (warp == 2 && lane == 0) {
         for (int s = 0; s < kSmemChunks; ++s) {
             if (issued[s] == 0u) continue;
-            tc::mbar_wait(tc::smem_u32(&c.full[s]), (issued[s] - 1u) & 1u,
-                          tc::now_ns() + 1000000000ull);
+            tc::mbar_wait_for(tc::smem_u32(&c.full[s]), (issued[s] - 1u) & 1u, 1000000000ull);
         }
     }
     tc::fence_before_sync();

@@ -79,6 +79,32 @@ __device__ __forceinline__ float dm_exp(float x) {
     return __fmul_rn(p, __uint_as_float((uint32_t)(k + 127) << 23));
 }
 
+// The inverse-CDF integer weight floor(exp(d) 2^40) of d = fp32(x / T) - M
+// for d <= 0 (M the row's maximum of fp32(x / T), finite): dm_exp's steps
+// with the 2^40 folded into its final power-of-two scale, and zero below
+// d = -28.  Both are exact rewrites: for -28 <= d <= 0, k = rint(d log2 e)
+// lies in [-41, 0], so p 2^k and p 2^(k + 40) are normal and the two
+// power-of-two products exact; below -28 the exp is under e^-28 (1 + 2^-20)
+// < 2^-40, whose scaled floor is 0 (as it is for d = -inf).  The select
+// keeps lanes of a warp from diverging.
+__device__ __forceinline__ uint64_t dm_cdf_weight(float d) {
+    const float kf = rintf(__fmul_rn(d, 0x1.715476p+0f));
+    float r = __fmaf_rn(-kf, 0x1.62e300p-1f, d);
+    r = __fmaf_rn(-kf, 0x1.2fefa2p-17f, r);
+    float p = 0x1.a01a02p-13f;
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);
+    p = __fmaf_rn(p, r, 0x1.000000p-1f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int k = __float2int_rn(kf);
+    const float w = __fmul_rn(p, __uint_as_float((uint32_t)(k + 167) << 23));
+    const uint64_t q = (uint64_t)__float2ull_rz(w);
+    return d >= -28.0f ? q : 0ull;
+}
+
 __device__ __forceinline__ float dm_tanh(float u) {
     float a = fabsf(u);
     if (a < 0.5f) {

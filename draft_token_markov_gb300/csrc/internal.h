@@ -27,7 +27,8 @@ constexpr size_t kWinCntN = (size_t)2 * kMaxSteps * kLineU32;
 constexpr int kBatchCntPerStep = kMaxRows / 16 + kMaxRows;
 constexpr size_t kBatchWinN = (size_t)kMaxSteps * kMaxRows;
 constexpr size_t kBatchCntN = (size_t)kMaxSteps * kBatchCntPerStep;
-constexpr int kCdfIds = kBatchThreads * 16;   // vocab ids per inverse-CDF sum block
+constexpr int kCdfRounds = 6;                 // 8-id loads per thread of an inverse-CDF block
+constexpr int kCdfIds = kBatchThreads * 8 * kCdfRounds;   // vocab ids per inverse-CDF block
 
 // The output-logit transform (muse_spark markov page, FusedMarkovParams):
 // multiplier and cap rounded to fp32, inv_cap = fp32(1) / fp32(cap).

@@ -203,6 +203,9 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     const int Gp = (p->chain_grid + kKeyPad - 1) / kKeyPad * kKeyPad;
     size_t chain_keys = (size_t)kMaxSteps * 2 * kChainRows * Gp;
     size_t batch_keys = (size_t)d.max_rows * p->batch_grid;
+    // the per-position path's inverse-CDF weight sums: one per 256 ids and row
+    const size_t unit_sums = (size_t)d.max_rows * ((d.vocab + 255) / 256);
+    if (batch_keys < unit_sums) batch_keys = unit_sums;
     p->keys_n = chain_keys > batch_keys ? chain_keys : batch_keys;
     p->noise_s0 = d.vocab;
     // fp32 noise of every row for the per-position kernels; the tcgen05 chain
@@ -514,7 +517,7 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
 }
 
 markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n, void *stream) {
-    if (fn < 0 || fn > 9 || n < 0 || (n > 0 && (!x || !y)) || (fn == 9 && n % 3 != 0))
+    if (fn < 0 || fn > 11 || n < 0 || (n > 0 && (!x || !y)) || (fn == 9 && n % 3 != 0))
         return MARKOV_EINVAL;
     if (launch_device_math(fn, x, y, n, (cudaStream_t)stream) != cudaSuccess) return MARKOV_ECUDA;
     return MARKOV_OK;

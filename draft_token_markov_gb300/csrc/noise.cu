@@ -78,6 +78,8 @@ __global__ void device_math_kernel(int fn, const float *__restrict__ x, float *_
                 // the noise byte of the uniform mantissa m (x holds m's bits)
                 r = (float)quantize_upper(gumbel_upper((uint64_t)(__float_as_uint(v) & 0x7fffffu) << 41));
                 break;
+            case 10: r = __uint_as_float((uint32_t)dm_cdf_weight(v)); break;
+            case 11: r = __uint_as_float((uint32_t)(dm_cdf_weight(v) >> 32)); break;
             case 7: r = dequantize_upper((uint32_t)v); break;
             case 8: r = dequantize_lower((uint32_t)v); break;
             case 0: r = dm_log(v); break;

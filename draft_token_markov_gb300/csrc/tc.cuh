@@ -77,6 +77,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     return true;
 }
 
+// The same with the limit counted from the first failed test: a phase that
+// is already complete costs one test and no timer read (a globaltimer read
+// costs about as much as an MMA issue).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_test(bar, parity)) return true;
+    return mbar_wait(bar, parity, now_ns() + timeout_ns);
+}
+
 // Warp maximum of a 64-bit key in two 32-bit reductions (high word, then
 // the low word among the lanes holding the highest high word).
 __device__ __forceinline__ uint64_t warp_max_u64(uint64_t x) {
@@ -97,6 +105,39 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         "%3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// L2 cache policies for the .L2::cache_hint forms: evict_last keeps lines
+// that later launches read again (the head), evict_first marks data read
+// once (base logits, the cache's last read).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// A read-only 16-byte global load with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const void *p, uint64_t policy) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(policy));
+    return r;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p) {

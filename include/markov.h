@@ -266,7 +266,10 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
  * fn 7 / 8 the upper / lower noise bound of the byte q passed as a float
  * value; fn 9 on triples (l, T, m bits), n a multiple of 3: the Gumbel key's
  * lower bound, its upper bound and the exact key fp32(l / T) + gumbel(u) as
- * the chain computes them.  These are the functions the kernels use;
+ * the chain computes them.  fn 10 / 11: the low / high 32 bits (read as
+ * uint32) of the inverse-CDF integer weight floor(exp(d) 2^40) of
+ * d = fp32(l / T) - M <= 0, as every inverse-CDF kernel computes it.  These
+ * are the functions the kernels use;
  * exposed so they can be compared bit for bit with an independent
  * implementation, or checked against it as bounds.  EINVAL for an unknown
  * fn. */

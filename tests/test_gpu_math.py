@@ -125,3 +125,41 @@ def test_gumbel_key_bounds_bracket_the_exact_key(gpu_lib):
     hi = np.where(np.isnan(hi), np.inf, hi)
     assert np.all(lo <= key), int(np.sum(~(lo <= key)))
     assert np.all(key <= hi), int(np.sum(~(key <= hi)))
+
+
+def _weights(api, d: np.ndarray) -> np.ndarray:
+    lo = _dev(api, 10, d).view(np.uint32).astype(np.uint64)
+    hi = _dev(api, 11, d).view(np.uint32).astype(np.uint64)
+    return lo | (hi << np.uint64(32))
+
+
+def _oracle_weights(d: np.ndarray) -> np.ndarray:
+    # the oracle's inverse-CDF weight: its exp, an exact fp32 scale by 2^40,
+    # then truncation to an unsigned integer
+    e = oracle.exp(d).astype(np.float32) * np.float32(2.0 ** 40)
+    return e.astype(np.uint64)
+
+
+def test_cdf_weight_matches_the_oracle(gpu_lib):
+    # (1) every 257th fp32 in [-40, 0] (bit patterns of -0 .. -40), (2) every
+    # fp32 around the -28 cut, (3) the d = fp32(x / T) - M of every finite
+    # BF16 logit x for several temperatures and maxima M >= every x / T
+    neg40 = int(np.float32(-40.0).view(np.uint32))
+    d1 = np.arange(0x80000000, neg40 + 1, 257, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    c = int(np.float32(-28.0).view(np.uint32))
+    d2 = np.arange(c - (1 << 18), c + (1 << 18), dtype=np.uint64).astype(np.uint32).view(np.float32)
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    x = (bits << 16).view(np.float32)
+    x = x[np.isfinite(x)]
+    d3 = []
+    for T in (0.37, 0.5, 0.7, 0.8, 1.0, 1.2, 3.0):
+        q = (x / np.float32(T)).astype(np.float32)
+        for M in (q.max(), np.float32(0.0) + q.max() * np.float32(0.5), np.float32(12.5),
+                  np.float32(30.0)):
+            d = (q - np.float32(M)).astype(np.float32)
+            d3.append(d[d <= 0])
+    d = np.concatenate([d1, d2, np.float32([-np.inf, -0.0, 0.0, -27.7, -27.73, -28.0])] + d3)
+    assert np.all((d <= 0) | np.isneginf(d))
+    got, want = _weights(gpu_lib, d), _oracle_weights(d)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (d[bad[:5]], got[bad[:5]], want[bad[:5]])
