@@ -83,7 +83,7 @@ struct Ctl {
     uint32_t lcta[2][kChainRows];
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
-    uint64_t scan[kThreads / 32];    // inverse-CDF scan: per-warp weight totals
+    uint64_t wsum[kChainRows][kThreads / 32];   // inverse CDF: per-row, per-warp weight totals
     uint32_t tmem_base;
     uint32_t tmem_ready;             // chunks copied into TMEM so far
     uint32_t abort;
@@ -136,16 +136,12 @@ __device__ __forceinline__ bool aborted(const Ctl &c, const SampleArgs &) {
     return *(volatile const uint32_t *)&c.abort != 0u;
 }
 
-// At a CTA barrier: this CTA's flag, or (thread 0 only, one L2 load, when
-// `global` is set) an error another CTA recorded.  The Gumbel positions
-// check the global status in their exchange poll instead, off the barrier.
-__device__ __forceinline__ bool stop_vote(Ctl &c, const SampleArgs &a, bool global = true) {
-    bool s = *(volatile const uint32_t *)&c.abort != 0u;
-    if (global && threadIdx.x == 0 && !s && ld_acquire_u32(a.status) != 0u) {
-        c.abort = 1u;
-        s = true;
-    }
-    return s;
+// At a CTA barrier: this CTA's abort flag.  An error another CTA recorded
+// reaches this one through its exchange polls, which watch the global
+// status off the barriers (a status load here would put an L2 round trip on
+// every barrier).
+__device__ __forceinline__ bool stop_vote(Ctl &c) {
+    return *(volatile const uint32_t *)&c.abort != 0u;
 }
 
 // packed key: ordered key (32) | 0x3FFFF - id (18) | epoch tag (14)
@@ -941,7 +937,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             else
                 epilogue<RANK, false, DT>(c, a, tmem, i, t0, nt, nts, ntm, b_sa, head_sa, gum_any, timeout, dcount);
         }
-        stop = __syncthreads_or(stop_vote(c, a, MODE != 0));
+        stop = __syncthreads_or(stop_vote(c));
         if (stop) break;
 
         // ------------------------------- phase B: agree on every row's winner
@@ -1081,7 +1077,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                 }
             }
-            stop = __syncthreads_or(stop_vote(c, a));
+            stop = __syncthreads_or(stop_vote(c));
             if (stop) break;
 
             // inverse CDF: rows whose maximum M is finite need the exact integer
@@ -1098,66 +1094,89 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             if (cdf_any) {
                 const uint32_t tag32 = epoch;
-                if (tid < kChainRows) c.sum[tid] = 0ull;
-                __syncthreads();
-                // kGR rows a time: every cached logit of the group is loaded
-                // before any weight, so the rows share one read latency
+                // thread t takes the contiguous ids [c0, c1) of the CTA's range,
+                // so each warp's ids are contiguous too: its weight totals per
+                // row (c.wsum) locate the target warp, and a warp scan of the
+                // threads' own totals (mine) the target thread, with no block
+                // barrier and no second pass over the whole range
+                const int len = v_end - v_begin;
+                const int chunk = (len + kThreads - 1) / kThreads;
+                const int c0 = v_begin + tid * chunk;
+                const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
                 constexpr int kMaxIds = (kTmemChunks + kSmemChunks) / (RANK / 64) * 128;
                 constexpr int kPT = (kMaxIds + kThreads - 1) / kThreads;   // ids per thread
                 constexpr int kGR = RANK == 64 ? 2 : 4;
-                for (int b0 = 0; b0 < R && b0 < kChainRows; b0 += kGR) {
+                uint64_t mine[kChainRows];
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) mine[b] = 0ull;
+                // kGR rows a time: every cached logit of the group is loaded
+                // before any weight, so the rows share one read latency
+#pragma unroll
+                for (int b0 = 0; b0 < kChainRows; b0 += kGR) {
+                    if (b0 >= R) break;
                     float xs[kGR][kPT];
                     bool use[kGR];
 #pragma unroll
                     for (int r = 0; r < kGR; ++r) {
                         const int b = b0 + r;
-                        const uint32_t o = b < R && b < kChainRows ? (uint32_t)(c.win[b] >> 32) : 0u;
-                        use[r] = b < R && b < kChainRows && c.sampling[b] && o != 0xffffffffu &&
-                                 !isinf(key_from_ordered(o));
+                        const uint32_t o = b < R ? (uint32_t)(c.win[b] >> 32) : 0u;
+                        use[r] = b < R && c.sampling[b] && o != 0xffffffffu && !isinf(key_from_ordered(o));
                         const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
 #pragma unroll
                         for (int k = 0; k < kPT; ++k) {
-                            const int v = v_begin + tid + k * kThreads;
+                            const int v = c0 + k;
                             xs[r][k] = 0.0f;
-                            if (use[r] && v < v_end)
+                            if (use[r] && v < c1)
                                 xs[r][k] = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
                         }
                     }
 #pragma unroll
                     for (int r = 0; r < kGR; ++r) {
-                        if (!use[r]) continue;
                         const int b = b0 + r;
-                        const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
                         uint64_t part = 0ull;
+                        if (use[r]) {
+                            const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
+                            const float T = c.T[b];
 #pragma unroll
-                        for (int k = 0; k < kPT; ++k) {
-                            if (v_begin + tid + k * kThreads >= v_end) break;
-                            const float x = __fdiv_rn(xs[r][k], c.T[b]);
-                            part += dm_cdf_weight(__fsub_rn(x, M));
+                            for (int k = 0; k < kPT; ++k)
+                                if (c0 + k < c1) part += dm_cdf_weight(__fsub_rn(__fdiv_rn(xs[r][k], T), M));
                         }
-    #pragma unroll
-                        for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-                        if (lane == 0) atomicAdd(&c.sum[b], (unsigned long long)part);
+                        mine[b] = part;
+                        if (__any_sync(0xffffffffu, use[r])) {
+#pragma unroll
+                            for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+                            if (lane == 0) c.wsum[b][warp] = part;
+                        }
                     }
                 }
                 __syncthreads();
-                // each row's sum tagged in its top 12 bits (a CTA's sum is
-                // below 4096 ids x 2^40), stored with release: this CTA's
-                // cache writes are visible to a CTA that reads the tagged sum
+                // each row's CTA sum tagged in its top 12 bits (below 4096 ids
+                // x 2^40): one relaxed 64-bit store carries value and epoch (no
+                // CTA reads another CTA's cache, so nothing else is ordered),
+                // into every replica of the row's slot array (a CTA polls
+                // replica cta % kTcReplicas, which spreads the polls over the
+                // L2 slices as the key slots do)
                 const uint32_t stag = tag32 & 0xFFFu;
-                if (tid < kChainRows && c.sampling[tid]) {
-                    uint64_t *sl = a.tc_sums + ((int64_t)i * kChainRows + tid) * Gp + cta;
-                    const uint64_t w = c.sum[tid] | ((uint64_t)stag << 52);
-                    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(sl), "l"(w) : "memory");
+                if (tid < kChainRows * kTcReplicas) {
+                    const int b = tid / kTcReplicas, rep = tid % kTcReplicas;
+                    uint64_t s = 0ull;
+                    if (b < R && c.sampling[b]) {
+#pragma unroll
+                        for (int w = 0; w < kThreads / 32; ++w) s += c.wsum[b][w];
+                        uint64_t *sl = a.tc_sums + (((int64_t)i * kChainRows + b) * kTcReplicas + rep) * Gp + cta;
+                        tc::st_relaxed_u64(sl, s | ((uint64_t)stag << 52));
+                    }
+                    if (rep == 0) c.sum[b] = s;
                 }
                 // every CTA learns every row's total and its own prefix
                 __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
-                if (warp < kChainRows && c.sampling[warp]) {
+                if (warp < kChainRows && warp < R && c.sampling[warp]) {
                     const int b = warp;
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     const float M = key_from_ordered(o);
                     if (o != 0xffffffffu && !isinf(M)) {
-                        const uint64_t *sl = a.tc_sums + ((int64_t)i * kChainRows + b) * Gp;
+                        const uint64_t *sl =
+                            a.tc_sums + (((int64_t)i * kChainRows + b) * kTcReplicas + cta % kTcReplicas) * Gp;
                         constexpr int kPer = kMaxGrid / 32;
                         const uint64_t dl = tc::now_ns() + timeout;
                         bool ok = true;
@@ -1185,8 +1204,6 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         if (!ok) {
                             if (lane == 0) fail(c, a, 4u, 0x8000u + i);
                         } else {
-                            // acquire: the cache writes of the CTAs whose sums were read
-                            asm volatile("fence.acq_rel.gpu;" ::: "memory");
                             uint64_t tot = 0ull, pre = 0ull;
 #pragma unroll
                             for (int u = 0; u < kPer; ++u) {
@@ -1202,51 +1219,43 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         }
                     }
                 }
-                stop = __syncthreads_or(stop_vote(c, a));
+                stop = __syncthreads_or(stop_vote(c));
                 if (stop) break;
-                for (int b = 0; b < R && b < kChainRows; ++b) {
-                    if (!c.sampling[b]) continue;
+                // the CTA whose prefix range holds the target: its warp whose
+                // range holds it, then that warp's thread, scans its own ids
+#pragma unroll
+                for (int b = 0; b < kChainRows; ++b) {
+                    if (b >= R || !c.sampling[b]) continue;
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     const float M = key_from_ordered(o);
                     if (o == 0xffffffffu || isinf(M)) continue;
                     const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
-                    const uint64_t H = dm_cdf_hash(c.hri[i][b]);
-                    const uint64_t target = __umul64hi(H, S);
-                    if (P <= target && target < P + Sc) {
+                    const uint64_t target = __umul64hi(dm_cdf_hash(c.hri[i][b]), S);
+                    if (!(P <= target && target < P + Sc)) continue;
+                    const uint64_t t = target - P;
+                    uint64_t wpre = 0ull;
+                    for (int w = 0; w < warp; ++w) wpre += c.wsum[b][w];
+                    const uint64_t ws = c.wsum[b][warp];
+                    if (!(ws && wpre <= t && t < wpre + ws)) continue;
+                    uint64_t incl = mine[b];
+#pragma unroll
+                    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+                        if (lane >= o2) incl += y;
+                    }
+                    uint64_t run = wpre + incl - mine[b];
+                    if (mine[b] && run <= t && t < run + mine[b]) {
                         const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                        const int len = v_end - v_begin;
-                        const int chunk = (len + kThreads - 1) / kThreads;
-                        const int c0 = v_begin + tid * chunk;
-                        const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
-                        uint64_t mine = 0ull;
                         for (int v = c0; v < c1; ++v) {
-                            const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
-                            mine += dm_cdf_weight(__fsub_rn(x, M));
-                        }
-                        uint64_t incl = mine;
-    #pragma unroll
-                        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                            if (lane >= o2) incl += y;
-                        }
-                        if (lane == 31) c.scan[warp] = incl;
-                        __syncthreads();
-                        uint64_t wpre = 0ull;
-                        for (int w = 0; w < warp; ++w) wpre += c.scan[w];
-                        uint64_t run = P + wpre + incl - mine;
-                        if (run <= target && target < run + mine) {
-                            for (int v = c0; v < c1; ++v) {
-                                const float x = __fdiv_rn(((DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v])), c.T[b]);
-                                run += dm_cdf_weight(__fsub_rn(x, M));
-                                if (run > target) {
-                                    tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
-                                                       ((uint64_t)v << 32) | tag32);
-                                    break;
-                                }
+                            const float x = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
+                            run += dm_cdf_weight(__fsub_rn(__fdiv_rn(x, c.T[b]), M));
+                            if (run > t) {
+                                tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
+                                                   ((uint64_t)v << 32) | tag32);
+                                break;
                             }
                         }
                     }
-                    __syncthreads();
                 }
                 // everyone learns the tokens the owners found
                 if (warp < kChainRows && c.sampling[warp] && lane == 0) {
@@ -1257,10 +1266,10 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         const uint64_t *slot = a.tok_slots + (int64_t)i * kChainRows + b;
                         const uint64_t dl = tc::now_ns() + timeout;
                         uint64_t t = 0ull;
-                        for (;;) {
+                        for (uint32_t spin = 0;; ++spin) {
                             t = tc::ld_relaxed_u64(slot);
                             if ((uint32_t)t == tag32) break;
-                            if (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u) {
+                            if ((spin & 15u) == 15u && (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
                                 fail(c, a, 4u, 0x9000u + i);
                                 break;
                             }
@@ -1273,7 +1282,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                             fail(c, a, 6u, 0xA000u + i);
                     }
                 }
-                stop = __syncthreads_or(stop_vote(c, a));
+                stop = __syncthreads_or(stop_vote(c));
                 if (stop) break;
             }
 
@@ -1300,7 +1309,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             if (tid == 128 && i + 1 < N) clear_position(c, (i + 1) & 1);
             tc::fence_proxy_async_smem();
             tc::fence_before_sync();
-            stop = __syncthreads_or(stop_vote(c, a));
+            stop = __syncthreads_or(stop_vote(c));
             tc::fence_after_sync();
         }
     }

@@ -71,7 +71,7 @@ struct SampleArgs {
     uint32_t *status;          // [2]: sticky device status, where it happened
     uint32_t *call_counter;    // calls of the persistent tcgen05 chain so far
     uint64_t *tc_keys;         // [N][8][kTcReplicas][Gp] tagged key slots of the tcgen05 chain
-    uint64_t *tc_sums;         // [N][8][Gp] inverse-CDF sum slots of the tcgen05 chain
+    uint64_t *tc_sums;         // [N][8][kTcReplicas][Gp] inverse-CDF sum slots of the tcgen05 chain
     uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
     uint64_t *win_max;         // [2 call parities][N][8 rows] x kLineU64: red.max words

@@ -221,7 +221,7 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMalloc(&p->sums, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->ctrl, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMalloc(&p->tc_keys, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&p->tc_sums, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMalloc(&p->tc_sums, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sum_tags, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMalloc(&p->tok_slots, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->win_max, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
@@ -233,7 +233,7 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMemset(p->bwin, 0, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->bcnt, 0, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
@@ -492,7 +492,7 @@ markov_status markov_plan_status(markov_plan *p) {
     // counters, and forget every tagged exchange slot
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_keys, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
