@@ -196,9 +196,20 @@ __device__ __noinline__ uint32_t transform_two_bf16(uint32_t lp, const Transform
     return bf16x2_rn(y0, y1);
 }
 
-// Integer inverse-CDF weight floor(exp(x / T - M) 2^40) of cached logit x.
-__device__ __forceinline__ uint64_t cdf_weight_of(float x, float T, float M) {
-    return dm_cdf_weight(__fsub_rn(__fdiv_rn(x, T), M));
+// Integer inverse-CDF weight floor(exp(x / T - M) 2^40) of cached logit x
+// (kPow2: T a power of two, rT = 1 / T).
+template <bool kPow2>
+__device__ __forceinline__ uint64_t cdf_weight_of(float x, float T, float rT, float M) {
+    return dm_cdf_weight(__fsub_rn(dm_div_T<kPow2>(x, T, rT), M));
+}
+
+// The weight sum of 8 cached logits.
+template <bool kPow2>
+__device__ __forceinline__ uint64_t cdf_weight8(const float (&x)[8], float T, float rT, float M) {
+    uint64_t s = 0ull;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += cdf_weight_of<kPow2>(x[e], T, rT, M);
+    return s;
 }
 
 // Eight consecutive cached logits (row b, position i, ids v .. v + 7, v a
@@ -556,6 +567,8 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
     if (idx < 0 || !samples(T)) return;
     if (win == 0ull) return;                  // the logits kernel decided the row
     const float M = key_from_ordered(packed_ordered(win));
+    const bool p2 = dm_pow2_temperature(T);
+    const float rT = p2 ? __frcp_rn(T) : 0.0f;
     const uint64_t pol = tc::policy_evict_first();
     uint64_t *units = a.sums + (int64_t)b * nu;
 
@@ -572,10 +585,7 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
 #pragma unroll
     for (int r = 0; r < kCdfRounds; ++r) {
         uint64_t part = 0ull;
-        if (ok[r]) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) part += cdf_weight_of(x[r][e], T, M);
-        }
+        if (ok[r]) part = p2 ? cdf_weight8<true>(x[r], T, rT, M) : cdf_weight8<false>(x[r], T, rT, M);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
         const int u = (c * kCdfRounds + r) * kBW + warp;
@@ -635,8 +645,7 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
         uint64_t wl = 0ull;
         if (v < a.V) {
             cache8_last(a, b, i, v, pol, y);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) wl += cdf_weight_of(y[e], T, M);
+            wl = p2 ? cdf_weight8<true>(y, T, rT, M) : cdf_weight8<false>(y, T, rT, M);
         }
         uint64_t inc = wl;
 #pragma unroll
@@ -649,7 +658,7 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
         if (wl && run <= tgt && tgt < run + wl) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                run += cdf_weight_of(y[e], T, M);
+                run += p2 ? cdf_weight_of<true>(y[e], T, rT, M) : cdf_weight_of<false>(y[e], T, rT, M);
                 if (hit < 0 && run > tgt) hit = e;
             }
         }

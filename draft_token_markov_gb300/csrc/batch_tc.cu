@@ -177,19 +177,22 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
     tc::fence_after_sync();
     const uint32_t tmem = c.tmem_base;
     int produced = 0;
-    // the head stays in L2 across positions; base logits are read once
-    const uint64_t keep = tc::policy_evict_last();
     if (warp == 0 && lane == 0) {
         // the first stages' head chunks (the head is an input: never written)
         for (int s = 0; s < kBtStages; ++s) c.issued[s] = 0u;
         for (; produced < nch && produced < kBtStages; ++produced) {
             const uint32_t bar = tc::smem_u32(&c.full[produced]);
             tc::mbar_expect_tx(bar, kBtChunk);
-            tc::tma_load_2d_hint(st_sa + produced * kBtChunk, &tmap, (produced % cpt) * 64,
-                                 (t0 + produced / cpt) * 128, bar, keep);
+            tc::tma_load_2d(st_sa + produced * kBtChunk, &tmap, (produced % cpt) * 64,
+                            (t0 + produced / cpt) * 128, bar);
             ++c.issued[produced];
         }
     }
+    // epilogue threads: row (32 (q % 2) + lane) of the group, tile X (q < 2)
+    // or Y (q >= 2) of each pair, ids 32 cg .. 32 cg + 31 of the tile
+    const int q = warp & 3, cg = (warp - 2) >> 2;
+    const int rr = 32 * (q & 1) + lane, b = row0 + rr;
+    const int hy = q >> 1;
     bt_pdl_wait();
 
     if (tid < kBtGroup) {
@@ -198,11 +201,6 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
         c.T[tid] = b < a.rows ? a.temperature[b] : 0.0f;
         c.live[tid] = b < a.rows && a.row_state_idx[b] >= 0;
     }
-    // epilogue threads: row (32 (q % 2) + lane) of the group, tile X (q < 2)
-    // or Y (q >= 2) of each pair, ids 32 cg .. 32 cg + 31 of the tile
-    const int q = warp & 3, cg = (warp - 2) >> 2;
-    const int rr = 32 * (q & 1) + lane, b = row0 + rr;
-    const int hy = q >> 1;
     if (warp >= 2) {
         // ---- the A operands: this thread's lane holds row rr of [E; 0]
         // (q < 2) or of [0; E] (q >= 2), columns 32 cg .. 32 cg + 31 (K
@@ -266,8 +264,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 }
                 const uint32_t bar = tc::smem_u32(&c.full[s]);
                 tc::mbar_expect_tx(bar, kBtChunk);
-                tc::tma_load_2d_hint(st_sa + s * kBtChunk, &tmap, (j % cpt) * 64, (t0 + j / cpt) * 128, bar,
-                                     keep);
+                tc::tma_load_2d(st_sa + s * kBtChunk, &tmap, (j % cpt) * 64, (t0 + j / cpt) * 128, bar);
                 ++c.issued[s];
             }
         }
@@ -340,7 +337,6 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
         const bool st32 = ((reinterpret_cast<uintptr_t>(cache_f32 ? (void *)a.cache_f : (void *)a.cache) & 31u) == 0u) &&
                           ((a.cache_s0 * (cache_f32 ? 4 : 2)) % 32) == 0 && ((a.cache_s1 * (cache_f32 ? 4 : 2)) % 32) == 0;
         constexpr int kNB = kBaseF32 ? 32 : 16;      // base words of 32 ids
-        const uint64_t once = tc::policy_evict_first();
         // the base logits of this thread's 32 ids of pair p (zeros outside)
         auto load_base = [&](int p, uint32_t (&w)[kNB]) {
             const int k = 2 * p + hy;
@@ -352,7 +348,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 for (int u = 0; u < 32; u += 4) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
                     if (on && vec && v0 + u < V) {
-                        x = tc::ld_nc_v4_hint(src + u, once);
+                        x = __ldg(reinterpret_cast<const uint4 *>(src + u));
                     } else if (on && !vec) {
                         x.x = v0 + u < V ? __float_as_uint(__ldg(src + u)) : 0u;
                         x.y = v0 + u + 1 < V ? __float_as_uint(__ldg(src + u + 1)) : 0u;
@@ -370,7 +366,7 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
                 for (int u = 0; u < 16; u += 4) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
                     if (on && vec && v0 + 2 * u < V) {
-                        x = tc::ld_nc_v4_hint(src + 2 * u, once);
+                        x = __ldg(reinterpret_cast<const uint4 *>(src + 2 * u));
                     } else if (on && !vec) {
                         uint32_t y[4];
 #pragma unroll

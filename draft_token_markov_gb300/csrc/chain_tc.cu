@@ -1137,9 +1137,18 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                         if (use[r]) {
                             const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
                             const float T = c.T[b];
+                            if (dm_pow2_temperature(T)) {
+                                const float rT = __frcp_rn(T);
 #pragma unroll
-                            for (int k = 0; k < kPT; ++k)
-                                if (c0 + k < c1) part += dm_cdf_weight(__fsub_rn(__fdiv_rn(xs[r][k], T), M));
+                                for (int k = 0; k < kPT; ++k)
+                                    if (c0 + k < c1)
+                                        part += dm_cdf_weight(__fsub_rn(dm_div_T<true>(xs[r][k], T, rT), M));
+                            } else {
+#pragma unroll
+                                for (int k = 0; k < kPT; ++k)
+                                    if (c0 + k < c1)
+                                        part += dm_cdf_weight(__fsub_rn(dm_div_T<false>(xs[r][k], T, 0.0f), M));
+                            }
                         }
                         mine[b] = part;
                         if (__any_sync(0xffffffffu, use[r])) {

@@ -86,9 +86,16 @@ __device__ __forceinline__ float dm_exp(float x) {
 // lies in [-41, 0], so p 2^k and p 2^(k + 40) are normal and the two
 // power-of-two products exact; below -28 the exp is under e^-28 (1 + 2^-20)
 // < 2^-40, whose scaled floor is 0 (as it is for d = -inf).  The select
-// keeps lanes of a warp from diverging.
+// keeps lanes of a warp from diverging.  The integer steps stay on the
+// FMA and integer pipes: rint of the rounded product by adding and
+// subtracting 1.5 2^23 (for |y| < 2^22 that sum's unit in the last place is
+// 1, so it rounds y to the nearest integer, ties to even, and its low bits
+// are that integer), and the floor of w = m 2^(e - 23) (m the 24-bit
+// significand) by shifting m.
 __device__ __forceinline__ uint64_t dm_cdf_weight(float d) {
-    const float kf = rintf(__fmul_rn(d, 0x1.715476p+0f));
+    const float y = __fmul_rn(d, 0x1.715476p+0f);
+    const float t = __fadd_rn(y, 0x1.8p23f);
+    const float kf = __fsub_rn(t, 0x1.8p23f);
     float r = __fmaf_rn(-kf, 0x1.62e300p-1f, d);
     r = __fmaf_rn(-kf, 0x1.2fefa2p-17f, r);
     float p = 0x1.a01a02p-13f;
@@ -99,10 +106,25 @@ __device__ __forceinline__ uint64_t dm_cdf_weight(float d) {
     p = __fmaf_rn(p, r, 0x1.000000p-1f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    const int k = __float2int_rn(kf);
-    const float w = __fmul_rn(p, __uint_as_float((uint32_t)(k + 167) << 23));
-    const uint64_t q = (uint64_t)__float2ull_rz(w);
+    const int k = (int)(__float_as_uint(t) - 0x4B400000u);
+    const uint32_t wb = __float_as_uint(__fmul_rn(p, __uint_as_float((uint32_t)(k + 167) << 23)));
+    // w >= 1/2 here: its biased exponent e >= 126, w = m 2^(e - 150)
+    const int sh = (int)(wb >> 23) - 150;
+    const uint32_t m = (wb & 0x007fffffu) | 0x00800000u;
+    const uint64_t q = sh >= 0 ? (uint64_t)m << (sh & 63) : (uint64_t)(m >> (-sh < 31 ? -sh : 31));
     return d >= -28.0f ? q : 0ull;
+}
+
+// fp32(x / T).  For T a positive normal power of two, 1 / T is exact and
+// the product x (1 / T) is the same real number as x / T, rounded once: the
+// multiply is the division's exact rewrite (kPow2 selects it; rT = 1 / T).
+__device__ __forceinline__ bool dm_pow2_temperature(float T) {
+    const uint32_t b = __float_as_uint(T);
+    return (b & 0x007fffffu) == 0u && (b >> 23) - 1u < 0xfeu;
+}
+template <bool kPow2>
+__device__ __forceinline__ float dm_div_T(float x, float T, float rT) {
+    return kPow2 ? __fmul_rn(x, rT) : __fdiv_rn(x, T);
 }
 
 __device__ __forceinline__ float dm_tanh(float u) {

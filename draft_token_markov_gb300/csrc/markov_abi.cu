@@ -517,7 +517,8 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
 }
 
 markov_status markov_device_math(int32_t fn, const float *x, float *y, int64_t n, void *stream) {
-    if (fn < 0 || fn > 11 || n < 0 || (n > 0 && (!x || !y)) || (fn == 9 && n % 3 != 0))
+    if (fn < 0 || fn > 12 || n < 0 || (n > 0 && (!x || !y)) || (fn == 9 && n % 3 != 0) ||
+        (fn == 12 && n % 2 != 0))
         return MARKOV_EINVAL;
     if (launch_device_math(fn, x, y, n, (cudaStream_t)stream) != cudaSuccess) return MARKOV_ECUDA;
     return MARKOV_OK;

@@ -69,6 +69,18 @@ __global__ void device_math_kernel(int fn, const float *__restrict__ x, float *_
         }
         return;
     }
+    if (fn == 12) {
+        // pairs (x, T): fp32(x / T) as the inverse-CDF kernels take it, and
+        // whether T took the power-of-two product
+        for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; 2 * t + 1 < n;
+             t += (int64_t)gridDim.x * blockDim.x) {
+            const float v = x[2 * t], T = x[2 * t + 1];
+            const bool p2 = dm_pow2_temperature(T);
+            y[2 * t] = p2 ? dm_div_T<true>(v, T, __frcp_rn(T)) : dm_div_T<false>(v, T, 0.0f);
+            y[2 * t + 1] = p2 ? 1.0f : 0.0f;
+        }
+        return;
+    }
     for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         float v = x[j];

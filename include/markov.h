@@ -268,8 +268,10 @@ markov_status markov_gumbel_noise(const int64_t *seeds, const float *temperature
  * lower bound, its upper bound and the exact key fp32(l / T) + gumbel(u) as
  * the chain computes them.  fn 10 / 11: the low / high 32 bits (read as
  * uint32) of the inverse-CDF integer weight floor(exp(d) 2^40) of
- * d = fp32(l / T) - M <= 0, as every inverse-CDF kernel computes it.  These
- * are the functions the kernels use;
+ * d = fp32(l / T) - M <= 0, as every inverse-CDF kernel computes it.  fn 12
+ * on pairs (l, T), n even: fp32(l / T) as the inverse-CDF kernels compute
+ * it (a product by 1 / T when T is a power of two) and 1 where that product
+ * was taken, else 0.  These are the functions the kernels use;
  * exposed so they can be compared bit for bit with an independent
  * implementation, or checked against it as bounds.  EINVAL for an unknown
  * fn. */

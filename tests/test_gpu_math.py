@@ -163,3 +163,25 @@ def test_cdf_weight_matches_the_oracle(gpu_lib):
     got, want = _weights(gpu_lib, d), _oracle_weights(d)
     bad = np.nonzero(got != want)[0]
     assert bad.size == 0, (d[bad[:5]], got[bad[:5]], want[bad[:5]])
+
+
+def test_temperature_division_is_ieee(gpu_lib):
+    # fp32(l / T) for every finite BF16 logit, powers of two from 2^-126 to
+    # 2^127 (the product path) and other temperatures (the division path),
+    # against numpy's IEEE float32 division
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    x = (bits << 16).view(np.float32)
+    x = x[np.isfinite(x)]
+    p2 = [np.float32(2.0) ** np.float32(k) for k in range(-126, 128, 7)] + [np.float32(0.5), np.float32(1.0)]
+    other = [np.float32(v) for v in (0.7, 0.8, 1.2, 3.0, 1e-30)]
+    pairs = []
+    for T in p2 + other:
+        pairs.append(np.stack([x, np.full_like(x, T)], axis=1))
+    xt = np.concatenate(pairs).astype(np.float32).reshape(-1)
+    y = _dev(gpu_lib, 12, xt).reshape(-1, 2)
+    l, T = xt.reshape(-1, 2)[:, 0], xt.reshape(-1, 2)[:, 1]
+    with np.errstate(all="ignore"):
+        want = (l / T).astype(np.float32)
+    _same(y[:, 0], want)
+    is_p2 = np.isin(T, np.float32(p2))
+    assert np.array_equal(y[:, 1] == 1.0, is_p2)
