@@ -272,12 +272,26 @@ def run_gpu(args):
     inp = W.make_call(w, base_f32=base_f32)
     head, embed = head.to(dev), embed.to(dev)
     d = {k: v.to(dev) for k, v in inp.items()}
-    plan = api.Plan(w.vocab, w.rank, w.steps, w.rows, device=local)
-    plan.set_path({"auto": 0, "chain": 1, "batch": 2, "simple": 3}[args.path])
     R, N, V = w.rows, w.steps, w.vocab
-    toks = torch.full((R, N), -1, dtype=torch.int64, device=dev)
-    cache = torch.empty((R, N, V), dtype=torch.float32 if cache_f32 else torch.bfloat16,
-                        device=dev)
+    S = args.shards
+    if S:
+        # the vocabulary-sharded chain, its S ranks emulated on this GPU: each
+        # rank's head rows in an allocation of their own, per-rank outputs
+        if w.mode != W.GUMBEL or base_f32 or cache_f32:
+            raise SystemExit("--shards takes a Gumbel workload with BF16 base and cache")
+        plan = api.ShardPlan(w.vocab, w.rank, w.steps, w.rows, S, device=local)
+        heads = [head[k * V // S:(k + 1) * V // S].clone() for k in range(S)]
+        toks_l = [torch.full((R, N), -1, dtype=torch.int64, device=dev) for _ in range(S)]
+        caches_l = [torch.empty((R, N, V), dtype=torch.bfloat16, device=dev) for _ in range(S)]
+        toks = toks_l[0]
+        status = api.markov_shard_plan_status
+    else:
+        plan = api.Plan(w.vocab, w.rank, w.steps, w.rows, device=local)
+        plan.set_path({"auto": 0, "chain": 1, "batch": 2, "simple": 3}[args.path])
+        toks = torch.full((R, N), -1, dtype=torch.int64, device=dev)
+        cache = torch.empty((R, N, V), dtype=torch.float32 if cache_f32 else torch.bfloat16,
+                            device=dev)
+        status = api.markov_plan_status
     live = int((inp["row_state_idx"] >= 0).sum())
     tokens_per_step = live * N
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -310,9 +324,14 @@ def run_gpu(args):
             anchor, seeds = calls["anchor"][k], calls["seeds"][k]
         if evs:
             evs[0].record(stream)
-        api.markov_chain_sample(plan, d["base"], head, embed, anchor, d["temperature"],
-                                seeds, d["row_state_idx"], w.mode, w.mult, w.cap, toks,
-                                cache, stream)
+        if S:
+            api.markov_chain_sample_sharded(plan, d["base"], heads, embed, anchor,
+                                            d["temperature"], seeds, d["row_state_idx"], w.mult,
+                                            w.cap, toks_l, caches_l, stream)
+        else:
+            api.markov_chain_sample(plan, d["base"], head, embed, anchor, d["temperature"],
+                                    seeds, d["row_state_idx"], w.mode, w.mult, w.cap, toks,
+                                    cache, stream)
         if evs:
             evs[1].record(stream)
 
@@ -320,11 +339,15 @@ def run_gpu(args):
         flush_l2(1)
         step()
     torch.cuda.synchronize()
-    st = api.markov_plan_status(plan)
+    st = status(plan)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
-    launches_per_step = plan.query(api.Q_LAST_LAUNCHES)
-    path = {1: "tcgen05 chain", 2: "batch", 3: "simple chain"}.get(plan.query(api.Q_LAST_PATH), "?")
+    if S:
+        launches_per_step = S + 1          # each rank's noise, then the chain
+        path = f"vocab-sharded chain ({S} ranks emulated on one GPU)"
+    else:
+        launches_per_step = plan.query(api.Q_LAST_LAUNCHES)
+        path = {1: "tcgen05 chain", 2: "batch", 3: "simple chain"}.get(plan.query(api.Q_LAST_PATH), "?")
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
@@ -349,7 +372,7 @@ def run_gpu(args):
         clocks.mark_end()
     if world > 1:
         dist.barrier()
-    st = api.markov_plan_status(plan)
+    st = status(plan)
     if st != 0:
         raise RuntimeError(f"device status {st} in the timed region")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -388,7 +411,7 @@ def run_gpu(args):
     typed = base_f32 or cache_f32
     chain_avg_s = statistics.mean(chain_ms) / 1000.0
     achieved = alg_bytes / chain_avg_s / 1e9
-    traffic = None if typed else _traffic()
+    traffic = None if (typed or S) else _traffic()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores = cpu_oracle_sample(args.cpu_seconds, name)
@@ -410,7 +433,7 @@ def run_gpu(args):
                    "mode": "gumbel" if w.mode == W.GUMBEL else "inverse cdf", "l2": "flushed before every step (256 MB write, then a 256 MB read of another buffer)",
                    "parallelism": f"replicas x{world}", "path": path,
                    "distinct_calls": args.calls or 1,
-                   "resident_head_bytes": plan.query(api.Q_RESIDENT_HEAD_BYTES)},
+                   "resident_head_bytes": 0 if S else plan.query(api.Q_RESIDENT_HEAD_BYTES)},
         "us_per_call": {"median": statistics.median(step_ms) * 1000.0,
                         "p99": sorted(step_ms)[min(len(step_ms) - 1,
                                                    int(0.99 * len(step_ms)))] * 1000.0,
@@ -419,7 +442,8 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "frac_of_nominal_8000_gbs": achieved / 8000.0,
-                     "kernel": {"tcgen05 chain": "chain_tc_kernel", "simple chain": "chain_kernel",
+                     "kernel": "sharded_chain_kernel" if S else
+                               {"tcgen05 chain": "chain_tc_kernel", "simple chain": "chain_kernel",
                                 "batch": "batch kernels"}.get(path, path),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_kind": peak_kind},
@@ -457,6 +481,9 @@ def main():
     ap.add_argument("--calls", type=int, default=0,
                     help="time this many distinct calls (fresh seeds and anchors per call, staged "
                          "on the device up front), one per timed step; sets --steps")
+    ap.add_argument("--shards", type=int, default=0, choices=[0, 1, 2, 4, 8],
+                    help="run the vocabulary-sharded chain with this many ranks emulated on "
+                         "the one GPU (Gumbel workloads)")
     ap.add_argument("--rows", type=int, default=0,
                     help="run the workload with this many rows instead of its own")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOAD_NAMES,

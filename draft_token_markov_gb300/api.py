@@ -77,6 +77,12 @@ def _declare(L):
         "markov_chain_sample_typed": (i32, [P, P, i32, i64, i64, P, P, P, P, P, P, i32, i32, f32,
                                             f32, P, i64, P, i32, i64, i64, P]),
         "markov_plan_status": (i32, [P]),
+        "markov_shard_plan_create": (i32, [c.POINTER(_Desc), i32, c.POINTER(P)]),
+        "markov_shard_plan_destroy": (None, [P]),
+        "markov_shard_plan_ctas": (i32, [P]),
+        "markov_shard_plan_status": (i32, [P]),
+        "markov_chain_sample_sharded": (i32, [P, P, i64, i64, P, P, P, P, P, P, i32, f32, f32,
+                                              P, i64, P, i64, i64, P]),
         "markov_status_string": (c.c_char_p, [i32]),
         "markov_gumbel_noise": (i32, [P, P, P, i32, i32, i32, P, i64, P]),
         "markov_device_math": (i32, [i32, P, P, i64, P]),
@@ -151,6 +157,115 @@ class Plan:
     @property
     def chain_max_rows(self) -> int:
         return int(lib().markov_chain_max_rows(self._h))
+
+
+class ShardPlan:
+    """A vocabulary-sharded plan: `world` ranks, each with scratch of its own
+    (the sharded chain's ranks, emulated on one GPU)."""
+
+    def __init__(self, vocab: int, rank: int, num_steps: int, max_rows: int, world: int,
+                 device: int | None = None, timeout_ms: int = 0):
+        if device is None:
+            device = torch.cuda.current_device()
+        d = _Desc(vocab, rank, num_steps, max_rows, device, timeout_ms)
+        h = ctypes.c_void_p()
+        _check(lib().markov_shard_plan_create(ctypes.byref(d), int(world), ctypes.byref(h)),
+               "markov_shard_plan_create")
+        self._h = h
+        self.vocab, self.rank, self.num_steps, self.max_rows = vocab, rank, num_steps, max_rows
+        self.world, self.device = world, device
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def ctas(self) -> int:
+        return int(lib().markov_shard_plan_ctas(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().markov_shard_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def shard_range(rank: int, world: int, vocab: int) -> tuple[int, int]:
+    """(first id, width) of `rank`'s vocabulary shard: rows [k V / world,
+    (k + 1) V / world) of the head (sharded_markov page, module docstring)."""
+    if world < 1 or not 0 <= rank < world or vocab % world:
+        raise ValueError("vocab must split evenly over the ranks")
+    w = vocab // world
+    return rank * w, w
+
+
+def agree_on_shards(group, vocab: int, offset: int, width: int) -> bool:
+    """Whether, on every rank of the torch.distributed `group`, (offset,
+    width) is that rank's vocabulary shard (shard_range); a collective that
+    every rank must enter (sharded_markov page, accepts_shard: a rank that
+    skipped it would leave its peers waiting)."""
+    import torch.distributed as dist
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    mine = torch.tensor([offset, width], dtype=torch.int64)
+    got = [torch.zeros(2, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(got, mine, group=group)
+    if vocab % world:
+        return False
+    return all(tuple(int(x) for x in got[k]) == shard_range(k, world, vocab) for k in range(world))
+
+
+def markov_chain_sample_sharded(plan: ShardPlan, base_logits, head_shards, embed, anchor_tokens,
+                                temperature, seeds, row_state_idx, output_multiplier: float = 1.0,
+                                soft_cap: float | None = None, draft_tokens=None,
+                                logit_caches=None, stream=None):
+    """Sample on every rank of `plan`; returns (draft_tokens, logit_caches),
+    one [rows, N] and one [rows, N, V] tensor per rank (allocated when not
+    given).  head_shards[k] is rank k's [V / world, r] BF16 head rows."""
+    rows, N, V = base_logits.shape
+    W = plan.world
+    dev = base_logits.device
+    if len(head_shards) != W:
+        raise ValueError(f"{W} head shards expected")
+    if draft_tokens is None:
+        draft_tokens = [torch.empty((rows, N), dtype=torch.int64, device=dev) for _ in range(W)]
+    if logit_caches is None:
+        logit_caches = [torch.empty((rows, N, V), dtype=torch.bfloat16, device=dev)
+                        for _ in range(W)]
+    if base_logits.stride(2) != 1:
+        raise ValueError("the last dimension of base_logits must be contiguous")
+    for k in range(W):
+        if not head_shards[k].is_contiguous():
+            raise ValueError("head shards must be contiguous")
+        if draft_tokens[k].stride(1) != 1 or logit_caches[k].stride(2) != 1:
+            raise ValueError("the last dimension of the outputs must be contiguous")
+        if (draft_tokens[k].stride(0) != draft_tokens[0].stride(0) or
+                logit_caches[k].stride()[:2] != logit_caches[0].stride()[:2]):
+            raise ValueError("every rank's outputs must have the same strides")
+    P = ctypes.c_void_p
+    heads = (P * W)(*[_dev(h, torch.bfloat16, "head_shards") for h in head_shards])
+    toks = (P * W)(*[_dev(t, torch.int64, "draft_tokens") for t in draft_tokens])
+    caches = (P * W)(*[_dev(c, torch.bfloat16, "logit_caches") for c in logit_caches])
+    cap = -1.0 if soft_cap is None else float(soft_cap)
+    code = lib().markov_chain_sample_sharded(
+        plan.handle, _dev(base_logits, torch.bfloat16, "base_logits"), base_logits.stride(0),
+        base_logits.stride(1), heads, _dev(embed, torch.bfloat16, "embed"),
+        _dev(anchor_tokens, torch.int32, "anchor_tokens"),
+        _dev(temperature, torch.float32, "temperature"), _dev(seeds, torch.int64, "seeds"),
+        _dev(row_state_idx, torch.int64, "row_state_idx"), rows, float(output_multiplier), cap,
+        toks, draft_tokens[0].stride(0), caches, logit_caches[0].stride(0),
+        logit_caches[0].stride(1), _stream(stream))
+    _check(code, "markov_chain_sample_sharded")
+    return draft_tokens, logit_caches
+
+
+def markov_shard_plan_status(plan: ShardPlan) -> int:
+    """The sticky device status of the sharded plan's calls (0 = ok); clears it."""
+    return int(lib().markov_shard_plan_status(plan.handle))
 
 
 def markov_noise_fork(plan: Plan, seeds, temperature, row_state_idx, stream=None):

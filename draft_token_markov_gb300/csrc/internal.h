@@ -85,9 +85,10 @@ struct SampleArgs {
 };
 
 // Kernel launchers (return the CUDA error of the launch).
+// v_offset: the global vocabulary id of column 0 of `out` (a shard's noise)
 cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
                          const int64_t *row_state_idx, int rows, int N, int V, float *out,
-                         int64_t out_s0, int mode_gumbel_only, cudaStream_t stream);
+                         int64_t out_s0, int mode_gumbel_only, cudaStream_t stream, int v_offset = 0);
 cudaError_t launch_device_math(int fn, const float *x, float *y, int64_t n, cudaStream_t s);
 cudaError_t chain_occupancy(int *blocks_per_sm);
 cudaError_t launch_chain(const SampleArgs &a, cudaStream_t stream);

@@ -6,7 +6,8 @@
 // drawn on a side stream before the chain runs (sharded_markov page,
 // fork_noise and _shard_noise_kernel).  The kernel is ALU bound: one 64-bit
 // hash and two logarithms per element; each thread makes 4 consecutive ids
-// and stores them as one 16-byte vector.
+// and stores them as one 16-byte vector.  A vocabulary shard's noise is the
+// same hash of the global id (v_offset + the shard's column).
 #include "common.cuh"
 #include "gumbel_bounds.cuh"
 
@@ -18,7 +19,7 @@ constexpr int kNoisePerThread = 4;
 __global__ void __launch_bounds__(kNoiseThreads)
 noise_kernel(const int64_t *__restrict__ seeds, const float *__restrict__ temperature,
              const int64_t *__restrict__ row_state_idx, int N, int V, float *__restrict__ out,
-             int64_t out_s0) {
+             int64_t out_s0, int v_offset) {
     const int sample = blockIdx.y;          // b * N + i
     const int b = sample / N;
     const int i = sample - b * N;
@@ -30,7 +31,7 @@ noise_kernel(const int64_t *__restrict__ seeds, const float *__restrict__ temper
          v0 += stride) {
         float g[kNoisePerThread];
 #pragma unroll
-        for (int j = 0; j < kNoisePerThread; ++j) g[j] = dm_gumbel(hri, (uint32_t)(v0 + j));
+        for (int j = 0; j < kNoisePerThread; ++j) g[j] = dm_gumbel(hri, (uint32_t)(v_offset + v0 + j));
         if (v0 + kNoisePerThread <= V && ((reinterpret_cast<uintptr_t>(dst + v0) & 15u) == 0u)) {
             *reinterpret_cast<float4 *>(dst + v0) = make_float4(g[0], g[1], g[2], g[3]);
         } else {
@@ -41,13 +42,13 @@ noise_kernel(const int64_t *__restrict__ seeds, const float *__restrict__ temper
 
 cudaError_t launch_noise(const int64_t *seeds, const float *temperature,
                          const int64_t *row_state_idx, int rows, int N, int V, float *out,
-                         int64_t out_s0, int /*mode_gumbel_only*/, cudaStream_t stream) {
+                         int64_t out_s0, int /*mode_gumbel_only*/, cudaStream_t stream, int v_offset) {
     int per_block = kNoiseThreads * kNoisePerThread;
     int bx = (V + per_block - 1) / per_block;
     if (bx > 65535) bx = 65535;
     dim3 grid(bx, rows * N);
     noise_kernel<<<grid, kNoiseThreads, 0, stream>>>(seeds, temperature, row_state_idx, N, V,
-                                                      out, out_s0);
+                                                      out, out_s0, v_offset);
     return cudaGetLastError();
 }
 

@@ -313,6 +313,74 @@ int64_t markov_plan_query(const markov_plan *plan, int32_t key);
 markov_status markov_plan_inject_status(markov_plan *plan, markov_status code, uint32_t where);
 markov_status markov_selftest_wait(int32_t which, int32_t timeout_us, void *stream);
 
+/* ------------------------------------------------------------------------
+ * The vocabulary-sharded chain (sharded_markov page, module docstring and
+ * "Per call" diagram), its ranks emulated on one GPU.
+ *
+ * Rank k of `world` owns rows [k V / world, (k + 1) V / world) of the head.
+ * Per draft position every rank computes its shard's logits, writes them
+ * into its own cache and into every peer's staging buffer, takes its shard's
+ * best key (fp32(l / T) + gumbel, l at T = 0; lowest id among equal keys, a
+ * NaN above all) and sends one 64-bit key per (rank, row, position) to every
+ * rank's mailbox; the best key of the world is the token on every rank.
+ * After the last position each rank copies its peers' columns from its
+ * staging buffer into its own cache.  Gumbel-max sampling only, as on the
+ * page.  Here the ranks are groups of CTAs of one cooperative launch on the
+ * plan's device, each with its own allocations (noise shard, staging buffer,
+ * mailbox, CTA key slots); the results equal markov_chain_sample's on the
+ * same inputs (the same bias tiles as MARKOV_PATH_CHAIN_SIMPLE: every rank's
+ * tokens and full cache are bit-identical to that path's). */
+typedef struct markov_shard_plan markov_shard_plan;
+
+/* A sharded plan for `world` ranks (1, 2, 4 or 8): vocab % (16 world) == 0
+ * (16-id tiles per rank), rank in {64, 128, 256}, 1 <= num_steps <= 16,
+ * 1 <= max_rows <= 8 (the MMA columns), timeout_ms as for markov_plan_create.
+ * Allocates every rank's scratch separately.  EINVAL for a bad desc or world;
+ * ENOTRESIDENT if no CTA per rank fits. */
+markov_status markov_shard_plan_create(const markov_desc *desc, int32_t world,
+                                       markov_shard_plan **out);
+
+/* Synchronize and free the plan's scratch.  NULL is a no-op. */
+void markov_shard_plan_destroy(markov_shard_plan *plan);
+
+/* CTAs of one sharded launch (world x CTAs per rank); -1 for NULL. */
+int32_t markov_shard_plan_ctas(const markov_shard_plan *plan);
+
+/* Synchronize, return and clear the sticky device status of the plan's calls
+ * (as markov_plan_status); after an error it also clears the key slots and
+ * mailboxes.  A call made while a status is pending writes nothing. */
+markov_status markov_shard_plan_status(markov_shard_plan *plan);
+
+/* Sample `rows` request rows (1 <= rows <= max_rows) on every rank.
+ *   base_logits   device [rows, N, V] BF16, full vocabulary (each rank reads
+ *                 its columns), strides base_s0 >= N base_s1, base_s1 >= V,
+ *                 last stride 1;
+ *   head_shards   host array of `world` device pointers: rank k's head rows
+ *                 [V / world, r] BF16, contiguous, 16-byte aligned;
+ *   embed         device [V, r] BF16, contiguous, 16-byte aligned (every
+ *                 rank's copy of the embedding table);
+ *   anchor_tokens, temperature, seeds, row_state_idx: device [rows] as for
+ *                 markov_chain_sample (T = 0 argmax; idx < 0 padding);
+ *   draft_tokens  host array of `world` device pointers, rank k's [rows, N]
+ *                 int64 output, row stride tok_s0 >= N;
+ *   logit_caches  host array of `world` device pointers, rank k's
+ *                 [rows, N, V] BF16 output (full vocabulary), 16-byte
+ *                 aligned, cache_s0 >= N cache_s1, cache_s1 >= V, both
+ *                 multiples of 8.
+ * Padding rows are written on no rank.  Asynchronous on `stream`; argument
+ * errors return EINVAL with nothing launched; a bounded wait that gives up
+ * records MARKOV_ETIMEOUT for markov_shard_plan_status. */
+markov_status markov_chain_sample_sharded(markov_shard_plan *plan, const uint16_t *base_logits,
+                                          int64_t base_s0, int64_t base_s1,
+                                          const uint16_t *const *head_shards,
+                                          const uint16_t *embed, const int32_t *anchor_tokens,
+                                          const float *temperature, const int64_t *seeds,
+                                          const int64_t *row_state_idx, int32_t rows,
+                                          float output_multiplier, float soft_cap,
+                                          int64_t *const *draft_tokens, int64_t tok_s0,
+                                          uint16_t *const *logit_caches, int64_t cache_s0,
+                                          int64_t cache_s1, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

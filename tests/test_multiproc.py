@@ -72,3 +72,38 @@ def test_two_gloo_ranks_replicas():
         assert got[0] == got[1]
         if rank != 0:
             assert ref_s < 1.0
+
+
+def _shard_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from draft_token_markov_gb300 import api
+        V = 129280
+        off, width = api.shard_range(rank, world, V)
+        ok = api.agree_on_shards(None, V, off, width)
+        # a rank that holds another rank's shard: every rank learns it
+        bad = api.agree_on_shards(None, V, off if rank == 0 else off - 16, width)
+        q.put((rank, off, width, ok, bad))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_vocab_shards():
+    # the host side of the vocabulary-sharded chain on a future multi-GPU
+    # box: each rank's shard is rows [k V / world, (k + 1) V / world) of the
+    # head, and the ranks check together that each holds its own
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [(r[1], r[2]) for r in res] == [(0, 64640), (64640, 64640)]
+    assert all(r[3] for r in res) and not any(r[4] for r in res)
