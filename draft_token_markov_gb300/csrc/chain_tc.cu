@@ -83,7 +83,7 @@ struct Ctl {
     uint32_t lcta[2][kChainRows];
     uint64_t win[kChainRows];
     unsigned long long sum[kChainRows];
-    uint64_t wsum[kChainRows][kThreads / 32];   // inverse CDF: per-row, per-warp weight totals
+    uint64_t wsum[kChainRows][kEpiThreads / 32];   // inverse CDF: per-row, per-epilogue-warp weight totals
     uint32_t tmem_base;
     uint32_t tmem_ready;             // chunks copied into TMEM so far
     uint32_t abort;
@@ -1077,6 +1077,37 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                 }
             }
+            // the inverse-CDF weights need the maxima, but fp32(x / T) of the
+            // CTA's cached logits does not: the epilogue warps (thread
+            // et = tid - 128 takes the contiguous ids [c0, c1)) load and
+            // divide them for the first kGR sampling rows while the maxima
+            // are exchanged, and keep them in registers for the weight pass
+            // and the owner's scan
+            constexpr int kMaxIds = (kTmemChunks + kSmemChunks) / (RANK / 64) * 128;
+            constexpr int kPT = (kMaxIds + kEpiThreads - 1) / kEpiThreads;   // ids per thread
+            constexpr int kGR = RANK == 64 ? 2 : 4;
+            const int et = tid - 128;
+            const int chunk = (v_end - v_begin + kEpiThreads - 1) / kEpiThreads;
+            const int c0 = v_begin + et * chunk;
+            const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
+            float q0[kGR][kPT];
+            if (warp >= 4) {
+#pragma unroll
+                for (int r = 0; r < kGR; ++r) {
+                    const bool s_r = r < R && c.sampling[r];
+                    const float T = c.T[r];
+                    const bool p2 = dm_pow2_temperature(T);
+                    const float rT = p2 ? __frcp_rn(T) : 0.0f;
+                    const int64_t crow = r * a.cache_s0 + (int64_t)i * a.cache_s1;
+#pragma unroll
+                    for (int k = 0; k < kPT; ++k) {
+                        float x = 0.0f;
+                        if (s_r && c0 + k < c1)
+                            x = (DT & 2) ? a.cache_f[crow + c0 + k] : dm_bf16_f32(a.cache[crow + c0 + k]);
+                        q0[r][k] = p2 ? dm_div_T<true>(x, T, rT) : dm_div_T<false>(x, T, 0.0f);
+                    }
+                }
+            }
             stop = __syncthreads_or(stop_vote(c));
             if (stop) break;
 
@@ -1094,67 +1125,47 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             }
             if (cdf_any) {
                 const uint32_t tag32 = epoch;
-                // thread t takes the contiguous ids [c0, c1) of the CTA's range,
-                // so each warp's ids are contiguous too: its weight totals per
-                // row (c.wsum) locate the target warp, and a warp scan of the
-                // threads' own totals (mine) the target thread, with no block
-                // barrier and no second pass over the whole range
-                const int len = v_end - v_begin;
-                const int chunk = (len + kThreads - 1) / kThreads;
-                const int c0 = v_begin + tid * chunk;
-                const int c1 = c0 + chunk < v_end ? c0 + chunk : v_end;
-                constexpr int kMaxIds = (kTmemChunks + kSmemChunks) / (RANK / 64) * 128;
-                constexpr int kPT = (kMaxIds + kThreads - 1) / kThreads;   // ids per thread
-                constexpr int kGR = RANK == 64 ? 2 : 4;
+                // the epilogue threads' weights: per row a register total
+                // (mine) and per warp a shared-memory total (c.wsum), so the
+                // owning warp and thread are found with no block barrier and
+                // no second pass over the range
                 uint64_t mine[kChainRows];
 #pragma unroll
                 for (int b = 0; b < kChainRows; ++b) mine[b] = 0ull;
-                // kGR rows a time: every cached logit of the group is loaded
-                // before any weight, so the rows share one read latency
+                if (warp >= 4) {
+                    const int ew = warp - 4;
 #pragma unroll
-                for (int b0 = 0; b0 < kChainRows; b0 += kGR) {
-                    if (b0 >= R) break;
-                    float xs[kGR][kPT];
-                    bool use[kGR];
-#pragma unroll
-                    for (int r = 0; r < kGR; ++r) {
-                        const int b = b0 + r;
-                        const uint32_t o = b < R ? (uint32_t)(c.win[b] >> 32) : 0u;
-                        use[r] = b < R && c.sampling[b] && o != 0xffffffffu && !isinf(key_from_ordered(o));
-                        const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
-#pragma unroll
-                        for (int k = 0; k < kPT; ++k) {
-                            const int v = c0 + k;
-                            xs[r][k] = 0.0f;
-                            if (use[r] && v < c1)
-                                xs[r][k] = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < kGR; ++r) {
-                        const int b = b0 + r;
+                    for (int b = 0; b < kChainRows; ++b) {
+                        if (b >= R) break;
+                        const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                        const bool use = c.sampling[b] && o != 0xffffffffu && !isinf(key_from_ordered(o));
                         uint64_t part = 0ull;
-                        if (use[r]) {
-                            const float M = key_from_ordered((uint32_t)(c.win[b] >> 32));
-                            const float T = c.T[b];
-                            if (dm_pow2_temperature(T)) {
-                                const float rT = __frcp_rn(T);
+                        if (use) {
+                            const float M = key_from_ordered(o);
+                            if (b < kGR) {
 #pragma unroll
                                 for (int k = 0; k < kPT; ++k)
-                                    if (c0 + k < c1)
-                                        part += dm_cdf_weight(__fsub_rn(dm_div_T<true>(xs[r][k], T, rT), M));
+                                    if (c0 + k < c1) part += dm_cdf_weight(__fsub_rn(q0[b < kGR ? b : 0][k], M));
                             } else {
+                                // rows past the first kGR: load and divide now
+                                const float T = c.T[b];
+                                const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                                float xs[kPT];
 #pragma unroll
                                 for (int k = 0; k < kPT; ++k)
-                                    if (c0 + k < c1)
-                                        part += dm_cdf_weight(__fsub_rn(dm_div_T<false>(xs[r][k], T, 0.0f), M));
+                                    xs[k] = (c0 + k < c1) ? ((DT & 2) ? a.cache_f[crow + c0 + k]
+                                                                      : dm_bf16_f32(a.cache[crow + c0 + k]))
+                                                          : 0.0f;
+#pragma unroll
+                                for (int k = 0; k < kPT; ++k)
+                                    if (c0 + k < c1) part += dm_cdf_weight(__fsub_rn(__fdiv_rn(xs[k], T), M));
                             }
                         }
                         mine[b] = part;
-                        if (__any_sync(0xffffffffu, use[r])) {
+                        if (__any_sync(0xffffffffu, use)) {
 #pragma unroll
                             for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-                            if (lane == 0) c.wsum[b][warp] = part;
+                            if (lane == 0) c.wsum[b][ew] = part;
                         }
                     }
                 }
@@ -1171,7 +1182,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     uint64_t s = 0ull;
                     if (b < R && c.sampling[b]) {
 #pragma unroll
-                        for (int w = 0; w < kThreads / 32; ++w) s += c.wsum[b][w];
+                        for (int w = 0; w < kEpiThreads / 32; ++w) s += c.wsum[b][w];
                         uint64_t *sl = a.tc_sums + (((int64_t)i * kChainRows + b) * kTcReplicas + rep) * Gp + cta;
                         tc::st_relaxed_u64(sl, s | ((uint64_t)stag << 52));
                     }
@@ -1232,36 +1243,48 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 if (stop) break;
                 // the CTA whose prefix range holds the target: its warp whose
                 // range holds it, then that warp's thread, scans its own ids
+                // (the first kGR rows from the registers)
+                if (warp >= 4) {
+                    const int ew = warp - 4;
 #pragma unroll
-                for (int b = 0; b < kChainRows; ++b) {
-                    if (b >= R || !c.sampling[b]) continue;
-                    const uint32_t o = (uint32_t)(c.win[b] >> 32);
-                    const float M = key_from_ordered(o);
-                    if (o == 0xffffffffu || isinf(M)) continue;
-                    const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
-                    const uint64_t target = __umul64hi(dm_cdf_hash(c.hri[i][b]), S);
-                    if (!(P <= target && target < P + Sc)) continue;
-                    const uint64_t t = target - P;
-                    uint64_t wpre = 0ull;
-                    for (int w = 0; w < warp; ++w) wpre += c.wsum[b][w];
-                    const uint64_t ws = c.wsum[b][warp];
-                    if (!(ws && wpre <= t && t < wpre + ws)) continue;
-                    uint64_t incl = mine[b];
+                    for (int b = 0; b < kChainRows; ++b) {
+                        if (b >= R || !c.sampling[b]) continue;
+                        const uint32_t o = (uint32_t)(c.win[b] >> 32);
+                        const float M = key_from_ordered(o);
+                        if (o == 0xffffffffu || isinf(M)) continue;
+                        const uint64_t S = s_tot[b], P = s_pre[b], Sc = c.sum[b];
+                        const uint64_t target = __umul64hi(dm_cdf_hash(c.hri[i][b]), S);
+                        if (!(P <= target && target < P + Sc)) continue;
+                        const uint64_t t = target - P;
+                        uint64_t wpre = 0ull;
+                        for (int w = 0; w < ew; ++w) wpre += c.wsum[b][w];
+                        const uint64_t ws = c.wsum[b][ew];
+                        if (!(ws && wpre <= t && t < wpre + ws)) continue;
+                        uint64_t incl = mine[b];
 #pragma unroll
-                    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-                        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
-                        if (lane >= o2) incl += y;
-                    }
-                    uint64_t run = wpre + incl - mine[b];
-                    if (mine[b] && run <= t && t < run + mine[b]) {
-                        const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
-                        for (int v = c0; v < c1; ++v) {
-                            const float x = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
-                            run += dm_cdf_weight(__fsub_rn(__fdiv_rn(x, c.T[b]), M));
-                            if (run > t) {
-                                tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
-                                                   ((uint64_t)v << 32) | tag32);
-                                break;
+                        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                            const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+                            if (lane >= o2) incl += y;
+                        }
+                        uint64_t run = wpre + incl - mine[b];
+                        if (mine[b] && run <= t && t < run + mine[b]) {
+                            const int64_t crow = b * a.cache_s0 + (int64_t)i * a.cache_s1;
+                            for (int k = 0; k < kPT; ++k) {
+                                const int v = c0 + k;
+                                if (v >= c1) break;
+                                float x;
+                                if (b < kGR) {
+                                    x = q0[b < kGR ? b : 0][k];
+                                } else {
+                                    const float xc = (DT & 2) ? a.cache_f[crow + v] : dm_bf16_f32(a.cache[crow + v]);
+                                    x = __fdiv_rn(xc, c.T[b]);
+                                }
+                                run += dm_cdf_weight(__fsub_rn(x, M));
+                                if (run > t) {
+                                    tc::st_relaxed_u64(a.tok_slots + (int64_t)i * kChainRows + b,
+                                                       ((uint64_t)v << 32) | tag32);
+                                    break;
+                                }
                             }
                         }
                     }
