@@ -212,26 +212,6 @@ __device__ __forceinline__ uint64_t cdf_weight8(const float (&x)[8], float T, fl
     return s;
 }
 
-// Eight consecutive cached logits (row b, position i, ids v .. v + 7, v a
-// multiple of 8: the cache's 16-byte alignment holds) as fp32.
-__device__ __forceinline__ void cache8(const SampleArgs &a, int b, int i, int v, float (&x)[8]) {
-    const int64_t o = b * a.cache_s0 + (int64_t)i * a.cache_s1 + v;
-    if (a.cache_f) {
-        const float4 p = __ldg(reinterpret_cast<const float4 *>(a.cache_f + o));
-        const float4 q = __ldg(reinterpret_cast<const float4 *>(a.cache_f + o + 4));
-        x[0] = p.x; x[1] = p.y; x[2] = p.z; x[3] = p.w;
-        x[4] = q.x; x[5] = q.y; x[6] = q.z; x[7] = q.w;
-    } else {
-        const uint4 p = __ldg(reinterpret_cast<const uint4 *>(a.cache + o));
-        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[2 * k] = __uint_as_float(w[k] << 16);
-            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-        }
-    }
-}
-
 }  // namespace
 
 // The logits kernel of position i, for row groups of 16 MT rows.  MMA
@@ -564,8 +544,17 @@ batch_cdf_kernel(const SampleArgs a, int i, int nb2, int nu) {
     const int64_t idx = a.row_state_idx[b];
     const float T = a.temperature[b];
     const uint64_t win = __ldcg(ws);
-    if (idx < 0 || !samples(T)) return;
-    if (win == 0ull) return;                  // the logits kernel decided the row
+    // padding, or a row whose token the logits kernel's last block wrote
+    if (idx < 0 || win == 0ull) return;
+    if (!samples(T) || !needs_sums(win)) {
+        // decided by its maximum (greedy, a NaN, +inf, all -inf): the row's
+        // first block writes the token (the tcgen05 logits kernel leaves it)
+        if (c == 0 && tid == 0) {
+            a.tokens[b * a.tok_s0 + i] = direct_token(a, win, T);
+            *ws = 0ull;
+        }
+        return;
+    }
     const float M = key_from_ordered(packed_ordered(win));
     const bool p2 = dm_pow2_temperature(T);
     const float rT = p2 ? __frcp_rn(T) : 0.0f;

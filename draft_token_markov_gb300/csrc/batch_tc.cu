@@ -33,9 +33,10 @@
 //          key with its lowest id; at the start it writes its row's
 //          embedding slice into the A operands
 // After the tiles the block's best per row goes into the row's winner word
-// (u64 atomic maximum); the last block of the row group writes the token of
-// every row the winner decides (batch.cu: the inverse-CDF sum kernel
-// follows for the other rows).
+// (u64 atomic maximum).  In Gumbel mode the last block of the row group
+// writes every row's token; in inverse-CDF mode the inverse-CDF kernel that
+// follows (batch.cu) writes the tokens the maxima decide and samples the
+// others.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -606,6 +607,10 @@ batch_tc_logits_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap t
     }
     unsigned long long *wins = reinterpret_cast<unsigned long long *>(a.bwin + (size_t)i * kMaxRows);
     if (tid < kBtGroup && c.best[tid]) atomicMax(wins + row0 + tid, c.best[tid]);
+    // inverse CDF: the inverse-CDF kernel that follows (it waits for this
+    // grid) writes the tokens the maxima decide, so no block here waits for
+    // the others (no fence, no done counter)
+    if (a.mode == 1) return;
     uint32_t *cnt = a.bcnt + (size_t)i * kBatchCntPerStep + blockIdx.y;
     if (!bt_last_block(cnt, (uint32_t)G, &c.flag)) return;
 
