@@ -387,22 +387,34 @@ def run_gpu(args):
     warm_ms = [e[0].elapsed_time(e[1]) for e in warm_ev]
     total_ms = max_over_ranks(sum(step_ms))
 
-    # end to end: host (pinned) inputs copied in, tokens copied out, per step
+    # end to end: the step's inputs in pinned host memory and its tokens back
+    # in host memory, per step.  The chain paths take the host arguments
+    # directly (the kernels read the inputs and write the tokens over the
+    # host link); the per-position path, whose kernels re-read the base
+    # logits at every position, copies them in first and the tokens out.
     h_in = {k: v.pin_memory() for k, v in inp.items()}
     h_tok = torch.empty((R, N), dtype=torch.int64).pin_memory()
+    e2e_host = not S and path != "batch"
     e2e_ms = []
     for k in range(max(3, min(args.steps, 50)) + 3):
         flush_l2(k)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for key in d:
-            d[key].copy_(h_in[key], non_blocking=True)
-        step()
-        h_tok.copy_(toks, non_blocking=True)
+        if e2e_host:
+            api.markov_chain_sample(plan, h_in["base"], head, embed, h_in["anchor"],
+                                    h_in["temperature"], h_in["seeds"], h_in["row_state_idx"],
+                                    w.mode, w.mult, w.cap, h_tok, cache, stream)
+        else:
+            for key in d:
+                d[key].copy_(h_in[key], non_blocking=True)
+            step()
+            h_tok.copy_(toks, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
         if k >= 3:
             e2e_ms.append(e0.elapsed_time(e1))
+    if e2e_host and status(plan) != 0:
+        raise RuntimeError("device status after the end-to-end steps")
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = h_tok.numel() * h_tok.element_size()
 
@@ -450,7 +462,10 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": {"value": tokens_per_step / (e2e_step / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step},
+                "ms_per_step": e2e_step,
+                "inputs": ("pinned host memory, read by the kernels over the host link; tokens "
+                           "written to pinned host memory" if e2e_host else
+                           "copied from pinned host memory; tokens copied back")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
     }

@@ -115,6 +115,18 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _dev_or_pinned(t: torch.Tensor, dtype: torch.dtype, name: str) -> int:
+    """A CUDA tensor, or a pinned CPU tensor the kernels read (or write) over
+    the host link (the inputs and tokens of the sample calls)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if not t.is_pinned():
+            raise TypeError(f"{name} must be a CUDA tensor or a pinned CPU tensor")
+        if t.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+        return t.data_ptr()
+    return _dev(t, dtype, name)
+
+
 MARKOV_BF16 = 0
 MARKOV_F32 = 1
 
@@ -288,9 +300,10 @@ def markov_chain_sample(plan: Plan, base_logits, head, embed, anchor_tokens, tem
     tensors are allocated when not given (padding rows are then left
     uninitialised, as the library never writes them).  base_logits and
     logit_cache may each be bfloat16 or float32 (markov_chain_sample_typed;
-    the cache defaults to bfloat16)."""
+    the cache defaults to bfloat16).  The inputs and draft_tokens may be
+    pinned CPU tensors, which the kernels read and write directly."""
     rows, N, V = base_logits.shape
-    dev = base_logits.device
+    dev = head.device
     if draft_tokens is None:
         draft_tokens = torch.empty((rows, N), dtype=torch.int64, device=dev)
     if logit_cache is None:
@@ -306,13 +319,15 @@ def markov_chain_sample(plan: Plan, base_logits, head, embed, anchor_tokens, tem
             raise ValueError(f"{n} must be contiguous")
     cap = -1.0 if soft_cap is None else float(soft_cap)
     code = lib().markov_chain_sample_typed(
-        plan.handle, _dev(base_logits, base_logits.dtype, "base_logits"),
+        plan.handle, _dev_or_pinned(base_logits, base_logits.dtype, "base_logits"),
         dtypes[base_logits.dtype], base_logits.stride(0), base_logits.stride(1),
         _dev(head, torch.bfloat16, "head"),
-        _dev(embed, torch.bfloat16, "embed"), _dev(anchor_tokens, torch.int32, "anchor_tokens"),
-        _dev(temperature, torch.float32, "temperature"), _dev(seeds, torch.int64, "seeds"),
-        _dev(row_state_idx, torch.int64, "row_state_idx"), rows, int(mode),
-        float(output_multiplier), cap, _dev(draft_tokens, torch.int64, "draft_tokens"),
+        _dev(embed, torch.bfloat16, "embed"),
+        _dev_or_pinned(anchor_tokens, torch.int32, "anchor_tokens"),
+        _dev_or_pinned(temperature, torch.float32, "temperature"),
+        _dev_or_pinned(seeds, torch.int64, "seeds"),
+        _dev_or_pinned(row_state_idx, torch.int64, "row_state_idx"), rows, int(mode),
+        float(output_multiplier), cap, _dev_or_pinned(draft_tokens, torch.int64, "draft_tokens"),
         draft_tokens.stride(0), _dev(logit_cache, logit_cache.dtype, "logit_cache"),
         dtypes[logit_cache.dtype], logit_cache.stride(0), logit_cache.stride(1), _stream(stream))
     _check(code, "markov_chain_sample")

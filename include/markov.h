@@ -151,6 +151,15 @@ markov_status markov_noise_join(markov_plan *plan, void *stream);
  *   logit_cache   device, BF16 [rows, N, V], element (b, i, v) at
  *                 b * cache_s0 + i * cache_s1 + v; pointer and strides
  *                 16-byte aligned (sharded_markov page, sample: cache asserts).
+ * Host-resident inputs and tokens: base_logits, anchor_tokens, temperature,
+ * seeds, row_state_idx and draft_tokens may instead be page-locked host
+ * memory the device can address (cudaHostAlloc, cudaHostRegister, or a
+ * pinned torch CPU tensor); the kernels then read the inputs and write the
+ * tokens over the host link during the call, with no staging copy (on
+ * GB300 the NVLink-C2C link; the bytes are the same, the results bit for bit
+ * those of device-resident arguments).  head, embed and logit_cache must be
+ * device memory.  The host must not write the inputs or read the tokens
+ * before the call's stream work completes.
  * Rows up to markov_chain_max_rows take one persistent launch; Gumbel calls
  * of up to 24 rows one persistent launch per 8-row slice (the noise hash
  * takes each row's index in the call); larger calls take the per-position
@@ -181,8 +190,9 @@ markov_status markov_chain_sample(markov_plan *plan, const uint16_t *base_logits
  *   is added in fp32 before the BF16 rounding).  Keys and tokens follow from
  *   the cached values exactly as in markov_chain_sample.
  * BF16 / BF16 is markov_chain_sample.  Every path takes every dtype pair
- * (each kernel is compiled per base and cache dtype).  Other arguments and
- * errors as markov_chain_sample; EINVAL for an unknown dtype. */
+ * (each kernel is compiled per base and cache dtype).  Other arguments
+ * (host-resident inputs and tokens included) and errors as
+ * markov_chain_sample; EINVAL for an unknown dtype. */
 markov_status markov_chain_sample_typed(markov_plan *plan, const void *base_logits,
                                         markov_dtype base_dtype, int64_t base_s0,
                                         int64_t base_s1, const uint16_t *head,
