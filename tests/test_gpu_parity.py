@@ -46,6 +46,12 @@ BATCHES = [
     W.small(3008, 256, 20, 3, W.GUMBEL, seed=8, padding_rows=(3, 19)),
     W.small(1024, 128, 70, 2, W.INVCDF, seed=9, temperatures=(0.0, 0.8, 1.0)),
     W.small(512, 64, 256, 2, W.GUMBEL, seed=10),
+    # two 64-row groups of the tcgen05 logits kernel, CTAs with a full tile
+    # pair and a ragged last tile (16400 = 128 x 128 + 16), every temperature
+    W.small(16400, 256, 100, 3, W.INVCDF, seed=11, padding_rows=(5, 64, 99),
+            temperatures=(0.0, 0.5, 0.8, 1.0, 1.2), spikes=2),
+    W.small(8192, 128, 130, 2, W.GUMBEL, seed=12, padding_rows=(0, 127),
+            temperatures=(0.0, 0.7, 1.0)),
 ]
 
 
