@@ -154,33 +154,6 @@ __device__ __forceinline__ uint32_t unpack_id(uint64_t p) {
 // bound: with a loop over the runtime CTA count the loads went out one L2
 // round trip apart, and a round took microseconds).
 constexpr int kMaxGrid = 160;             // CTAs the exchanges take
-__device__ __forceinline__ bool poll_max(const uint64_t *slots, int G, uint32_t tag, uint64_t deadline,
-                         const SampleArgs &a, uint64_t &out) {
-    constexpr int kPer = kMaxGrid / 32;
-    const int lane = threadIdx.x & 31;
-    for (uint32_t spin = 0;; ++spin) {
-        uint64_t k[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u)
-            k[u] = lane + 32 * u < G ? tc::ld_relaxed_u64(slots + lane + 32 * u) : (uint64_t)tag;
-        bool fresh = true;
-        uint64_t m = 0ull;
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            if ((uint32_t)(k[u] & 0x3FFFu) != tag) fresh = false;
-            m = k[u] > m ? k[u] : m;
-        }
-        if (__all_sync(0xffffffffu, fresh)) {
-            out = tc::warp_max_u64(m);
-            return true;
-        }
-        if ((spin & 15u) == 15u) {
-            bool bad = tc::now_ns() > deadline || ld_acquire_u32(a.status) != 0u;
-            if (__any_sync(0xffffffffu, bad)) return false;
-        }
-    }
-}
-
 }  // namespace
 
 namespace {
@@ -1058,23 +1031,48 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                 asm volatile("bar.sync 2, %0;" ::"n"(kEpiThreads) : "memory");
             }
         } else {
-            if (warp < kChainRows) {
-                const int b = warp;
-                const uint64_t m = c.cbest[i & 1][b];
-                uint64_t *slots = a.tc_keys + ((int64_t)i * kChainRows + b) * kTcReplicas * Gp;
-                if (lane < kTcReplicas) tc::st_relaxed_u64(slots + lane * Gp + cta, (m & ~0x3FFFull) | tag);
-                slots += (cta % kTcReplicas) * Gp;
-                if (c.live[b]) {
-                    if (lane == 0 && m != 0ull) {
-                        const uint16_t *er = a.embed + (int64_t)unpack_id(m) * RANK;
-                        for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(reinterpret_cast<const uint8_t *>(er) + o);
+            // the rows' maxima as in Gumbel mode: red.max into one word per
+            // (position, row), a release-add on the position's counter, one
+            // polled word per CTA, then the 8 words
+            if (warp == 0) {
+                const size_t par = (size_t)(c.call & 1u);
+                uint64_t *wm = a.win_max + ((par * kMaxSteps + i) * kChainRows) * kLineU64;
+                uint32_t *wc = a.win_cnt + (par * kMaxSteps + i) * kLineU32;
+                if (lane < kChainRows && c.live[lane])
+                    tc::red_max_u64(wm + lane * kLineU64, (uint64_t)c.cbest[i & 1][lane]);
+                __syncwarp();
+                if (lane == 0) {
+                    bool ok = true;
+                    tc::red_release_add_u32(wc, 1u);
+                    const uint64_t dl = tc::now_ns() + timeout;
+                    for (uint32_t spin = 0;; ++spin) {
+                        if ((int32_t)(ld_acquire_u32(wc) - (uint32_t)G) >= 0) break;
+                        if ((spin & 15u) == 15u && (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                            ok = false;
+                            break;
+                        }
                     }
-                    uint64_t w = 0ull;
-                    if (!poll_max(slots, G, tag, tc::now_ns() + timeout, a, w)) {
-                        if (lane == 0) fail(c, a, 4u, 0x7000u + i);
-                    } else if (lane == 0) {
-                        c.win[b] = w;
+                    if (ok) {
+                        uint64_t w8[kChainRows];
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b)
+                            w8[b] = c.live[b] ? tc::ld_relaxed_u64(wm + b * kLineU64) : 0ull;
+#pragma unroll
+                        for (int b = 0; b < kChainRows; ++b) c.win[b] = w8[b];
+                    } else {
+                        fail(c, a, 4u, 0x7000u + i);
                     }
+                }
+                __syncwarp();
+            } else if (warp == 2 && lane < kChainRows && c.live[lane]) {
+                // this CTA's candidates into L2 (the winning CTA's prefetch
+                // serves every CTA's gather of a greedy row's token)
+                const uint64_t m = c.cbest[i & 1][lane];
+                const uint32_t id = unpack_id(m);
+                if (m != 0ull && id < (uint32_t)V && i + 1 < N) {
+                    const uint8_t *er = reinterpret_cast<const uint8_t *>(a.embed + (int64_t)id * RANK);
+#pragma unroll
+                    for (int o = 0; o < RANK * 2; o += 128) tc::prefetch_l2(er + o);
                 }
             }
             // the inverse-CDF weights need the maxima, but fp32(x / T) of the

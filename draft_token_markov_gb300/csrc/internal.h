@@ -16,7 +16,7 @@ constexpr int kChainThreads = 512;     // threads of a chain CTA (one CTA per SM
 constexpr int kBatchThreads = 256;
 constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
 constexpr int kKeyPad = 16;            // u64 slots per CTA-key block are padded to 128 B
-constexpr int kTcReplicas = 8;         // copies of each tcgen05-chain key slot array
+constexpr int kTcReplicas = 8;         // copies of each tcgen05-chain sum slot array
 constexpr int kLineU64 = 16;           // one 128-byte line per exchange word
 constexpr int kLineU32 = 32;
 constexpr size_t kWinMaxN = (size_t)2 * kMaxSteps * kChainRows * kLineU64;
@@ -70,7 +70,6 @@ struct SampleArgs {
     uint32_t *bar_base;        // the counter's value at the start of a launch
     uint32_t *status;          // [2]: sticky device status, where it happened
     uint32_t *call_counter;    // calls of the persistent tcgen05 chain so far
-    uint64_t *tc_keys;         // [N][8][kTcReplicas][Gp] tagged key slots of the tcgen05 chain
     uint64_t *tc_sums;         // [N][8][kTcReplicas][Gp] inverse-CDF sum slots of the tcgen05 chain
     uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
