@@ -1168,67 +1168,64 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
                     }
                 }
                 __syncthreads();
-                // each row's CTA sum tagged in its top 12 bits (below 4096 ids
-                // x 2^40): one relaxed 64-bit store carries value and epoch (no
-                // CTA reads another CTA's cache, so nothing else is ordered),
-                // into every replica of the row's slot array (a CTA polls
-                // replica cta % kTcReplicas, which spreads the polls over the
-                // L2 slices as the key slots do)
-                const uint32_t stag = tag32 & 0xFFFu;
-                if (tid < kChainRows * kTcReplicas) {
-                    const int b = tid / kTcReplicas, rep = tid % kTcReplicas;
-                    uint64_t s = 0ull;
-                    if (b < R && c.sampling[b]) {
+                // each row's CTA sum into slot (position, row, CTA), then a
+                // release-add on the position's counter, which the maxima
+                // took to G and the sums take on to 2G: once a CTA reads 2G
+                // every slot of the position holds this call's sum
+                const size_t par = (size_t)(c.call & 1u);
+                uint32_t *wc = a.win_cnt + (par * kMaxSteps + i) * kLineU32;
+                if (warp == 0) {
+                    if (lane < kChainRows) {
+                        const int b = lane;
+                        uint64_t s = 0ull;
+                        if (b < R && c.sampling[b]) {
 #pragma unroll
-                        for (int w = 0; w < kEpiThreads / 32; ++w) s += c.wsum[b][w];
-                        uint64_t *sl = a.tc_sums + (((int64_t)i * kChainRows + b) * kTcReplicas + rep) * Gp + cta;
-                        tc::st_relaxed_u64(sl, s | ((uint64_t)stag << 52));
+                            for (int w = 0; w < kEpiThreads / 32; ++w) s += c.wsum[b][w];
+                            tc::st_relaxed_u64(a.tc_sums + ((int64_t)i * kChainRows + b) * Gp + cta, s);
+                        }
+                        c.sum[b] = s;
                     }
-                    if (rep == 0) c.sum[b] = s;
+                    __syncwarp();
+                    if (lane == 0) tc::red_release_add_u32(wc, 1u);
                 }
-                // every CTA learns every row's total and its own prefix
+                // every CTA learns every row's total and its own prefix: per
+                // row one warp, whose lane 0 polls the counter and whose lanes
+                // then read the row's slots together
                 __shared__ uint64_t s_tot[kChainRows], s_pre[kChainRows];
                 if (warp < kChainRows && warp < R && c.sampling[warp]) {
                     const int b = warp;
                     const uint32_t o = (uint32_t)(c.win[b] >> 32);
                     const float M = key_from_ordered(o);
                     if (o != 0xffffffffu && !isinf(M)) {
-                        const uint64_t *sl =
-                            a.tc_sums + (((int64_t)i * kChainRows + b) * kTcReplicas + cta % kTcReplicas) * Gp;
-                        constexpr int kPer = kMaxGrid / 32;
-                        const uint64_t dl = tc::now_ns() + timeout;
                         bool ok = true;
-                        uint64_t s5[kPer];
-                        for (uint32_t spin = 0;; ++spin) {
-                            // all loads of a round in flight together
-                            uint64_t w5[kPer];
-#pragma unroll
-                            for (int u = 0; u < kPer; ++u)
-                                w5[u] = lane + 32 * u < G ? tc::ld_relaxed_u64(sl + lane + 32 * u)
-                                                          : ((uint64_t)stag << 52);
-                            bool fresh = true;
-#pragma unroll
-                            for (int u = 0; u < kPer; ++u) {
-                                fresh = fresh && (uint32_t)(w5[u] >> 52) == stag;
-                                s5[u] = w5[u] & ((1ull << 52) - 1ull);
-                            }
-                            if (__all_sync(0xffffffffu, fresh)) break;
-                            if ((spin & 15u) == 15u &&
-                                __any_sync(0xffffffffu, tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
-                                ok = false;
-                                break;
+                        if (lane == 0) {
+                            const uint64_t dl = tc::now_ns() + timeout;
+                            for (uint32_t spin = 0;; ++spin) {
+                                if ((int32_t)(ld_acquire_u32(wc) - 2u * (uint32_t)G) >= 0) break;
+                                if ((spin & 15u) == 15u && (tc::now_ns() > dl || ld_acquire_u32(a.status) != 0u)) {
+                                    ok = false;
+                                    break;
+                                }
                             }
                         }
+                        __syncwarp();
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
                         if (!ok) {
                             if (lane == 0) fail(c, a, 4u, 0x8000u + i);
                         } else {
+                            const uint64_t *sl = a.tc_sums + ((int64_t)i * kChainRows + b) * Gp;
+                            constexpr int kPer = kMaxGrid / 32;
+                            uint64_t s5[kPer];
+#pragma unroll
+                            for (int u = 0; u < kPer; ++u)
+                                s5[u] = lane + 32 * u < G ? tc::ld_relaxed_u64(sl + lane + 32 * u) : 0ull;
                             uint64_t tot = 0ull, pre = 0ull;
 #pragma unroll
                             for (int u = 0; u < kPer; ++u) {
                                 tot += s5[u];
                                 if (lane + 32 * u < cta) pre += s5[u];
                             }
-    #pragma unroll
+#pragma unroll
                             for (int o2 = 16; o2 > 0; o2 >>= 1) {
                                 tot += __shfl_xor_sync(0xffffffffu, tot, o2);
                                 pre += __shfl_xor_sync(0xffffffffu, pre, o2);

@@ -16,7 +16,6 @@ constexpr int kChainThreads = 512;     // threads of a chain CTA (one CTA per SM
 constexpr int kBatchThreads = 256;
 constexpr int kTile = 16;              // vocab ids per MMA tile (m16)
 constexpr int kKeyPad = 16;            // u64 slots per CTA-key block are padded to 128 B
-constexpr int kTcReplicas = 8;         // copies of each tcgen05-chain sum slot array
 constexpr int kLineU64 = 16;           // one 128-byte line per exchange word
 constexpr int kLineU32 = 32;
 constexpr size_t kWinMaxN = (size_t)2 * kMaxSteps * kChainRows * kLineU64;
@@ -70,13 +69,13 @@ struct SampleArgs {
     uint32_t *bar_base;        // the counter's value at the start of a launch
     uint32_t *status;          // [2]: sticky device status, where it happened
     uint32_t *call_counter;    // calls of the persistent tcgen05 chain so far
-    uint64_t *tc_sums;         // [N][8][kTcReplicas][Gp] inverse-CDF sum slots of the tcgen05 chain
-    uint32_t *sum_tags;        // [N][8][Gp] epoch tags of those sum slots
+    uint64_t *tc_sums;         // [N][8][Gp] inverse-CDF sum slots of the tcgen05 chain
     uint64_t *tok_slots;       // [N][8] inverse-CDF token slots, (id << 32) | epoch
     uint64_t *win_max;         // [2 call parities][N][8 rows] x kLineU64: red.max words
     uint64_t *bwin;            // [kMaxSteps][kMaxRows] per-position path winners (0: none)
     uint32_t *bcnt;            // [kMaxSteps][kBatchCntPerStep] its done counters
-    uint32_t *win_cnt;         // [2 call parities][N] x kLineU32: CTAs that reported
+    uint32_t *win_cnt;         // [2 call parities][N] x kLineU32: CTAs that reported (the
+                               // inverse-CDF chain counts on to 2G for its sums)
     uint64_t timeout_ns;
     int grid;                  // persistent grid size (chain) or vocab blocks (batch)
     int row_base;              // the call's row index of this launch's row 0 (row slices

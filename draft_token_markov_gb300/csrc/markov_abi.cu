@@ -32,7 +32,6 @@ struct markov_plan {
     bool batch_tc_ok = false;     // the per-position logits on the tcgen05 kernel
     int tc_grid = 0;
     uint64_t *tc_sums = nullptr;
-    uint32_t *sum_tags = nullptr;
     uint64_t *tok_slots = nullptr;
     uint64_t *win_max = nullptr;
     uint32_t *win_cnt = nullptr;
@@ -42,7 +41,6 @@ struct markov_plan {
     uint32_t *bcnt = nullptr;
     bool batch_dirty = false;
     size_t tc_slots_n = 0;
-    size_t tc_sums_n = 0;         // tc_slots_n * kTcReplicas
     CUtensorMap tmap;
     const void *tmap_head = nullptr;
     cudaStream_t side = nullptr;
@@ -84,7 +82,6 @@ void free_plan(markov_plan *p) {
     if (p->tc_sums) cudaFree(p->tc_sums);
     if (p->bwin) cudaFree(p->bwin);
     if (p->bcnt) cudaFree(p->bcnt);
-    if (p->sum_tags) cudaFree(p->sum_tags);
     if (p->tok_slots) cudaFree(p->tok_slots);
     if (p->win_max) cudaFree(p->win_max);
     if (p->win_cnt) cudaFree(p->win_cnt);
@@ -213,13 +210,11 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
     if (p->tc_ok && noise_bytes < bound_bytes) noise_bytes = bound_bytes;
     const int Gtc = p->tc_grid > 0 ? p->tc_grid : 1;
     p->tc_slots_n = (size_t)kMaxSteps * kChainRows * ((Gtc + kKeyPad - 1) / kKeyPad * kKeyPad);
-    p->tc_sums_n = p->tc_slots_n * kTcReplicas;
     if (cudaMalloc(&p->noise, noise_bytes) != cudaSuccess ||
         cudaMalloc(&p->keys, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->sums, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->ctrl, 8 * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMalloc(&p->tc_sums, p->tc_sums_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMalloc(&p->sum_tags, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMalloc(&p->tc_sums, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->tok_slots, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->win_max, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMalloc(&p->win_cnt, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
@@ -229,8 +224,7 @@ markov_status markov_plan_create(const markov_desc *desc, markov_plan **out) {
         cudaMalloc(&p->bcnt, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->bwin, 0, kBatchWinN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->bcnt, 0, kBatchCntN * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(p->tc_sums, 0, p->tc_sums_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->keys, 0, p->keys_n * sizeof(uint64_t)) != cudaSuccess ||
@@ -396,7 +390,6 @@ markov_status markov_chain_sample_typed(markov_plan *p, const void *base_logits,
     a.status = p->ctrl + 2;
     a.call_counter = p->ctrl + 4;
     a.tc_sums = p->tc_sums;
-    a.sum_tags = p->sum_tags;
     a.tok_slots = p->tok_slots;
     a.win_max = p->win_max;
     a.win_cnt = p->win_cnt;
@@ -486,8 +479,7 @@ markov_status markov_plan_status(markov_plan *p) {
     // a launch gave up: clear the status, restart the barrier and call
     // counters, and forget every tagged exchange slot
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
-        cudaMemset(p->tc_sums, 0, p->tc_sums_n * sizeof(uint64_t)) != cudaSuccess ||
-        cudaMemset(p->sum_tags, 0, p->tc_slots_n * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_max, 0, kWinMaxN * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->win_cnt, 0, kWinCntN * sizeof(uint32_t)) != cudaSuccess ||
