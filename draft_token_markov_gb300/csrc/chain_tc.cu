@@ -69,7 +69,8 @@ constexpr uint32_t kDynSmem = kSmemHead + kSmemB + 1024;   // + alignment slack
 struct Ctl {
     uint64_t full[kSmemChunks];      // TMA landed in slot s
     uint64_t cpdone[kSmemChunks];    // slot s copied into TMEM
-    uint64_t dfull[2];               // accumulator b holds a finished tile
+    uint64_t dfull[2][2];            // accumulator b holds a finished tile (index 1: the
+                                     // odd tiles when the epilogue halves take turns)
     uint64_t dfree[2];               // accumulator b read out by its epilogue
     uint64_t fin[2];                 // issuer b's MMAs all complete (exit)
     uint64_t bstaged;                // the next position's B operand is staged
@@ -257,7 +258,7 @@ template <int RANK>
 __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const uint32_t tmem, const int W,
                                             const int i, const int nt, const int ntm,
                                             const uint32_t b_sa, const uint32_t head_sa,
-                                            const uint64_t timeout, uint32_t &uses) {
+                                            const uint64_t timeout, const bool alt, uint32_t &uses) {
     constexpr int cpt = RANK / 64;
     const int lane = threadIdx.x & 31;
     const uint32_t d = tmem + kDCol + 16u * (uint32_t)W;
@@ -320,7 +321,7 @@ __device__ __forceinline__ void issue_tiles(Ctl &c, const SampleArgs &a, const u
             }
         }
         if (!ok) break;
-        tc::commit_elect(tc::smem_u32(&c.dfull[W]));
+        tc::commit_elect(tc::smem_u32(&c.dfull[W][alt ? ((k - W) >> 1) & 1 : 0]));
         ++uses;
     }
     __syncwarp();
@@ -416,7 +417,13 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     constexpr int kTilesWG = (kMaxChunks / cpt + 1) / 2;   // tiles per group, at most
     constexpr bool kRegs = kTilesWG <= 4;                  // pass-2 tiles kept in registers
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1, rb = kRowsT * hr;
+    const int ew = warp - 4, wg = ew >> 3, q = warp & 3, hr = (ew >> 2) & 1;
+    // inverse-CDF calls of at most 4 rows: the warps of both row halves take
+    // rows 0-3 of the group's tiles in turn (half hr the tiles wg + 2 u with
+    // u % 2 == hr, their own full barrier and 4 hand-back arrivals a tile)
+    // instead of the second half idling while the first does every tile
+    const bool alt = kCdf && a.rows <= kRowsT;
+    const int rb = alt ? 0 : kRowsT * hr;
     const int V = a.V;
     const int par = i & 1;
     uint32_t live_m = 0u, samp_m = 0u, div_m = 0u;   // this thread's 4 rows, bit j = row rb + j
@@ -467,7 +474,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                         : 0u;
         qq = (ok2 && gum_m != 0u) ? __ldcg(gq + 2 * v) : 0u;
     };
-    load_tile(wg, nb, nq);
+    load_tile(alt ? wg + 2 * hr : wg, nb, nq);
     bool ok = true;
     if (nts >= 0 && wg == 1) {
         // group 1, before its first tile: the bias of tile nts, 16 ids per
@@ -488,11 +495,12 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
     int ntw = 0;   // tiles this warp processed
 #pragma unroll 1
     for (int k = wg; k < nt; k += 2) {
+        if (alt && (((k - wg) >> 1) & 1) != hr) continue;
         uint32_t cb[kRowsT];
 #pragma unroll
         for (int j = 0; j < kRowsT; ++j) cb[j] = nb[j];
         const uint32_t cq = nq;
-        load_tile(k + 2, nb, nq);
+        load_tile(alt ? k + 4 : k + 2, nb, nq);
         if (__shfl_sync(0xffffffffu, lane == 0 ? aborted(c, a) : false, 0)) {
             ok = false;
             break;
@@ -514,7 +522,7 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
             r[3] = __float_as_uint(sb.w);
         } else {
             if (lane == 0)
-                ok = tc::mbar_wait_for(tc::smem_u32(&c.dfull[wg]), dcount & 1u, timeout);
+                ok = tc::mbar_wait_for(tc::smem_u32(&c.dfull[wg][alt ? hr : 0]), dcount & 1u, timeout);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0) fail(c, a, 4u, 0x6000u + i);
@@ -726,6 +734,8 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
     const int v_begin = t0 * 128;
     const int v_end = t1 * 128 < V ? t1 * 128 : V;
     const int Gp = (G + kKeyPad - 1) / kKeyPad * kKeyPad;
+    // the epilogue halves take the tiles in turn (inverse CDF, at most 4 rows)
+    const bool alt = MODE == 1 && R <= kRowsT;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
@@ -734,8 +744,9 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
             tc::mbar_init(tc::smem_u32(&c.cpdone[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(tc::smem_u32(&c.dfull[b]), 1);
-            tc::mbar_init(tc::smem_u32(&c.dfree[b]), kEpiWarps / 2);
+            tc::mbar_init(tc::smem_u32(&c.dfull[b][0]), 1);
+            tc::mbar_init(tc::smem_u32(&c.dfull[b][1]), 1);
+            tc::mbar_init(tc::smem_u32(&c.dfree[b]), alt ? kEpiWarps / 4 : kEpiWarps / 2);
             tc::mbar_init(tc::smem_u32(&c.fin[b]), 1);
         }
         tc::mbar_init(tc::smem_u32(&c.bstaged), 1);
@@ -818,7 +829,7 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
         const int nts = (MODE == 0 && RANK == 256 && nt == kMaxChunks / cpt && i > 0) ? nt - 1 : -1;
         // ------------------------------------- phase A: MMA and epilogue
         if (warp < 2) {
-            issue_tiles<RANK>(c, a, tmem, warp, i, nts >= 0 ? nts : nt, ntm, b_sa, head_sa, timeout, uses);
+            issue_tiles<RANK>(c, a, tmem, warp, i, nts >= 0 ? nts : nt, ntm, b_sa, head_sa, timeout, alt, uses);
         } else if (warp < 4 && i > 0) {
             // warps 2 and 3 after the head load: the next position's base
             // logits into L2, off the chain's critical path
@@ -915,7 +926,6 @@ chain_tc_kernel(const SampleArgs a, const __grid_constant__ CUtensorMap tmap, in
 
         // ------------------------------- phase B: agree on every row's winner
         const uint32_t epoch = c.call * (uint32_t)kMaxSteps + (uint32_t)i + 1u;
-        const uint32_t tag = epoch & 0x3FFFu;
         if (MODE == 0) {
             // Gumbel and greedy rows: warp 0 reports this CTA's best key per
             // row and collects the winners; warps 0-3 stage the winners'
