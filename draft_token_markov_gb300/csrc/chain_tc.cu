@@ -227,9 +227,8 @@ __device__ __forceinline__ void prefetch_base(const Ctl &c, const SampleArgs &a,
     }
 }
 
-// The output-logit transform of two packed cached logits (out of line: only
-// soft-capped heads take it, and its tanh is long).
-__device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf) {
+// The output-logit transform of two packed cached logits.
+__device__ __forceinline__ uint32_t transform_pair_inl(uint32_t lp, const Transform &tf) {
     float y0 = __fmul_rn(__uint_as_float(lp << 16), tf.mult);
     float y1 = __fmul_rn(__uint_as_float(lp & 0xffff0000u), tf.mult);
     if (tf.has_cap) {
@@ -237,6 +236,13 @@ __device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf
         y1 = __fmul_rn(tf.cap, dm_tanh(__fmul_rn(y1, tf.inv_cap)));
     }
     return bf16x2_rn(y0, y1);
+}
+
+// The same out of line, for the Gumbel kernels (whose code is large already;
+// the inverse-CDF kernels take it inline, where the two pairs' tanh chains
+// overlap).
+__device__ __noinline__ uint32_t transform_pair(uint32_t lp, const Transform &tf) {
+    return transform_pair_inl(lp, tf);
 }
 
 // The output-logit transform of one fp32 logit, kept in fp32 (fp32 caches).
@@ -571,8 +577,13 @@ __device__ __forceinline__ void epilogue(Ctl &c, const SampleArgs &a, const uint
                 if (valid && ((live_m >> j) & 1u)) cache_fi[j * a.cache_s0 + v] = lf4[j];
         } else {
             if (a.tf.has_transform) {
-                lp[0] = transform_pair(lp[0], a.tf);
-                lp[1] = transform_pair(lp[1], a.tf);
+                if (kCdf) {
+                    lp[0] = transform_pair_inl(lp[0], a.tf);
+                    lp[1] = transform_pair_inl(lp[1], a.tf);
+                } else {
+                    lp[0] = transform_pair(lp[0], a.tf);
+                    lp[1] = transform_pair(lp[1], a.tf);
+                }
             }
 #pragma unroll
             for (int j = 0; j < kRowsT; ++j) {
