@@ -26,10 +26,12 @@
 //          each exchange this CTA's candidate embedding rows into L2
 //   3      lane 0: copies the TMEM-resident chunks from their shared-memory
 //          staging slot into TMEM (position 0 only); later: base prefetch
-//   4-19   the epilogue (warps 4-11 accumulator 0, 12-19 accumulator 1); at
-//          position 0, before it, the noise bounds of position 0 while the
-//          head streams in; after every position, the next position's
-//          noise bounds while the winners are exchanged
+//   4-19   the epilogue (warps 4-11 accumulator 0, 12-19 accumulator 1;
+//          inverse-CDF calls of at most 4 rows: the two row halves of each
+//          accumulator's warps take its tiles in turn); at position 0,
+//          before it, the noise bounds of position 0 while the head streams
+//          in; after every position, the next position's noise bounds while
+//          the winners are exchanged
 //   0-3    after each position: warp 0 exchanges every row's key with the
 //          other CTAs, and warps 0-3 stage markov_embed[token] of rows w and
 //          w + 4 as the next position's B operand
@@ -37,8 +39,10 @@
 // best key into one word per (position, row) with red.max and then adds 1
 // to the position's counter (release); one thread per CTA polls the
 // counter (acquire, bounded) until all CTAs have counted and reads the
-// winners.  Inverse-CDF rows keep per-CTA slots tagged with the position
-// epoch (maximum, then sums and the owner's scan).
+// winners.  Inverse-CDF rows take their maxima the same way, then count
+// their per-CTA weight sums (one slot per CTA) on the same counter up to 2G;
+// the CTA whose prefix range holds the target scans for the token and
+// publishes it in a word tagged with the call's epoch.
 
 #include <cuda.h>
 #include <cuda_fp16.h>

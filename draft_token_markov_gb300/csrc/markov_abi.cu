@@ -27,7 +27,7 @@ struct markov_plan {
     uint32_t *ctrl = nullptr;     // [0] barrier count, [1] barrier base, [2..3] status,
                                   // [4] call counter of the tcgen05 chain
     size_t keys_n = 0;
-    // the tcgen05 chain: tagged exchange slots and the head's TMA descriptor
+    // the tcgen05 chain: exchange slots and words, and the head's TMA descriptor
     bool tc_ok = false;
     bool batch_tc_ok = false;     // the per-position logits on the tcgen05 kernel
     int tc_grid = 0;
@@ -477,7 +477,7 @@ markov_status markov_plan_status(markov_plan *p) {
         return MARKOV_ECUDA;
     if (ctrl[2] == 0u) return MARKOV_OK;
     // a launch gave up: clear the status, restart the barrier and call
-    // counters, and forget every tagged exchange slot
+    // counters, and clear every exchange slot and word
     if (cudaMemset(p->ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess ||
         cudaMemset(p->tc_sums, 0, p->tc_slots_n * sizeof(uint64_t)) != cudaSuccess ||
         cudaMemset(p->tok_slots, 0, (size_t)kMaxSteps * kChainRows * sizeof(uint64_t)) != cudaSuccess ||
