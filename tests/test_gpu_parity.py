@@ -251,6 +251,35 @@ def test_tcgen05_chain_takes_the_chain_workloads(gpu_lib):
         plan.close()
 
 
+# Inverse-CDF calls of at most 4 rows, where the two row halves of the
+# tcgen05 chain's epilogue warps take each accumulator's tiles in turn:
+# vocabularies with 5 to 11 tiles per CTA (odd and even counts per
+# accumulator, ragged last tiles), every rank, greedy and sampling rows, a
+# padding row, the soft cap with a tie and a NaN row; and 5 rows, where the
+# halves split the rows again.
+TURNS = [
+    W.small(107088, 64, 1, 3, W.INVCDF, seed=13, temperatures=(0.7,)),
+    W.small(107088, 128, 2, 2, W.INVCDF, seed=14, temperatures=(0.0, 0.6)),
+    W.small(129264, 256, 3, 2, W.INVCDF, seed=15, mult=0.5, cap=30.0, tie_row=1, nan_row=2,
+            temperatures=(0.7, 1.0)),
+    W.small(200016, 128, 4, 2, W.INVCDF, seed=16, padding_rows=(2,), temperatures=(0.5, 1.2)),
+    W.small(107088, 128, 5, 2, W.INVCDF, seed=17, temperatures=(0.0, 0.7, 1.0)),
+]
+
+
+@pytest.mark.parametrize("w", TURNS, ids=_ids(TURNS))
+def test_inverse_cdf_epilogue_turns(gpu_lib, w):
+    plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, w.rows)
+    try:
+        inp = W.make_call(w)
+        toks, cache = U.run(gpu_lib, w, inp, CHAIN, plan=plan)
+        assert plan.query(gpu_lib.Q_LAST_PATH) == CHAIN
+        rep = U.check(w, inp, toks, cache)
+        assert rep.ok(), rep.summary()
+    finally:
+        plan.close()
+
+
 def test_bad_arguments_launch_nothing(gpu_lib):
     w = W.TINY
     plan = gpu_lib.Plan(w.vocab, w.rank, w.steps, 4)
